@@ -1,0 +1,18 @@
+"""CPU float64 oracle for Jagged Flash Attention.
+
+Test infrastructure: imported only by the tests, the package smoke check and the
+benchmark's CPU-baseline leg.  The library never routes through it.
+"""
+from .jfa_oracle import (  # noqa: F401
+    causal_visible,
+    jagged_backward,
+    jagged_forward,
+    padded_dense_forward,
+    relpos_bias,
+    sequence_backward,
+    sequence_forward,
+    sequence_reference,
+    softmax_rows,
+    tiled_subtraction_forward,
+    to_f64,
+)

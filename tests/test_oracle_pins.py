@@ -1,0 +1,403 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+* hand-derived worked examples (tests/golden), closed forms;
+* brute-force padded dense attention with a -inf mask;
+* torch's own float64 scaled_dot_product_attention (forward and autograd);
+* central finite differences of the backward;
+* invariants of softmax attention;
+* the tiled online softmax with the subtraction correction ("Jagged Flash
+  Attention (JFA)", "Four generations" item 1) reproduces exact attention;
+* planted mistakes in the oracle are caught by these pins.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.jfa_oracle as orc
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def rand_batch(rng, lq, lk, H=2, d=8, bias_buckets=0, scale_vals=1.0):
+    lq, lk = np.asarray(lq), np.asarray(lk)
+    qo = np.concatenate([[0], np.cumsum(lq)]).astype(np.int64)
+    ko = np.concatenate([[0], np.cumsum(lk)]).astype(np.int64)
+    q = rng.standard_normal((qo[-1], H, d)) * scale_vals
+    k = rng.standard_normal((ko[-1], H, d)) * scale_vals
+    v = rng.standard_normal((ko[-1], H, d))
+    do = rng.standard_normal((qo[-1], H, d))
+    bt = rng.standard_normal((H, bias_buckets)) * 0.5 if bias_buckets else None
+    return q, k, v, do, qo, ko, bt
+
+
+CASES = [
+    # (lq, lk, causal, bias)
+    ([3, 1, 5], [3, 1, 5], False, False),
+    ([3, 1, 5], [3, 1, 5], True, False),
+    ([4, 2, 6], [7, 1, 3], False, True),
+    ([4, 2, 6], [7, 1, 3], True, True),
+    ([0, 5, 2], [4, 0, 2], False, False),
+    ([0, 5, 2, 3], [4, 0, 2, 3], True, True),
+]
+
+
+# --------------------------------------------------------------------------- golden
+def _ev(x):
+    return eval(x, {"__builtins__": {}}, {"log": math.log}) if isinstance(x, str) else x
+
+
+def _arr(x):
+    if x is None:
+        return None
+    return np.vectorize(_ev, otypes=[np.float64])(np.array(x, dtype=object))
+
+
+@pytest.mark.parametrize("case", json.load(open(os.path.join(HERE, "golden", "worked_examples.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_worked_examples(case):
+    q, k, v, do = (_arr(case[n]) for n in ("q", "k", "v", "dout"))
+    bt = _arr(case["bias_table"])
+    args = dict(scale=_ev(case["scale"]), causal=case["causal"], bias_table=bt,
+                bias_center=case["bias_center"])
+    out, lse = orc.jagged_forward(q, k, v, case["q_offsets"], case["kv_offsets"], **args)
+    np.testing.assert_allclose(out, _arr(case["out"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, _arr(case["lse"]), rtol=0, atol=1e-13)
+    dq, dk, dv = orc.jagged_backward(do, q, k, v, case["q_offsets"], case["kv_offsets"], **args)
+    np.testing.assert_allclose(dq, _arr(case["dq"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, _arr(case["dk"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, _arr(case["dv"]), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- brute force
+@pytest.mark.parametrize("lq,lk,causal,bias", CASES)
+def test_matches_padded_dense(lq, lk, causal, bias):
+    rng = np.random.default_rng(1)
+    q, k, v, _, qo, ko, bt = rand_batch(rng, lq, lk, bias_buckets=16 if bias else 0)
+    kw = dict(scale=0.37, causal=causal, bias_table=bt, bias_center=8)
+    o1, l1 = orc.jagged_forward(q, k, v, qo, ko, **kw)
+    o2, l2 = orc.padded_dense_forward(q, k, v, qo, ko, **kw)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    fin = np.isfinite(l2)
+    assert np.array_equal(fin, np.isfinite(l1))
+    np.testing.assert_allclose(l1[fin], l2[fin], rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- library
+def _sdpa_seq(qb, kb, vb, scale, mask):
+    """torch float64 SDPA for one sequence, one head; mask bool [Lq, Lk] (True = visible)
+    or a float additive matrix, or None."""
+    t = lambda a: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    Q, K, V = t(qb[None, None]), t(kb[None, None]), t(vb[None, None])
+    attn_mask = None if mask is None else torch.tensor(mask)[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=attn_mask, scale=scale)
+    return Q, K, V, o
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lq,Lk", [(5, 5), (3, 7), (6, 6), (1, 4)])
+def test_matches_torch_sdpa_fwd_bwd(causal, Lq, Lk):
+    rng = np.random.default_rng(2)
+    d, scale = 6, 0.41
+    qb, kb, vb, dob = (rng.standard_normal((n, d)) for n in (Lq, Lk, Lk, Lq))
+    mask = torch.ones(Lq, Lk, dtype=torch.bool).tril(diagonal=Lk - Lq).numpy() if causal else None
+    Q, K, V, o = _sdpa_seq(qb, kb, vb, scale, mask)
+    o.backward(torch.tensor(dob)[None, None])
+    vis = orc.causal_visible(Lq, Lk) if causal else None
+    o_ref, _ = orc.sequence_forward(qb, kb, vb, scale, None, vis)
+    np.testing.assert_allclose(o_ref, o.detach()[0, 0].numpy(), rtol=0, atol=1e-12)
+    dq, dk, dv = orc.sequence_backward(dob, qb, kb, vb, scale, None, vis)
+    np.testing.assert_allclose(dq, Q.grad[0, 0].numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, K.grad[0, 0].numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, V.grad[0, 0].numpy(), rtol=0, atol=1e-12)
+
+
+def test_additive_bias_matches_torch_float_mask():
+    rng = np.random.default_rng(3)
+    Lq, Lk, d, scale = 4, 6, 5, 0.3
+    qb, kb, vb, dob = (rng.standard_normal((n, d)) for n in (Lq, Lk, Lk, Lq))
+    bias = rng.standard_normal((Lq, Lk))
+    Q, K, V, o = _sdpa_seq(qb, kb, vb, scale, bias)
+    o.backward(torch.tensor(dob)[None, None])
+    o_ref, lse = orc.sequence_forward(qb, kb, vb, scale, bias, None)
+    np.testing.assert_allclose(o_ref, o.detach()[0, 0].numpy(), rtol=0, atol=1e-12)
+    dq, dk, dv = orc.sequence_backward(dob, qb, kb, vb, scale, bias, None)
+    np.testing.assert_allclose(dq, Q.grad[0, 0].numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, K.grad[0, 0].numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, V.grad[0, 0].numpy(), rtol=0, atol=1e-12)
+    # lse is the natural log-sum-exp of the scaled, biased scores
+    ref = torch.logsumexp(torch.tensor(scale * qb @ kb.T + bias), dim=1).numpy()
+    np.testing.assert_allclose(lse, ref, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- finite differences
+def _objective(q, k, v, do, qo, ko, kw):
+    out, _ = orc.jagged_forward(q, k, v, qo, ko, **kw)
+    return float(np.sum(do * out))
+
+
+@pytest.mark.parametrize("lq,lk,causal,bias", [
+    ([2, 5], [3, 4], False, True),
+    ([4, 3], [2, 3], True, True),
+    ([3, 1], [3, 1], True, False),
+])
+def test_backward_finite_differences(lq, lk, causal, bias):
+    rng = np.random.default_rng(4)
+    q, k, v, do, qo, ko, bt = rand_batch(rng, lq, lk, H=2, d=4, bias_buckets=12 if bias else 0)
+    kw = dict(scale=0.7, causal=causal, bias_table=bt, bias_center=6)
+    grads = orc.jagged_backward(do, q, k, v, qo, ko, **kw)
+    eps = 1e-6
+    for which, g in zip(range(3), grads):
+        num = np.zeros_like(g)
+        base = [q, k, v]
+        it = np.nditer(base[which], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [a.copy() for a in base]
+            minus = [a.copy() for a in base]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            num[idx] = (_objective(*plus, do, qo, ko, kw) - _objective(*minus, do, qo, ko, kw)) / (2 * eps)
+        rel = np.linalg.norm(num - g) / max(np.linalg.norm(g), 1e-30)
+        assert rel <= 1e-7, (which, rel)
+
+
+# --------------------------------------------------------------------------- invariants
+def test_rows_sum_to_one_and_D_identity():
+    rng = np.random.default_rng(5)
+    Lq, Lk, d = 5, 9, 4
+    qb, kb, vb, dob = (rng.standard_normal((n, d)) for n in (Lq, Lk, Lk, Lq))
+    vis = orc.causal_visible(Lq, Lk)
+    s = orc.sequence_scores(qb, kb, 0.5, None, vis)
+    p, _ = orc.softmax_rows(s)
+    np.testing.assert_allclose(p.sum(1), 1.0, atol=1e-14)
+    assert np.all(p[~vis] == 0)
+    o = p @ vb
+    dp = dob @ vb.T
+    np.testing.assert_allclose((dob * o).sum(1), (p * dp).sum(1), atol=1e-13)
+
+
+def test_constant_v_gives_constant_output():
+    rng = np.random.default_rng(6)
+    q, k, v, _, qo, ko, bt = rand_batch(rng, [3, 7], [5, 2], bias_buckets=16)
+    c = rng.standard_normal(v.shape[1:])
+    v[:] = c
+    out, _ = orc.jagged_forward(q, k, v, qo, ko, 0.8, causal=False, bias_table=bt, bias_center=8)
+    np.testing.assert_allclose(out, np.broadcast_to(c, out.shape), atol=1e-13)
+
+
+def test_single_key_closed_form():
+    rng = np.random.default_rng(7)
+    Lq, d, scale = 4, 5, 0.3
+    qb, dob = rng.standard_normal((Lq, d)), rng.standard_normal((Lq, d))
+    kb, vb = rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    o, lse = orc.sequence_forward(qb, kb, vb, scale)
+    np.testing.assert_allclose(o, np.repeat(vb, Lq, 0), atol=1e-14)
+    np.testing.assert_allclose(lse, scale * (qb @ kb[0]), atol=1e-14)
+    dq, dk, dv = orc.sequence_backward(dob, qb, kb, vb, scale)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+    np.testing.assert_allclose(dv[0], dob.sum(0), atol=1e-13)
+
+
+def test_key_permutation_invariance():
+    rng = np.random.default_rng(8)
+    Lq, Lk, d = 4, 9, 6
+    qb, kb, vb = (rng.standard_normal((n, d)) for n in (Lq, Lk, Lk))
+    bias = rng.standard_normal((Lq, Lk))
+    perm = rng.permutation(Lk)
+    o1, l1 = orc.sequence_forward(qb, kb, vb, 0.5, bias)
+    o2, l2 = orc.sequence_forward(qb, kb[perm], vb[perm], 0.5, bias[:, perm])
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_sequence_permutation_and_duplication():
+    rng = np.random.default_rng(9)
+    lq, lk = [3, 5, 2], [4, 1, 6]
+    q, k, v, _, qo, ko, bt = rand_batch(rng, lq, lk, bias_buckets=16)
+    kw = dict(scale=0.6, causal=True, bias_table=bt, bias_center=8)
+    o, l = orc.jagged_forward(q, k, v, qo, ko, **kw)
+    order = [2, 0, 2, 1]
+    cat = lambda x, off: np.concatenate([x[off[b]:off[b + 1]] for b in order])
+    lq2 = [lq[b] for b in order]
+    lk2 = [lk[b] for b in order]
+    qo2 = np.concatenate([[0], np.cumsum(lq2)])
+    ko2 = np.concatenate([[0], np.cumsum(lk2)])
+    o2, l2 = orc.jagged_forward(cat(q, qo), cat(k, ko), cat(v, ko), qo2, ko2, **kw)
+    np.testing.assert_allclose(o2, cat(o, qo), atol=1e-14)
+    np.testing.assert_allclose(l2, np.concatenate([l[:, qo[b]:qo[b + 1]] for b in order], 1), atol=1e-14)
+
+
+def test_zero_scale_gives_mean_of_visible_values():
+    rng = np.random.default_rng(10)
+    Lq, Lk, d = 3, 5, 4
+    qb, kb, vb = (rng.standard_normal((n, d)) for n in (Lq, Lk, Lk))
+    o, lse = orc.sequence_forward(qb, kb, vb, 0.0)
+    np.testing.assert_allclose(o, np.repeat(vb.mean(0, keepdims=True), Lq, 0), atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(Lk), atol=1e-14)
+    vis = orc.causal_visible(Lq, Lk)    # row i sees the first i + 3 keys
+    o, lse = orc.sequence_forward(qb, kb, vb, 0.0, None, vis)
+    for i in range(Lq):
+        np.testing.assert_allclose(o[i], vb[:i + 3].mean(0), atol=1e-14)
+        assert abs(lse[i] - math.log(i + 3)) < 1e-14
+
+
+def test_constant_bias_shifts_only_lse():
+    rng = np.random.default_rng(11)
+    q, k, v, _, qo, ko, _ = rand_batch(rng, [4, 3], [6, 2])
+    bt = np.full((2, 16), 1.75)
+    o1, l1 = orc.jagged_forward(q, k, v, qo, ko, 0.5)
+    o2, l2 = orc.jagged_forward(q, k, v, qo, ko, 0.5, bias_table=bt, bias_center=8)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l2 - l1, 1.75, atol=1e-13)
+
+
+@pytest.mark.parametrize("delta", [-2, 0, 1, 3])
+def test_one_hot_bias_selects_relative_position(delta):
+    """A dominant bias at bucket center+delta makes query i attend to key i+delta
+    (bucket = j - i + center): pins the sign, the index and the center."""
+    rng = np.random.default_rng(12)
+    L, d, center = 7, 3, 10
+    q, k, v, _, qo, ko, _ = rand_batch(rng, [L], [L], H=1, d=d)
+    bt = np.zeros((1, 21))
+    bt[0, center + delta] = 200.0
+    out, lse = orc.jagged_forward(q, k, v, qo, ko, 0.1, bias_table=bt, bias_center=center)
+    for i in range(L):
+        j = i + delta
+        if 0 <= j < L:
+            np.testing.assert_allclose(out[i, 0], v[j, 0], atol=1e-12)
+
+
+def test_bias_bucket_clamps_at_table_edges():
+    rng = np.random.default_rng(13)
+    L, center = 9, 2
+    q, k, v, _, qo, ko, _ = rand_batch(rng, [L], [L], H=1, d=2)
+    bt = np.zeros((1, 5))
+    bt[0, 4] = 300.0     # last bucket: every j - i + 2 >= 4, i.e. j >= i + 2
+    out, _ = orc.jagged_forward(q, k, v, qo, ko, 0.0, bias_table=bt, bias_center=center)
+    for i in range(L):
+        js = [j for j in range(L) if j - i + center >= 4]
+        if js:
+            np.testing.assert_allclose(out[i, 0], v[js, 0].mean(0), atol=1e-12)
+
+
+def test_causal_bottom_right_closed_forms():
+    rng = np.random.default_rng(14)
+    d, scale = 3, 0.9
+    # Lq > Lk: the first Lq - Lk rows see nothing.
+    qb, kb, vb, dob = rng.standard_normal((3, d)), rng.standard_normal((1, d)), \
+        rng.standard_normal((1, d)), rng.standard_normal((3, d))
+    vis = orc.causal_visible(3, 1)
+    o, lse = orc.sequence_forward(qb, kb, vb, scale, None, vis)
+    assert np.all(o[:2] == 0) and np.all(np.isneginf(lse[:2]))
+    np.testing.assert_allclose(o[2], vb[0], atol=1e-14)
+    np.testing.assert_allclose(lse[2], scale * qb[2] @ kb[0], atol=1e-14)
+    dq, dk, dv = orc.sequence_backward(dob, qb, kb, vb, scale, None, vis)
+    assert np.all(dq[:2] == 0)
+    np.testing.assert_allclose(dv[0], dob[2], atol=1e-14)
+    # Lq < Lk: the last query row sees every key, exactly like non-causal.
+    qb, kb, vb = rng.standard_normal((2, d)), rng.standard_normal((5, d)), rng.standard_normal((5, d))
+    o_c, _ = orc.sequence_forward(qb, kb, vb, scale, None, orc.causal_visible(2, 5))
+    o_n, _ = orc.sequence_forward(qb, kb, vb, scale)
+    np.testing.assert_allclose(o_c[1], o_n[1], atol=1e-14)
+    o_first, _ = orc.sequence_forward(qb[:1], kb[:4], vb[:4], scale)
+    np.testing.assert_allclose(o_c[0], o_first[0], atol=1e-14)
+
+
+def test_empty_sequences():
+    rng = np.random.default_rng(15)
+    q, k, v, do, qo, ko, _ = rand_batch(rng, [0, 3, 2], [2, 0, 3])
+    out, lse = orc.jagged_forward(q, k, v, qo, ko, 0.5)
+    assert np.all(out[0:3] == 0) and np.all(np.isneginf(lse[:, 0:3]))
+    dq, dk, dv = orc.jagged_backward(do, q, k, v, qo, ko, 0.5)
+    assert np.all(dq[0:3] == 0)
+    assert np.all(dk[0:2] == 0) and np.all(dv[0:2] == 0)   # keys of seq 0 have no queries
+
+
+def test_offsets_validation():
+    q = np.zeros((3, 1, 2))
+    with pytest.raises(ValueError):
+        orc.jagged_forward(q, q, q, [0, 2, 1], [0, 1, 3], 1.0)
+    with pytest.raises(ValueError):
+        orc.jagged_forward(q, q, q, [1, 3], [0, 3], 1.0)
+
+
+# --------------------------------------------------------------------------- subtraction scheme
+@pytest.mark.parametrize("lq,lk,causal,bias", [
+    ([1, 127, 128, 129], [1, 127, 128, 129], False, False),
+    ([129, 3], [257, 255], False, True),
+    ([130, 5], [130, 5], True, True),
+    ([40, 200], [300, 7], True, False),
+    ([0, 2, 3], [5, 0, 256], False, False),
+])
+def test_subtraction_scheme_is_exact(lq, lk, causal, bias):
+    rng = np.random.default_rng(16)
+    q, k, v, _, qo, ko, bt = rand_batch(rng, lq, lk, H=1, d=8, bias_buckets=1024 if bias else 0)
+    kw = dict(scale=0.35, causal=causal, bias_table=bt, bias_center=512)
+    o1, l1 = orc.jagged_forward(q, k, v, qo, ko, **kw)
+    o2, l2 = orc.tiled_subtraction_forward(q, k, v, qo, ko, **kw)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    fin = np.isfinite(l1)
+    assert np.array_equal(fin, np.isfinite(l2))
+    np.testing.assert_allclose(l2[fin], l1[fin], rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- planted mistakes
+def _pins_pass(fn):
+    try:
+        fn()
+        return True
+    except AssertionError:
+        return False
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    golden = json.load(open(os.path.join(HERE, "golden", "worked_examples.json")))["cases"]
+
+    def all_pins():
+        for c in golden:
+            test_worked_examples(c)
+        for delta in (-2, 1):
+            test_one_hot_bias_selects_relative_position(delta)
+        test_backward_finite_differences([2, 5], [3, 4], False, True)
+        test_causal_bottom_right_closed_forms()
+        test_matches_torch_sdpa_fwd_bwd(True, 3, 7)
+
+    assert _pins_pass(all_pins)
+
+    orig_bias = orc.relpos_bias
+    orig_vis = orc.causal_visible
+    orig_bwd = orc.sequence_backward
+    orig_scores = orc.sequence_scores
+
+    mutants = {
+        "bias index i - j": lambda: monkeypatch.setattr(
+            orc, "relpos_bias", lambda t, Lq, Lk, c: orig_bias(t, Lk, Lq, c).T if Lq and Lk else orig_bias(t, Lq, Lk, c)),
+        "top-left causal": lambda: monkeypatch.setattr(
+            orc, "causal_visible", lambda Lq, Lk: np.arange(Lk)[None, :] <= np.arange(Lq)[:, None]),
+        "dK without scale": lambda: monkeypatch.setattr(
+            orc, "sequence_backward",
+            lambda do, q, k, v, s, b=None, vis=None: (lambda g: (g[0], g[1] / s if s else g[1], g[2]))(
+                orig_bwd(do, q, k, v, s, b, vis))),
+        "bias scaled too": lambda: monkeypatch.setattr(
+            orc, "sequence_scores",
+            lambda q, k, s, b=None, vis=None: orig_scores(q, k, s, None if b is None else s * b, vis)),
+        "dropped D term": lambda: monkeypatch.setattr(
+            orc, "sequence_backward",
+            lambda do, q, k, v, s, b=None, vis=None: _bwd_without_D(orig_scores, do, q, k, v, s, b, vis)),
+    }
+    for name, plant in mutants.items():
+        monkeypatch.undo()
+        plant()
+        assert not _pins_pass(all_pins), f"planted mistake not caught: {name}"
+    monkeypatch.undo()
+    assert _pins_pass(all_pins)
+
+
+def _bwd_without_D(scores, do, q, k, v, s, b, vis):
+    p, _ = orc.softmax_rows(scores(q, k, s, b, vis))
+    ds = p * (do @ v.T)
+    return s * ds @ k, s * ds.T @ q, p.T @ do
