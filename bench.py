@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Jagged Flash Attention benchmark on GB300.
+
+One step = the whole hot path on one synthetic jagged batch: planner + forward,
+then planner + preprocess + dK/dV pass + dQ pass (jfa_forward + jfa_backward).
+Metric: valid-token TFLOPS (bf16), forward+backward, counting only the (query, key)
+pairs the attention visits: fwd 4*d*H*P, bwd 10*d*H*P flops, P = sum_b Lq_b*Lk_b
+(causal: the visible pairs).  Inputs are resident in HBM for `value`; `e2e` times
+the same step through the public call with pinned host buffers copied in and the
+results copied out every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl jfa|reference]
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own batch of the same
+workload (independent problems, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, make_batch  # noqa: E402
+
+METRIC = "jagged attn fwd/bwd valid-token TFLOPS bf16 on 1 GB300; % of tensor peak"
+DEFAULT_CONFIG = "gem_self"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- accounting
+def valid_pairs(lq, lk, causal):
+    """Visited (query, key) pairs: Lq*Lk, or with bottom-right causal alignment the
+    pairs j <= i + (Lk - Lq)."""
+    lq = np.asarray(lq, dtype=np.int64)
+    lk = np.asarray(lk, dtype=np.int64)
+    if not causal:
+        return int((lq * lk).sum())
+    tot = 0
+    for a, b in zip(lq.tolist(), lk.tolist()):
+        first = max(0, a - b)            # rows before this see no key
+        n = a - first
+        if n <= 0 or b <= 0:
+            continue
+        s0 = first + (b - a) + 1         # keys seen by row `first`
+        tot += n * s0 + n * (n - 1) // 2
+    return tot
+
+
+def workload_flops(batch):
+    P = valid_pairs(batch.q_lengths, batch.kv_lengths, batch.cfg.causal)
+    dH = batch.cfg.head_dim * batch.cfg.heads
+    return {"pairs": P, "fwd": 4.0 * dH * P, "bwd": 10.0 * dH * P, "dkdv": 8.0 * dH * P, "dq": 2.0 * dH * P}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def config_dict(cfg, name):
+    d = {"workload": name, "batch": cfg.batch, "heads": cfg.heads, "head_dim": cfg.head_dim,
+         "lengths": list(cfg.lengths), "causal": cfg.causal,
+         "kv_lengths": list(cfg.kv_lengths) if cfg.kv_lengths else "same as query",
+         "bias": f"relpos table [H,{cfg.bias_buckets}] fp32, bucket j-i+{cfg.bias_center}" if cfg.bias_buckets
+         else None, "seed": cfg.seed, "l2": "inputs larger than L2, no flush"}
+    return d
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.path = tempfile.mktemp(prefix="jfa_clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.uuid = str(getattr(torch.cuda.get_device_properties(device_index), "uuid", ""))
+        except Exception:
+            self.uuid = ""
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if self.uuid:
+            mine = [r for r in rows if self.uuid.replace("GPU-", "") in r[1]]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        idx0 = rows[0][0]
+        rows = [r for r in rows if r[0] == idx0]
+
+        def num(s):
+            try:
+                return float(s.split()[0])
+            except Exception:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(batch, budget_s, rng_seed=0):
+    """Run the float64 oracle forward+backward on (sequence, head) pairs of the batch,
+    drawn in a seeded order, until `budget_s` of wall time is spent.  Returns
+    (valid fwd+bwd flops processed, seconds, pairs done)."""
+    import oracle.jfa_oracle as orc
+
+    cfg = batch.cfg
+    rng = np.random.default_rng(rng_seed)
+    B = batch.q_lengths.numel()
+    order = rng.permutation(B)
+    lq, lk = batch.q_lengths.numpy(), batch.kv_lengths.numpy()
+    center = cfg.bias_center if batch.bias is not None else 0
+    done_flops, pairs, t0 = 0.0, 0, time.perf_counter()
+    dH = cfg.head_dim
+    for b in order:
+        h = int(rng.integers(cfg.heads))
+        orc.sequence_reference(int(b), h, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets,
+                               cfg.scale, cfg.causal, batch.bias, center, dout=batch.dout)
+        P = valid_pairs([lq[b]], [lk[b]], cfg.causal)
+        done_flops += 14.0 * dH * P
+        pairs += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done_flops, time.perf_counter() - t0, pairs
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- padded SDPA
+def padded_sdpa(batch, steps):
+    """Dense SDPA on the batch padded to its longest sequence (the padding-waste
+    comparison): time per fwd+bwd step and peak memory."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+
+    cfg = batch.cfg
+    dev = batch.q.device
+    B, H, d = batch.q_lengths.numel(), cfg.heads, cfg.head_dim
+    Lq, Lk = int(batch.q_lengths.max()), int(batch.kv_lengths.max())
+    qo, ko = batch.q_offsets.cpu().tolist(), batch.kv_offsets.cpu().tolist()
+
+    def pad(x, off, L):
+        out = torch.zeros((B, L, H, d), dtype=x.dtype, device=dev)
+        for b in range(B):
+            out[b, : off[b + 1] - off[b]] = x[off[b]:off[b + 1]]
+        return out.transpose(1, 2).contiguous()
+
+    q, k, v = pad(batch.q, qo, Lq), pad(batch.k, ko, Lk), pad(batch.v, ko, Lk)
+    do = pad(batch.dout, qo, Lq)
+    mask = None
+    if not cfg.causal:
+        mask = (torch.arange(Lk, device=dev)[None, :] < batch.kv_lengths.to(dev)[:, None])[:, None, None, :]
+    if cfg.bias_buckets:
+        i = torch.arange(Lq, device=dev)[:, None]
+        j = torch.arange(Lk, device=dev)[None, :]
+        idx = (j - i + cfg.bias_center).clamp(0, cfg.bias_buckets - 1)
+        bias = batch.bias[:, idx][None]  # [1, H, Lq, Lk]
+        if cfg.causal:
+            bias = bias.masked_fill(j > i, float("-inf"))
+        mask = bias.to(torch.bfloat16)
+    backends = [SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION, SDPBackend.MATH] if mask is None \
+        else [SDPBackend.EFFICIENT_ATTENTION, SDPBackend.CUDNN_ATTENTION, SDPBackend.MATH]
+    for be in backends:
+        try:
+            qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+
+            def step():
+                with sdpa_kernel([be]):
+                    o = torch.nn.functional.scaled_dot_product_attention(
+                        qq, kk, vv, attn_mask=mask, is_causal=cfg.causal and mask is None, scale=cfg.scale)
+                o.backward(do)
+            step()
+            torch.cuda.synchronize()
+            torch.cuda.reset_peak_memory_stats()
+            base = torch.cuda.memory_allocated()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            peak = torch.cuda.max_memory_allocated() - base
+            return {"backend": str(be).split(".")[-1], "ms_per_step": round(ms, 3),
+                    "padded_shape": [B, H, Lq, Lk], "peak_extra_gb": round(peak / 1e9, 3)}
+        except Exception as e:  # backend not applicable: try the next
+            last = repr(e)[:200]
+            torch.cuda.synchronize()
+            continue
+    return {"unavailable": last}
+
+
+# ----------------------------------------------------------------------------- main arms
+def run_jfa(args, rank, world, device):
+    from jagged_attention_recsys_jfa_gb300 import jfa
+
+    name = args.config
+    cfg = CONFIGS[name]
+    batch = make_batch(cfg, device=device, seed=cfg.seed + rank)
+    fl = workload_flops(batch)
+    center = cfg.bias_center if batch.bias is not None else 0
+    out = torch.empty_like(batch.q)
+    lse = torch.empty((cfg.heads, batch.q.shape[0]), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(batch.q), torch.empty_like(batch.k), torch.empty_like(batch.v)
+    B, H, d = batch.q_lengths.numel(), cfg.heads, cfg.head_dim
+    Tq, Tk = batch.q.shape[0], batch.k.shape[0]
+    ws_f = torch.empty(jfa.workspace_size(B, H, d, Tq, Tk, False), dtype=torch.uint8, device=device)
+    ws_b = torch.empty(jfa.workspace_size(B, H, d, Tq, Tk, True), dtype=torch.uint8, device=device)
+
+    def fwd(q=batch.q, k=batch.k, v=batch.v, qo=batch.q_offsets, ko=batch.kv_offsets):
+        jfa.jfa_forward(q, k, v, qo, ko, batch.bias, center, cfg.scale, cfg.causal, out=out, lse=lse,
+                        workspace=ws_f)
+
+    def bwd(q=batch.q, k=batch.k, v=batch.v, do=batch.dout, qo=batch.q_offsets, ko=batch.kv_offsets):
+        jfa.jfa_backward(do, q, k, v, out, lse, qo, ko, batch.bias, center, cfg.scale, cfg.causal,
+                         dq=dq, dk=dk, dv=dv, workspace=ws_b)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    st = jfa.jfa_check_status(ws_f) or jfa.jfa_check_status(ws_b)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- timed region: inputs resident in HBM
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(device.index or 0)
+    torch.cuda.reset_peak_memory_stats()
+    mem_base = torch.cuda.memory_allocated()
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    jfa.jfa_timing_read()  # drop anything recorded before
+    jfa.jfa_timing_enable(True)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    jfa.jfa_timing_enable(False)
+    clk = clocks.stop()
+    per_kernel = jfa.jfa_timing_read()
+    peak_mem = torch.cuda.max_memory_allocated() - mem_base
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    st = jfa.jfa_check_status(ws_f) or jfa.jfa_check_status(ws_b)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region")
+
+    # max over ranks of the timed region, sum of work over ranks
+    t_local = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    w_local = torch.tensor([fl["fwd"] + fl["bwd"]], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t_local, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(w_local, op=torch.distributed.ReduceOp.SUM)
+    t_max_s = float(t_local.item()) / 1e3
+    total_flops = float(w_local.item()) * args.steps
+    value = total_flops / t_max_s / 1e12
+    launches = sum(c for _, c in per_kernel.values())
+
+    # ---- end to end through the public call with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {n: pin(getattr(batch, n)) for n in ("q", "k", "v", "dout", "q_offsets", "kv_offsets")}
+    h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+             for n, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    d_in = {n: torch.empty_like(getattr(batch, n)) for n in h_in}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        fwd(d_in["q"], d_in["k"], d_in["v"], d_in["q_offsets"], d_in["kv_offsets"])
+        bwd(d_in["q"], d_in["k"], d_in["v"], d_in["dout"], d_in["q_offsets"], d_in["kv_offsets"])
+        for n, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            h_out[n].copy_(t, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    t_e2e = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = total_flops / float(t_e2e.item()) / 1e12
+
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel = largest share of the timed region's kernel time
+    kinds = {k: v for k, v in per_kernel.items() if v[1] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][0])
+    algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"]}
+    ms_dom, n_dom = kinds[dom]
+    traffic = load_traffic(dom, name)
+    if dom in algo:
+        achieved = algo[dom] / (ms_dom / n_dom / 1e3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16 dense (burst)",
+                    "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": float(peaks["hbm_gbs"]),
+                    "unit": "GB/s", "frac": None, "traffic": traffic}
+    kernels = {k: {"ms_per_launch": round(v[0] / v[1], 4), "launches": v[1],
+                   "share": round(v[0] / sum(x[0] for x in kinds.values()), 4)} for k, v in kinds.items()}
+    for k, f in algo.items():
+        if k in kernels:
+            kernels[k]["algorithmic_tflops"] = round(f / (kernels[k]["ms_per_launch"] / 1e3) / 1e12, 1)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu_batch = make_batch(cfg, device="cpu")
+        f_done, secs, npairs = oracle_sample(cpu_batch, args.cpu_seconds)
+        cpu = {"value": round(f_done / secs / 1e12, 6), "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{npairs} (sequence, head) pairs of the {name} workload (CPU-seeded batch), float64 "
+                         f"forward+backward, {secs:.1f} s"}
+    sdpa = None
+    if not args.no_sdpa and world == 1:
+        s = padded_sdpa(batch, max(2, min(args.steps, 5)))
+        if "ms_per_step" in s:
+            s["valid_tflops"] = round((fl["fwd"] + fl["bwd"]) / (s["ms_per_step"] / 1e3) / 1e12, 1)
+            s["jfa_ms_per_step"] = round(total_ms / args.steps, 3)
+            s["jfa_peak_extra_gb"] = round(peak_mem / 1e9, 3)
+        sdpa = s
+
+    step_ms = t_max_s * 1e3 / args.steps
+    peak_tf = float(peaks["bf16_tflops"])
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded jagged batch, values N(0,1) in bf16)",
+        "config": config_dict(cfg, name),
+        "pct_of_tensor_peak": round(100 * value / world / peak_tf, 2),
+        "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fl["fwd"] / (fwd_ms / 1e3) / 1e12, 1),
+                "pct_of_peak": round(100 * fl["fwd"] / (fwd_ms / 1e3) / 1e12 / peak_tf, 2)},
+        "bwd": {"ms": round(bwd_ms, 4), "tflops": round(fl["bwd"] / (bwd_ms / 1e3) / 1e12, 1),
+                "pct_of_peak": round(100 * fl["bwd"] / (bwd_ms / 1e3) / 1e12 / peak_tf, 2)},
+        "valid_pairs": fl["pairs"], "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches, "clocks": clk, "padded_sdpa": sdpa,
+        "peak_mem_extra_gb": round(peak_mem / 1e9, 3),
+    }
+    return res
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if one matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(workload, {}).get(kernel)
+    except Exception:
+        return None
+
+
+def run_reference(args):
+    """The oracle as the reference arm: float64 on the host cores, a bounded sample of
+    the workload per step."""
+    name = args.config
+    cfg = CONFIGS[name]
+    batch = make_batch(cfg, device="cpu")
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for w in range(args.warmup):
+        oracle_sample(batch, per_step / 4, rng_seed=100 + w)
+    f_tot, s_tot, n_tot = 0.0, 0.0, 0
+    for i in range(args.steps):
+        f, s, n = oracle_sample(batch, per_step, rng_seed=i)
+        f_tot, s_tot, n_tot = f_tot + f, s_tot + s, n_tot + n
+    value = f_tot / s_tot / 1e12
+    sample = (f"{n_tot} (sequence, head) pairs of the {name} workload over {args.steps} steps "
+              f"(about {per_step:.0f} s each), float64 forward+backward")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * s_tot / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded jagged batch, values N(0,1) in bf16)", "config": config_dict(cfg, name),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="jfa", choices=["jfa", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sdpa", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        res = run_jfa(args, rank, world, device)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

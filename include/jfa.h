@@ -1,0 +1,129 @@
+/*
+ * jfa.h -- C ABI of the GB300 (sm_103a) Jagged Flash Attention library.
+ *
+ * Operation.  Exact softmax attention, forward and backward, computed directly on
+ * variable-length sequences packed as jagged tensors (values plus int64 offsets),
+ * never padded to the longest sequence, with an optional per-head additive bias and
+ * unequal query and key/value lengths ("Jagged Flash Attention (JFA)", Definition).
+ * "Exact" is the FlashAttention sense: tiling plus online softmax changes only the
+ * rounding, never the function ("TLX-Optimized Jagged Flash Attention: Approaching
+ * FA4-Level Performance on Blackwell", section "Why Jagged Flash Attention Deserves
+ * Attention").  For sequence b, head h, local query row i < Lq_b and key j < Lk_b:
+ *
+ *   s_ij   = scale * q_i . k_j + beta_h(i, j)
+ *   lse_i  = ln sum_j exp(s_ij)                 (over visible j)
+ *   out_i  = sum_j exp(s_ij - lse_i) v_j
+ *
+ * with Lq_b = q_offsets[b+1] - q_offsets[b], Lk_b = kv_offsets[b+1] - kv_offsets[b].
+ * Causal: key j is visible to query i iff j <= i + (Lk_b - Lq_b) (bottom-right
+ * alignment; equal lengths give the usual j <= i).  A query row with no visible key
+ * (Lk_b = 0, or causal with Lq_b > Lk_b) gets out = 0 and lse = -inf, and no gradient.
+ *
+ * Layout.  q, out, dout, dq: bf16 [total_q, H, d] row-major (token-major, heads
+ * contiguous); k, v, dk, dv: bf16 [total_kv, H, d]; lse: fp32 [H, total_q];
+ * offsets: int64 [B+1], offsets[0] = 0, non-decreasing, offsets[B] = total.  Empty
+ * sequences are allowed.
+ *
+ * Ownership and execution.  Every pointer is a DEVICE pointer owned by the caller.
+ * The library allocates nothing, keeps no state between calls (one process-wide
+ * cache of driver entry points aside), and enqueues all work asynchronously on
+ * `stream`.  Scratch memory is the caller's `workspace` (size from
+ * jfa_workspace_size, 256-byte aligned).  Calls sharing a workspace must not overlap.
+ *
+ * Errors.  Argument errors detectable on the host are returned synchronously and
+ * enqueue nothing.  Errors found on the device (malformed offsets, a bounded
+ * pipeline wait that ran out) are written to a status word in the workspace; read
+ * it with jfa_check_status (which synchronises the stream).  On a device error the
+ * outputs are unspecified.
+ *
+ * Requirements.  d in {64, 128}; H >= 1; B >= 1; every tensor pointer 16-byte
+ * aligned; an sm_100-family GPU (built for sm_103a).
+ */
+#ifndef JFA_H_
+#define JFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* jfa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  JFA_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128}, unsupported bias kind */
+  JFA_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
+  JFA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  JFA_ERR_BAD_OFFSETS = 5, /* device: offsets not 0-based, not monotone, or last != total */
+  JFA_ERR_TIMEOUT = 6      /* device: a bounded pipeline wait ran out; outputs unspecified */
+} jfa_status;
+
+/* Additive attention bias ("custom attention biases", "Jagged Flash Attention
+ * (JFA)", Definition).  kind 0 = none.  kind 1 = per-head relative-position table:
+ *   beta_h(i, j) = table[h * num_buckets + clamp(j - i + center, 0, num_buckets - 1)]
+ * with i, j local 0-based positions; added after scaling.  `table` is a device
+ * fp32 [H][num_buckets] array; num_buckets in [1, 8192]. */
+typedef struct {
+  int kind;
+  const float* table;
+  int num_buckets;
+  int center;
+} jfa_bias;
+
+/* Bytes of workspace jfa_forward (is_backward = 0) or jfa_backward (is_backward = 1)
+ * needs for these sizes.  Returns 0 on invalid sizes. */
+size_t jfa_workspace_size(int B, int H, int d, int64_t total_q, int64_t total_kv, int is_backward);
+
+/* Forward.  Writes out (bf16 [total_q, H, d]) and lse (fp32 [H, total_q], natural
+ * log of the row's sum of exp(s_ij)).  bias may be NULL. */
+jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_t* q_offsets,
+                       const int64_t* kv_offsets, int B, int H, int d, int64_t total_q, int64_t total_kv,
+                       const jfa_bias* bias, float scale, int causal, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, jfa_stream_t stream);
+
+/* Backward of sum(dout * out) w.r.t. q, k, v ("efficient backward passes",
+ * "Jagged Flash Attention (JFA)", Definition; split scheme of "Four generations"
+ * item 2: dK/dV computed per key/value block, dQ in a separate pass that owns each
+ * dQ tile, no atomics).  out and lse must be the forward's results for the same
+ * inputs.  The bias is a constant (no bias gradient).  dq, dk, dv are bf16 with the
+ * shapes of q, k, v and are fully overwritten (rows of keys no query sees get 0). */
+jfa_status jfa_backward(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const int64_t* q_offsets, const int64_t* kv_offsets, int B, int H,
+                        int d, int64_t total_q, int64_t total_kv, const jfa_bias* bias, float scale,
+                        int causal, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        jfa_stream_t stream);
+
+/* Synchronises `stream`, then returns the device status word of the last call that
+ * used `workspace` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT) and clears it. */
+jfa_status jfa_check_status(void* workspace, jfa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* jfa_status_string(jfa_status s);
+
+/* Number of kernels the last successful jfa_forward / jfa_backward call on this
+ * thread enqueued (for launch accounting). */
+int jfa_last_launch_count(void);
+
+/* Description of the last failed CUDA runtime/driver call made by this library on the
+ * calling thread (the cause behind a JFA_ERR_CUDA); "" if none.  Thread-local, static. */
+const char* jfa_last_error(void);
+
+/* Kernel kinds for per-kernel timing. */
+enum { JFA_KERNEL_PLAN = 0, JFA_KERNEL_FORWARD = 1, JFA_KERNEL_BWD_PREPROCESS = 2, JFA_KERNEL_BWD_DKDV = 3,
+       JFA_KERNEL_BWD_DQ = 4, JFA_NUM_KERNEL_KINDS = 5 };
+
+/* Benchmark support (not part of the attention itself).  While enabled (process-wide),
+ * every kernel launch is bracketed by two CUDA events recorded on the launch stream.
+ * jfa_timing_read waits for the recorded events, adds each kernel's elapsed time (ms)
+ * to ms[kind] and its launch count to launches[kind] for kind < n_kinds, then drops
+ * the records.  Both return JFA_ERR_CUDA if an event call fails. */
+jfa_status jfa_timing_enable(int on);
+jfa_status jfa_timing_read(double* ms, int* launches, int n_kinds);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JFA_H_ */

@@ -1,0 +1,754 @@
+// Jagged Flash Attention backward for sm_103a.
+//
+// The gradients of sum(dO * O) (standard FlashAttention-2 backward, the lineage
+// "Jagged Flash Attention (JFA)" builds on) computed in the split scheme of "Four
+// generations" item 2 -- no atomics anywhere:
+//   preprocess   D_i = sum_c dO_ic O_ic                            (HBM-bound)
+//   dK/dV pass   one CTA work item per (sequence, head, key tile); loops over the
+//                query tiles that see it: S^T = K Q^T, P^T = exp(S^T - lse),
+//                dV += P^T dO, dP^T = V dO^T, dS^T = P^T o (dP^T - D), dK += dS^T Q
+//   dQ pass      one item per (sequence, head, query tile), the only writer of its
+//                dQ tile: S = Q K^T, P, dP = dO V^T, dS = P o (dP - D), dQ += dS K
+// Rows past a sequence end arrive as zeros (per-sequence tensor maps); padded query
+// rows carry lse = D = 0, so they add nothing to dK/dV, and padded key rows add
+// nothing to dQ.  Both passes are persistent (grid = #SMs) over longest-first lists
+// and warp specialised: warp 0 loads (TMA), warp 1 issues tcgen05 MMAs, warps 2-9
+// are two warpgroups that split the 128 columns of each S/dP tile (64 each).
+// TMEM: S [0,128), dP [128,256), two d-column accumulators from 256.  P and dS are
+// written back as bf16 over the S / dP columns the warpgroup owns and feed the
+// accumulating MMAs straight from TMEM.
+#include <cuda_bf16.h>
+
+#include "jfa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace jfa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  const int64_t* q_off;
+  const int64_t* kv_off;
+  int H;
+  int64_t total_q, total_kv;
+  float scale, scale_log2;
+  int causal;
+  const float* bias2;  // [H][num_buckets] bias * log2(e), or nullptr
+  int num_buckets, center;
+  const CUtensorMap* maps;
+  const WorkItem* items;
+  const int* n_items;
+  int* status;
+  const float* lse;    // [H][total_q]
+  const float* delta;  // [H][total_q]
+  __nv_bfloat16* g0;   // dK (dK/dV pass) or dQ (dQ pass)
+  __nv_bfloat16* g1;   // dV (dK/dV pass)
+};
+
+__device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
+  }
+}
+
+// ---------------------------------------------------------------- preprocess
+__global__ void delta_kernel(const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ out,
+                             float* __restrict__ delta, int64_t total_q, int H, int d) {
+  const int64_t n = total_q * H;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < n;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t row = idx / H;
+    const int h = int(idx - row * H);
+    const uint4* a = reinterpret_cast<const uint4*>(dout + idx * d);
+    const uint4* b = reinterpret_cast<const uint4*>(out + idx * d);
+    float acc = 0.f;
+    for (int c = 0; c < d / 8; ++c) {
+      const uint4 x = __ldg(a + c), y = __ldg(b + c);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[t]));
+        const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[t]));
+        acc = fmaf(xf.x, yf.x, acc);
+        acc = fmaf(xf.y, yf.y, acc);
+      }
+    }
+    delta[int64_t(h) * total_q + row] = acc;
+  }
+}
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = D == 128 ? 2 : 3;  // ring stages, each two tiles
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kColS = 0, kColP = 128, kColA0 = 256, kColA1 = 256 + D;
+  // resident pair (K,V or Q,dO) + ring of pairs + per-stage lse/D vectors
+  static constexpr int kSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes + kStages * 2 * 128 * 4 + 1024;
+};
+
+// Load one row-tile (128 rows x D columns, D/64 boxes of 16 KB) through a tensor map.
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int col0, int row0) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) tma_load_2d(dst + c * 16384, m, bar, col0 + c * 64, row0);
+}
+
+// 32 columns from TMEM -> floats.
+__device__ __forceinline__ void ld_cols32(uint32_t taddr, float* x) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(r[c]);
+}
+
+// Store 64 fp32 values as 32 packed bf16x2 TMEM columns.
+__device__ __forceinline__ void st_bf16_64(uint32_t taddr, const float* v) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) pk[t] = pack_bf16x2(v[2 * t], v[2 * t + 1]);
+  tmem_st32(taddr, pk);
+}
+
+// Write `ncols` (a multiple of 32) accumulator columns of this thread's TMEM lane, times
+// `mul`, as bf16 to global (or zeros when `zero`).
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float mul, __nv_bfloat16* dst,
+                                              bool valid, bool zero) {
+  for (int cc = 0; cc < ncols / 32; ++cc) {
+    uint32_t r[32];
+    if (!zero) {
+      tmem_ld32(taddr + cc * 32, r);
+      tmem_ld_wait();
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+      pk[t] = zero ? 0u : pack_bf16x2(__uint_as_float(r[2 * t]) * mul, __uint_as_float(r[2 * t + 1]) * mul);
+    if (valid) {
+      uint4* o = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) o[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+    }
+  }
+}
+
+// ================================================================== dK / dV pass
+template <int D, bool kBias>
+__global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kTileBytes;
+  uint8_t* sRing = smem + 2 * C::kTileBytes;  // stage s: Q at 2s, dO at 2s+1
+  float* sVec = reinterpret_cast<float*>(sRing + C::kStages * 2 * C::kTileBytes);  // [stage][2][128]: lse2, D
+
+  __shared__ uint64_t kv_full, kv_empty, st_full, dpt_full, p_full, ds_full, acc_full, acc_empty, mma_done;
+  __shared__ uint64_t stage_full[C::kStages], stage_empty[C::kStages];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
+    mbar_init(&st_full, 1);
+    mbar_init(&dpt_full, 1);
+    mbar_init(&p_full, 256);
+    mbar_init(&ds_full, 256);
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 256);
+    mbar_init(&mma_done, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&stage_full[i], 1);
+      mbar_init(&stage_empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n_items = *p.n_items;
+  volatile int* abort_flag = &abort_sh;
+  const bool causal = p.causal != 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer warp
+    uint32_t stage_n = 0, item_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const WorkItem it = p.items[idx];
+      const int64_t qo = p.q_off[it.b], ko = p.kv_off[it.b];
+      const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - ko);
+      int first, count;
+      q_tiles_for_kv_tile(it.t, Lq, Lk, causal, &first, &count);
+      if (count == 0) continue;
+      const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
+      const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
+      const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
+      const CUtensorMap* mdo = p.maps + size_t(it.b) * kNumMapSlots + kMapDO;
+      if (lane == 0) {
+        tmap_acquire(mq);
+        tmap_acquire(mk);
+        tmap_acquire(mv);
+        tmap_acquire(mdo);
+        if (mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) {
+          mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
+          load_tile<D>(sK, mk, &kv_full, it.h * D, it.t * kBN);
+          load_tile<D>(sV, mv, &kv_full, it.h * D, it.t * kBN);
+        } else {
+          ok = false;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      ++item_n;
+      const float* lse_h = p.lse + int64_t(it.h) * p.total_q + qo;
+      const float* dl_h = p.delta + int64_t(it.h) * p.total_q + qo;
+      for (int i = 0; i < count; ++i) {
+        const int qt = first + i;
+        const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(&stage_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) { ok = false; break; }
+        // per-query vectors for this tile: lse in log2 units (+inf for rows that see no
+        // key, so exp2 gives 0) and D; 0 for rows past the sequence end
+        float* vec = sVec + e * 256;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = qt * kBM + lane + 32 * r;
+          float l2 = 0.f, dd = 0.f;
+          if (row < Lq) {
+            const float l = __ldg(lse_h + row);
+            l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+            dd = __ldg(dl_h + row);
+          }
+          vec[lane + 32 * r] = l2;
+          vec[128 + lane + 32 * r] = dd;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&stage_full[e], 2 * C::kTileBytes);
+          uint8_t* dst = sRing + e * 2 * C::kTileBytes;
+          load_tile<D>(dst, mq, &stage_full[e], it.h * D, qt * kBM);
+          load_tile<D>(dst + C::kTileBytes, mdo, &stage_full[e], it.h * D, qt * kBM);
+        }
+        __syncwarp();
+        ++stage_n;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      const uint32_t f = stage_n > C::kStages ? stage_n - C::kStages : 0;
+      for (uint32_t n = f; n < stage_n; ++n) drain_wait(&stage_full[n % C::kStages], (n / C::kStages) & 1);
+      if (item_n > 0) drain_wait(&kv_full, (item_n - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(sRing);
+      uint32_t stage_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        tc_fence_after();
+        return true;
+      };
+      // S^T (or dP^T) = A_tile(keys x D) * B_tile(queries x D)^T, both K-major
+      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + dcol, sdesc_sw128(a + o, 16, 1024), sdesc_sw128(b + o, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      // acc(keys x D) += X^T (TMEM bf16, keys x 128 queries, two 64-column halves) * B(queries x D, MN-major)
+      auto mma_acc = [&](uint32_t dcol, uint32_t xcol, uint32_t b, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(b + kk * 2048, 16384, 1024),
+                  kIdAcc, (acc || kk > 0) ? 1u : 0u);
+      };
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const WorkItem it = p.items[idx];
+        const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+        int first, count;
+        q_tiles_for_kv_tile(it.t, Lq, Lk, causal, &first, &count);
+        if (count == 0) continue;
+        if (!wait(&kv_full, item_n & 1)) { ok = false; break; }
+        ++item_n;
+        const uint32_t s0 = stage_n;
+        auto qa = [&](uint32_t n) { return aR + (n % C::kStages) * 2 * C::kTileBytes; };
+        if (!wait(&stage_full[s0 % C::kStages], (s0 / C::kStages) & 1)) { ok = false; break; }
+        mma_nt(C::kColS, aK, qa(s0));
+        umma_commit(&st_full);
+        mma_nt(C::kColP, aV, qa(s0) + C::kTileBytes);
+        umma_commit(&dpt_full);
+        for (int i = 0; i < count && ok; ++i) {
+          const uint32_t n = s0 + i;
+          if (!wait(&p_full, tile_n & 1)) { ok = false; break; }
+          if (i == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
+          mma_acc(C::kColA1, C::kColS, qa(n) + C::kTileBytes, i > 0);  // dV += P^T dO
+          if (i + 1 < count) {
+            if (!wait(&stage_full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1)) { ok = false; break; }
+            mma_nt(C::kColS, aK, qa(n + 1));
+            umma_commit(&st_full);
+          }
+          if (!wait(&ds_full, tile_n & 1)) { ok = false; break; }
+          ++tile_n;
+          mma_acc(C::kColA0, C::kColP, qa(n), i > 0);  // dK += dS^T Q
+          umma_commit(&stage_empty[n % C::kStages]);
+          if (i + 1 < count) {
+            mma_nt(C::kColP, aV, qa(n + 1) + C::kTileBytes);
+            umma_commit(&dpt_full);
+          }
+        }
+        if (!ok) break;
+        stage_n = s0 + count;
+        ++acc_n;
+        umma_commit(&acc_full);
+        umma_commit(&kv_empty);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      umma_commit(&mma_done);
+      drain_wait(&mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warpgroups
+    const int w = (warp - 2) >> 2;      // column half owned: queries [64w, 64w+64)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row within the tile
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
+    const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
+    const float sl2 = p.scale_log2;
+    uint32_t stage_n = 0, tile_n = 0, acc_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const WorkItem it = p.items[idx];
+      const int64_t qo = p.q_off[it.b], ko = p.kv_off[it.b];
+      const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - ko);
+      int first, count;
+      q_tiles_for_kv_tile(it.t, Lq, Lk, causal, &first, &count);
+      const int j = it.t * kBN + row;  // local key index
+      const bool valid = j < Lk;
+      __nv_bfloat16* dk_row = p.g0 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
+      __nv_bfloat16* dv_row = p.g1 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
+      if (count == 0) {
+        store_acc_row(0, D / 2, 0.f, dk_row, valid, true);
+        store_acc_row(0, D / 2, 0.f, dv_row, valid, true);
+        continue;
+      }
+      const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
+      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
+      for (int i = 0; i < count && ok; ++i) {
+        const int qt = first + i;
+        const uint32_t e = stage_n % C::kStages;
+        if (!mbar_wait(&stage_full[e], (stage_n / C::kStages) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++stage_n;
+        const float* lse2 = sVec + e * 256 + 64 * w;
+        const float* dvec = sVec + e * 256 + 128 + 64 * w;
+        if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        float x[64];
+        ld_cols32(tS, x);
+        ld_cols32(tS + 32, x + 32);
+        const int i0 = qt * kBM + 64 * w;  // local query index of column 0 of this half
+        if (kBias) {
+          const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
+          if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 - c)) - lse2[c];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1))) - lse2[c];
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, -lse2[c]);
+        }
+        if (causal) {
+          const int lim = j - diag - i0;  // columns c < lim are hidden
+          if (lim > 0) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < lim) x[c] = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P^T
+        st_bf16_64(tS, x);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full);
+        if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++tile_n;
+        tc_fence_after();
+        float dp[64];
+        ld_cols32(tP, dp);
+        ld_cols32(tP + 32, dp + 32);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) dp[c] = x[c] * (dp[c] - dvec[c]);  // dS^T
+        st_bf16_64(tP, dp);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
+      }
+      if (!ok) break;
+      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      ++acc_n;
+      tc_fence_after();
+      store_acc_row(tmem + lane_addr + C::kColA0 + w * (D / 2), D / 2, p.scale, dk_row, valid, false);
+      store_acc_row(tmem + lane_addr + C::kColA1 + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
+      tc_fence_before();
+      mbar_arrive(&acc_empty);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ================================================================== dQ pass
+template <int D, bool kBias>
+__global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::kTileBytes;
+  uint8_t* sRing = smem + 2 * C::kTileBytes;  // stage s: K at 2s, V at 2s+1
+
+  __shared__ uint64_t qdo_full, qdo_empty, s_full, s_free, dp_full, ds_full, acc_full, acc_empty, mma_done;
+  __shared__ uint64_t stage_full[C::kStages], stage_empty[C::kStages];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(&qdo_full, 1);
+    mbar_init(&qdo_empty, 1);
+    mbar_init(&s_full, 1);
+    mbar_init(&s_free, 256);
+    mbar_init(&dp_full, 1);
+    mbar_init(&ds_full, 256);
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 256);
+    mbar_init(&mma_done, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&stage_full[i], 1);
+      mbar_init(&stage_empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n_items = *p.n_items;
+  volatile int* abort_flag = &abort_sh;
+  const bool causal = p.causal != 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage_n = 0, item_n = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const WorkItem it = p.items[idx];
+        const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+        const int nkv = kv_tiles_for_q_tile(it.t, Lq, Lk, causal);
+        if (nkv == 0) continue;
+        const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
+        const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
+        const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
+        const CUtensorMap* mdo = p.maps + size_t(it.b) * kNumMapSlots + kMapDO;
+        tmap_acquire(mq);
+        tmap_acquire(mk);
+        tmap_acquire(mv);
+        tmap_acquire(mdo);
+        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
+        load_tile<D>(sQ, mq, &qdo_full, it.h * D, it.t * kBM);
+        load_tile<D>(sDO, mdo, &qdo_full, it.h * D, it.t * kBM);
+        ++item_n;
+        for (int jt = 0; jt < nkv; ++jt) {
+          const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
+          if (!mbar_wait(&stage_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+          mbar_arrive_expect_tx(&stage_full[e], 2 * C::kTileBytes);
+          uint8_t* dst = sRing + e * 2 * C::kTileBytes;
+          load_tile<D>(dst, mk, &stage_full[e], it.h * D, jt * kBN);
+          load_tile<D>(dst + C::kTileBytes, mv, &stage_full[e], it.h * D, jt * kBN);
+          ++stage_n;
+        }
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      const uint32_t f = stage_n > C::kStages ? stage_n - C::kStages : 0;
+      for (uint32_t n = f; n < stage_n; ++n) drain_wait(&stage_full[n % C::kStages], (n / C::kStages) & 1);
+      if (item_n > 0) drain_wait(&qdo_full, (item_n - 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aR = smem_u32(sRing);
+      uint32_t stage_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + dcol, sdesc_sw128(a + o, 16, 1024), sdesc_sw128(b + o, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      auto ka = [&](uint32_t n) { return aR + (n % C::kStages) * 2 * C::kTileBytes; };
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const WorkItem it = p.items[idx];
+        const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+        const int nkv = kv_tiles_for_q_tile(it.t, Lq, Lk, causal);
+        if (nkv == 0) continue;
+        if (!wait(&qdo_full, item_n & 1)) { ok = false; break; }
+        ++item_n;
+        const uint32_t s0 = stage_n;
+        if (!wait(&stage_full[s0 % C::kStages], (s0 / C::kStages) & 1)) { ok = false; break; }
+        mma_nt(C::kColS, aQ, ka(s0));
+        umma_commit(&s_full);
+        mma_nt(C::kColP, aDO, ka(s0) + C::kTileBytes);
+        umma_commit(&dp_full);
+        for (int jt = 0; jt < nkv && ok; ++jt) {
+          const uint32_t n = s0 + jt;
+          if (jt + 1 < nkv) {
+            if (!wait(&s_free, tile_n & 1)) { ok = false; break; }
+            if (!wait(&stage_full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1)) { ok = false; break; }
+            mma_nt(C::kColS, aQ, ka(n + 1));
+            umma_commit(&s_full);
+          }
+          if (!wait(&ds_full, tile_n & 1)) { ok = false; break; }
+          ++tile_n;
+          if (jt == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
+          // dQ += dS (TMEM, queries x keys) * K (keys x D, MN-major)
+          const uint32_t kb = ka(n);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(tmem + C::kColA0, tmem + C::kColP + (kk >> 2) * 64 + (kk & 3) * 8,
+                    sdesc_sw128(kb + kk * 2048, 16384, 1024), kIdAcc, (jt > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&stage_empty[n % C::kStages]);
+          if (jt + 1 < nkv) {
+            mma_nt(C::kColP, aDO, ka(n + 1) + C::kTileBytes);
+            umma_commit(&dp_full);
+          }
+        }
+        if (!ok) break;
+        // the last tile's s_free arrival has no consumer above: take it here
+        if (!wait(&s_free, tile_n - 1 & 1)) { ok = false; break; }
+        stage_n = s0 + nkv;
+        ++acc_n;
+        umma_commit(&acc_full);
+        umma_commit(&qdo_empty);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      umma_commit(&mma_done);
+      drain_wait(&mma_done, 0);
+    }
+  } else {
+    const int w = (warp - 2) >> 2;  // key columns [64w, 64w+64)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
+    const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
+    const float sl2 = p.scale_log2;
+    uint32_t tile_n = 0, acc_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const WorkItem it = p.items[idx];
+      const int64_t qo = p.q_off[it.b];
+      const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+      const int nkv = kv_tiles_for_q_tile(it.t, Lq, Lk, causal);
+      const int i = it.t * kBM + row;
+      const bool valid = i < Lq;
+      __nv_bfloat16* dq_row = p.g0 + ((qo + i) * p.H + it.h) * int64_t(D) + w * (D / 2);
+      if (nkv == 0) {
+        store_acc_row(0, D / 2, 0.f, dq_row, valid, true);
+        continue;
+      }
+      float lse2 = 0.f, dd = 0.f;
+      if (valid) {
+        const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
+        lse2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+        dd = __ldg(p.delta + int64_t(it.h) * p.total_q + qo + i);
+      }
+      const int diag = Lk - Lq;
+      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
+      for (int jt = 0; jt < nkv && ok; ++jt) {
+        if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        float x[64];
+        ld_cols32(tS, x);
+        ld_cols32(tS + 32, x + 32);
+        tc_fence_before();
+        mbar_arrive(&s_free);
+        const int j0 = jt * kBN + 64 * w;  // local key index of column 0 of this half
+        const int n_real = Lk - j0;        // columns >= n_real are past the sequence end
+        if (kBias) {
+          const int idx0 = j0 - i + p.center;
+          if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 + c)) - lse2;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 + c, 0), p.num_buckets - 1))) - lse2;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, -lse2);
+        }
+        if (causal) {
+          const int lim = i + diag - j0;  // columns c > lim are hidden
+          if (lim < 63) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c > lim) x[c] = -INFINITY;
+          }
+        }
+        if (n_real < 64) {
+          // padded keys (zero rows) would score exp2(-lse): keep them out of dS so it stays finite
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c >= n_real) x[c] = -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P
+        if (!mbar_wait(&dp_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++tile_n;
+        tc_fence_after();
+        float dp[64];
+        ld_cols32(tP, dp);
+        ld_cols32(tP + 32, dp + 32);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) dp[c] = x[c] * (dp[c] - dd);  // dS
+        st_bf16_64(tP, dp);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
+      }
+      if (!ok) break;
+      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      ++acc_n;
+      tc_fence_after();
+      store_acc_row(tmem + lane_addr + C::kColA0 + w * (D / 2), D / 2, p.scale, dq_row, valid, false);
+      tc_fence_before();
+      mbar_arrive(&acc_empty);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLayout& L, bool dq_pass) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  BwdParams bp;
+  bp.q_off = pr.q_off;
+  bp.kv_off = pr.kv_off;
+  bp.H = pr.H;
+  bp.total_q = pr.total_q;
+  bp.total_kv = pr.total_kv;
+  bp.scale = pr.scale;
+  bp.scale_log2 = pr.scale * kLog2e;
+  bp.causal = pr.causal;
+  bp.bias2 = pr.bias_table ? reinterpret_cast<const float*>(w + L.bias2) : nullptr;
+  bp.num_buckets = pr.num_buckets;
+  bp.center = pr.center;
+  bp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
+  bp.items = reinterpret_cast<const WorkItem*>(w + (dq_pass ? L.dq : L.dkv));
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);
+  bp.n_items = dq_pass ? &hdr->n_dq : &hdr->n_dkv;
+  bp.status = &reinterpret_cast<WsHeader*>(w)->status;
+  bp.lse = lse;
+  bp.delta = reinterpret_cast<const float*>(w + L.delta);
+  bp.g0 = nullptr;
+  bp.g1 = nullptr;
+  return bp;
+}
+
+template <typename K>
+cudaError_t launch_big(K kern, int smem, int grid, const BwdParams& bp, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 320, smem, stream>>>(bp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const void* out, void* ws,
+                                  const WsLayout& L, cudaStream_t stream) {
+  const int64_t n = pr.total_q * pr.H;
+  if (n == 0) return cudaSuccess;
+  int grid = int(std::min<int64_t>((n + 255) / 256, 152 * 16));
+  delta_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(dout),
+                                         static_cast<const __nv_bfloat16*>(out),
+                                         reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.delta), pr.total_q,
+                                         pr.H, pr.d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dk, void* dv,
+                            int num_sms, cudaStream_t stream) {
+  BwdParams bp = make_params(pr, lse, ws, L, false);
+  bp.g0 = static_cast<__nv_bfloat16*>(dk);
+  bp.g1 = static_cast<__nv_bfloat16*>(dv);
+  const bool bias = pr.bias_table != nullptr;
+  if (pr.d == 128)
+    return bias ? launch_big(dkdv_kernel<128, true>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream)
+                : launch_big(dkdv_kernel<128, false>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream);
+  return bias ? launch_big(dkdv_kernel<64, true>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream)
+              : launch_big(dkdv_kernel<64, false>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream);
+}
+
+cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, int num_sms,
+                          cudaStream_t stream) {
+  BwdParams bp = make_params(pr, lse, ws, L, true);
+  bp.g0 = static_cast<__nv_bfloat16*>(dq);
+  const bool bias = pr.bias_table != nullptr;
+  if (pr.d == 128)
+    return bias ? launch_big(dq_kernel<128, true>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream)
+                : launch_big(dq_kernel<128, false>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream);
+  return bias ? launch_big(dq_kernel<64, true>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream)
+              : launch_big(dq_kernel<64, false>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream);
+}
+
+}  // namespace jfa

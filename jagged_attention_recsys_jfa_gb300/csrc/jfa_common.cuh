@@ -1,0 +1,115 @@
+// Shared definitions of the jagged attention kernels: tile sizes, the work-item
+// format written by the planner, and the workspace layout.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+
+#include "../../include/jfa.h"
+
+namespace jfa {
+
+constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
+constexpr int kBN = 128;  // key rows per tile
+constexpr int kMaxBuckets = 8192;
+constexpr int kCostBuckets = 2048;  // planner's counting-sort buckets (cost clamped)
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded pipeline waits: 2 s
+
+// One unit of work for a persistent CTA.
+//   forward: (b, h, t) = query-tile pair {2t, 2t+1} of sequence b, head h
+//   dQ pass: (b, h, t) = query tile t
+//   dK/dV  : (b, h, t) = key/value tile t
+// cost = number of tile pairs visited (used only for ordering, longest first).
+struct WorkItem {
+  int b, h, t, cost;
+};
+
+// Tensor-map slots per sequence (per-sequence maps clip TMA boxes at the sequence end
+// so rows past it arrive as zeros).
+enum MapSlot { kMapQ = 0, kMapK = 1, kMapV = 2, kMapDO = 3, kNumMapSlots = 4 };
+
+// Header at the start of the workspace.
+struct WsHeader {
+  int status;      // jfa_status of device-side checks (0 = ok)
+  int n_fwd;       // number of forward items
+  int n_dq;        // number of dQ items
+  int n_dkv;       // number of dK/dV items
+  int pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct WsLayout {
+  size_t maps = 0;     // CUtensorMap[B][kNumMapSlots]
+  size_t fwd = 0;      // WorkItem[cap_fwd]
+  size_t dq = 0;       // WorkItem[cap_dq]
+  size_t dkv = 0;      // WorkItem[cap_dkv]
+  size_t bias2 = 0;    // float[H][num_buckets]  bias table pre-multiplied by log2(e)
+  size_t delta = 0;    // float[H][total_q]   (backward: D_i = rowsum(dO * O))
+  size_t total = 0;
+  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Capacities are upper bounds on the item counts for any offsets with these totals:
+//   sum_b ceil(ceil(L_b/128)/2) <= total/256 + B,  sum_b ceil(L_b/128) <= total/128 + B.
+__host__ __device__ inline WsLayout make_layout(int B, int H, int64_t total_q, int64_t total_kv,
+                                                bool backward) {
+  WsLayout L;
+  size_t off = sizeof(WsHeader);
+  L.maps = align_up(off, 128);
+  off = L.maps + size_t(B) * kNumMapSlots * 128;
+  L.cap_fwd = int64_t(H) * (total_q / 256 + B + 1);
+  L.fwd = align_up(off, 16);
+  off = L.fwd + size_t(L.cap_fwd) * sizeof(WorkItem);
+  L.bias2 = align_up(off, 256);
+  off = L.bias2 + size_t(H) * size_t(kMaxBuckets) * sizeof(float);
+  if (backward) {
+    L.cap_dq = int64_t(H) * (total_q / 128 + B + 1);
+    L.dq = align_up(off, 16);
+    off = L.dq + size_t(L.cap_dq) * sizeof(WorkItem);
+    L.cap_dkv = int64_t(H) * (total_kv / 128 + B + 1);
+    L.dkv = align_up(off, 16);
+    off = L.dkv + size_t(L.cap_dkv) * sizeof(WorkItem);
+    L.delta = align_up(off, 256);
+    off = L.delta + size_t(H) * size_t(total_q) * sizeof(float);
+  }
+  L.total = align_up(off, 256);
+  return L;
+}
+
+// Number of key tiles query tile t of a sequence visits (bottom-right causal).
+__host__ __device__ inline int kv_tiles_for_q_tile(int t, int Lq, int Lk, bool causal) {
+  if (Lk <= 0 || t * kBM >= Lq) return 0;
+  if (!causal) return (Lk + kBN - 1) / kBN;
+  const int i_max = min(t * kBM + kBM - 1, Lq - 1);
+  const int last_j = min(Lk - 1, i_max + (Lk - Lq));
+  return last_j < 0 ? 0 : last_j / kBN + 1;
+}
+
+// First query tile that sees any key of key tile t (causal), and the count of query tiles visited.
+__host__ __device__ inline void q_tiles_for_kv_tile(int t, int Lq, int Lk, bool causal, int* first,
+                                                    int* count) {
+  const int nq = (Lq + kBM - 1) / kBM;
+  if (Lq <= 0 || t * kBN >= Lk) {
+    *first = 0;
+    *count = 0;
+    return;
+  }
+  if (!causal) {
+    *first = 0;
+    *count = nq;
+    return;
+  }
+  // key j is seen by query i iff i >= j - (Lk - Lq); the smallest key of the tile is t*kBN
+  const int i_min = max(0, t * kBN - (Lk - Lq));
+  if (i_min >= Lq) {
+    *first = 0;
+    *count = 0;
+    return;
+  }
+  *first = i_min / kBM;
+  *count = nq - *first;
+}
+
+}  // namespace jfa

@@ -1,0 +1,449 @@
+// Jagged Flash Attention forward for sm_103a.
+//
+// What it computes: exact softmax attention per jagged sequence ("Jagged Flash
+// Attention (JFA)", Definition), via tiling plus online softmax ("TLX-Optimized
+// Jagged Flash Attention ...", section "Why Jagged Flash Attention Deserves
+// Attention"), with the jagged boundary handled by the subtraction scheme ("Four
+// generations" item 1): tile loads through per-sequence tensor maps deliver zero
+// rows past the sequence end, so padded keys score exactly 0; their contribution
+// n_pad * exp(0 - m) is subtracted from the row sum once, on the last key tile.
+// No -inf mask pass touches jagged boundaries (causal masking of diagonal tiles is
+// a real mask, not a jagged one).
+//
+// How (one persistent CTA per SM, "Four generations" item 3: warp specialisation
+// plus persistent scheduling over a longest-first work list):
+//   warp 0      TMA producer: Q tile pair, then K_j, V_j into a ring of smem stages
+//   warp 1      MMA issuer:   S_s = Q_s K_j^T (tcgen05, SS, fp32 in TMEM);
+//                             O_s += P_s V_j (tcgen05, A = P from TMEM, B = V from smem)
+//   warps 2-5   softmax for query tile 0 of the pair (one TMEM lane = one query row)
+//   warps 6-9   softmax for query tile 1
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d, 256+2d).
+// P (bf16) overwrites the first 64 columns of its S region.  The issue order
+// PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) lets one tile's softmax overlap the other
+// tile's MMAs (ping-pong).  The running max is only raised (and O rescaled) when
+// it grows by more than 2^8, which keeps exp2 arguments <= 8 in between.
+#include <cuda_bf16.h>
+
+#include "jfa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace jfa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FwdParams {
+  const int64_t* q_off;
+  const int64_t* kv_off;
+  int H;
+  int64_t total_q;
+  float scale_log2;      // scale * log2(e), > 0
+  int causal;
+  const float* bias2;    // [H][num_buckets] bias * log2(e), or nullptr
+  int num_buckets, center;
+  const CUtensorMap* maps;  // [B][kNumMapSlots]
+  const WorkItem* items;
+  const int* n_items;
+  int* status;
+  __nv_bfloat16* out;
+  float* lse;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kSmemBytes = 2 * kTileBytes + kStages * kTileBytes + 1024;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+struct ItemInfo {
+  int b, h, t0, t1;
+  int64_t qo, ko;
+  int Lq, Lk;
+  int nkv0, nkv1, njt;
+  bool has1;
+};
+
+__device__ __forceinline__ ItemInfo decode(const FwdParams& p, int idx) {
+  const WorkItem it = p.items[idx];
+  ItemInfo r;
+  r.b = it.b;
+  r.h = it.h;
+  r.t0 = 2 * it.t;
+  r.t1 = r.t0 + 1;
+  r.qo = p.q_off[it.b];
+  r.ko = p.kv_off[it.b];
+  r.Lq = int(p.q_off[it.b + 1] - r.qo);
+  r.Lk = int(p.kv_off[it.b + 1] - r.ko);
+  r.has1 = r.t1 * kBM < r.Lq;
+  r.nkv0 = kv_tiles_for_q_tile(r.t0, r.Lq, r.Lk, p.causal != 0);
+  r.nkv1 = r.has1 ? kv_tiles_for_q_tile(r.t1, r.Lq, r.Lk, p.causal != 0) : 0;
+  r.njt = max(r.nkv0, r.nkv1);
+  return r;
+}
+
+__device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Wait that ignores the abort flag: used only to drain copies already in flight.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
+  }
+}
+
+template <int D, bool kBias>
+__global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                          // 2 tiles
+  uint8_t* sRing = smem + 2 * C::kTileBytes;   // kStages tiles
+
+  __shared__ uint64_t q_full, q_empty, mma_done;
+  __shared__ uint64_t kv_full[C::kStages], kv_empty[C::kStages];
+  __shared__ uint64_t s_full[2], p_full[2], o_full[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
+    mbar_init(&mma_done, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&o_full[s], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n_items = *p.n_items;
+  volatile int* abort_flag = &abort_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t ring_n = 0, item_n = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const ItemInfo it = decode(p, idx);
+        if (it.njt == 0) continue;
+        const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
+        const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
+        const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
+        tmap_acquire(mq);
+        tmap_acquire(mk);
+        tmap_acquire(mv);
+        if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        mbar_arrive_expect_tx(&q_full, (it.has1 ? 2 : 1) * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kBoxes; ++c) {
+          tma_load_2d(sQ + c * 16384, mq, &q_full, it.h * D + c * 64, it.t0 * kBM);
+          if (it.has1) tma_load_2d(sQ + C::kTileBytes + c * 16384, mq, &q_full, it.h * D + c * 64, it.t1 * kBM);
+        }
+        ++item_n;
+        for (int j = 0; j < it.njt && ok; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t e = ring_n % C::kStages, ph = (ring_n / C::kStages) & 1;
+            if (!mbar_wait(&kv_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+            mbar_arrive_expect_tx(&kv_full[e], C::kTileBytes);
+            uint8_t* dst = sRing + e * C::kTileBytes;
+#pragma unroll
+            for (int c = 0; c < C::kBoxes; ++c)
+              tma_load_2d(dst + c * 16384, kv ? mv : mk, &kv_full[e], it.h * D + c * 64, j * kBN);
+            ++ring_n;
+          }
+        }
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      // drain: every copy this thread started has landed before the CTA can exit
+      const uint32_t first = ring_n > C::kStages ? ring_n - C::kStages : 0;
+      for (uint32_t n = first; n < ring_n; ++n) drain_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1);
+      if (item_n > 0) drain_wait(&q_full, (item_n - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, false, true);
+      const uint32_t colS[2] = {C::kColS0, C::kColS1};
+      const uint32_t colO[2] = {C::kColO0, C::kColO1};
+      const uint32_t sQ_addr = smem_u32(sQ), sR_addr = smem_u32(sRing);
+      uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0};
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const ItemInfo it = decode(p, idx);
+        if (it.njt == 0) continue;
+        const int nkv[2] = {it.nkv0, it.nkv1};
+        if (!mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++item_n;
+        tc_fence_after();
+        int s_left = it.nkv0 + it.nkv1;
+        auto issue_S = [&](int s, uint32_t e) {
+          const uint32_t qa = sQ_addr + s * C::kTileBytes, ka = sR_addr + e * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_ss(tmem + colS[s], sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(ka + o, 16, 1024), kIdS,
+                    kk > 0);
+          }
+          umma_commit(&s_full[s]);
+          if (--s_left == 0) umma_commit(&q_empty);
+        };
+        auto issue_PV = [&](int s, uint32_t e, bool acc) {
+          const uint32_t va = sR_addr + e * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdPV,
+                    (acc || kk > 0) ? 1u : 0u);
+        };
+        auto wait_full = [&](uint32_t n) -> bool {
+          const bool r = mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, kWaitTimeoutNs);
+          tc_fence_after();
+          return r;
+        };
+        const uint32_t n0 = ring_n;  // K_j at n0 + 2j, V_j at n0 + 2j + 1
+        if (!wait_full(n0)) { ok = false; break; }
+        if (it.nkv0 > 0) issue_S(0, n0 % C::kStages);
+        if (it.nkv1 > 0) issue_S(1, n0 % C::kStages);
+        umma_commit(&kv_empty[n0 % C::kStages]);
+        for (int j = 0; j < it.njt && ok; ++j) {
+          const uint32_t nv = n0 + 2 * j + 1, nk = n0 + 2 * j + 2;
+          if (!wait_full(nv)) { ok = false; break; }
+          bool k_ready = false;
+          for (int s = 0; s < 2 && ok; ++s) {
+            if (j < nkv[s]) {
+              if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+              ++p_n[s];
+              tc_fence_after();
+              issue_PV(s, nv % C::kStages, j > 0);
+              if (j == nkv[s] - 1) umma_commit(&o_full[s]);
+            }
+            if (j + 1 < nkv[s]) {
+              if (!k_ready) {
+                if (!wait_full(nk)) { ok = false; break; }
+                k_ready = true;
+              }
+              issue_S(s, nk % C::kStages);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&kv_empty[nv % C::kStages]);
+          if (j + 1 < it.njt) umma_commit(&kv_empty[nk % C::kStages]);
+        }
+        ring_n = n0 + 2 * it.njt;
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      umma_commit(&mma_done);
+      drain_wait(&mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int s = (warp - 2) >> 2;
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + (s ? C::kColS1 : C::kColS0);
+    const uint32_t tO = tmem + lane_addr + (s ? C::kColO1 : C::kColO0);
+    const float sl2 = p.scale_log2;
+    uint32_t s_n = 0, o_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const ItemInfo it = decode(p, idx);
+      const int t = s ? it.t1 : it.t0;
+      if (t * kBM >= it.Lq) continue;
+      const int nkv = s ? it.nkv1 : it.nkv0;
+      const int i = t * kBM + row;  // local query index
+      const bool valid_row = i < it.Lq;
+      __nv_bfloat16* orow = p.out + ((it.qo + i) * p.H + it.h) * int64_t(D);
+      float* lrow = p.lse + int64_t(it.h) * p.total_q + it.qo + i;
+      if (nkv == 0) {
+        if (valid_row) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+          *lrow = -INFINITY;
+        }
+        continue;
+      }
+      const int diag = it.Lk - it.Lq;  // causal: key j visible iff j <= i + diag
+      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++s_n;
+        tc_fence_after();
+        float x[128];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            tmem_ld32(tS + cc * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[cc * 32 + c] = __uint_as_float(r[c]);
+          }
+        }
+        const int kv0 = j * kBN;
+        const bool last = (j == nkv - 1);
+        if (kBias) {
+          // x = scale*log2e * (q.k) + bias*log2e, bias only on real key columns
+          const int n_real = min(kBN, it.Lk - kv0);
+          const int idx0 = kv0 - i + p.center;
+          if (idx0 >= 0 && idx0 + kBN - 1 < p.num_buckets && n_real == kBN) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 + c));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int bi = min(max(idx0 + c, 0), p.num_buckets - 1);
+              x[c] = c < n_real ? fmaf(x[c], sl2, __ldg(brow + bi)) : x[c] * sl2;
+            }
+          }
+        }
+        if (p.causal) {
+          const int lim = i + diag - kv0;  // last visible column of this row in this tile
+          if (lim < kBN - 1) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > lim) x[c] = -INFINITY;
+          }
+        }
+        float mx = x[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+        const float m_tile = kBias ? mx : mx * sl2;
+        // raise the reference max only when it grows by more than 2^8
+        const bool need = m_tile > m + kRescaleThreshold;
+        const float m_new = need ? m_tile : m;
+        const float alpha = need ? ex2_approx(m - m_new) : 1.f;  // m = -inf gives 0
+        if (__any_sync(0xffffffffu, need) && j > 0) {
+          uint32_t r[32];
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            tmem_ld32(tO + cc * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            tmem_st32(tO + cc * 32, r);
+          }
+        }
+        l *= alpha;
+        m = m_new;
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        float sum = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int t2 = 0; t2 < 16; ++t2) {
+            const float a = kBias ? x[cc * 32 + 2 * t2] - m_use : fmaf(x[cc * 32 + 2 * t2], sl2, -m_use);
+            const float b = kBias ? x[cc * 32 + 2 * t2 + 1] - m_use : fmaf(x[cc * 32 + 2 * t2 + 1], sl2, -m_use);
+            const float pa = ex2_approx(a), pb = ex2_approx(b);
+            sum += pa + pb;
+            pk[t2] = pack_bf16x2(pa, pb);
+          }
+          tmem_st16(tS + cc * 16, pk);
+        }
+        if (last && !p.causal && kv0 + kBN > it.Lk) {
+          // subtraction scheme: padded keys scored exactly 0, each added exp2(0 - m_use)
+          sum -= float(kv0 + kBN - it.Lk) * ex2_approx(-m_use);
+        }
+        l += sum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[s]);
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, lse = ln(sum) = (m + log2 l) * ln 2
+      if (!mbar_wait(&o_full[s], o_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      ++o_n;
+      tc_fence_after();
+      const bool live = l > 0.f;
+      const float inv_l = live ? 1.f / l : 0.f;
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tO + cc * 32, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2)
+          pk[t2] = pack_bf16x2(__uint_as_float(r[2 * t2]) * inv_l, __uint_as_float(r[2 * t2 + 1]) * inv_l);
+        if (valid_row) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+      }
+      if (valid_row) *lrow = live ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before();
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int D, bool kBias>
+cudaError_t launch_fwd_t(const FwdParams& fp, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_kernel<D, kBias>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(fp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void* out, float* lse, int num_sms,
+                           cudaStream_t stream) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  FwdParams fp;
+  fp.q_off = pr.q_off;
+  fp.kv_off = pr.kv_off;
+  fp.H = pr.H;
+  fp.total_q = pr.total_q;
+  fp.scale_log2 = pr.scale * kLog2e;
+  fp.causal = pr.causal;
+  fp.bias2 = pr.bias_table ? reinterpret_cast<const float*>(w + L.bias2) : nullptr;
+  fp.num_buckets = pr.num_buckets;
+  fp.center = pr.center;
+  fp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
+  fp.items = reinterpret_cast<const WorkItem*>(w + L.fwd);
+  fp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_fwd;
+  fp.status = &reinterpret_cast<WsHeader*>(w)->status;
+  fp.out = static_cast<__nv_bfloat16*>(out);
+  fp.lse = lse;
+  const int grid = num_sms;
+  const bool bias = pr.bias_table != nullptr;
+  if (pr.d == 128) return bias ? launch_fwd_t<128, true>(fp, grid, stream) : launch_fwd_t<128, false>(fp, grid, stream);
+  return bias ? launch_fwd_t<64, true>(fp, grid, stream) : launch_fwd_t<64, false>(fp, grid, stream);
+}
+
+}  // namespace jfa

@@ -1,0 +1,202 @@
+// Planner kernel: validates the jagged offsets, builds one TMA tensor map per
+// (sequence, tensor) whose row extent is that sequence's length -- so tile loads
+// past a sequence end arrive as zeros, which the subtraction scheme of "Jagged
+// Flash Attention (JFA)", "Four generations" item 1, relies on -- and writes the
+// persistent kernels' work lists sorted longest first (counting sort on cost),
+// the scheduling that keeps SMs busy when short sequences finish early (same
+// page, "Why standard FlashAttention falls short" and item 3).
+#include "jfa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace jfa {
+namespace {
+
+struct PlanParams {
+  const int64_t* q_off;
+  const int64_t* kv_off;
+  int B, H;
+  int64_t total_q, total_kv;
+  int causal, backward;
+  uint8_t* ws;
+  WsLayout L;
+  const float* bias;  // [H][nb] or nullptr
+  int nb;
+};
+
+enum ListKind { kListFwd = 0, kListDq = 1, kListDkv = 2 };
+
+__device__ __forceinline__ int list_units(int kind, int Lq, int Lk) {
+  const int nq = (Lq + kBM - 1) / kBM;
+  if (kind == kListFwd) return (nq + 1) / 2;
+  if (kind == kListDq) return nq;
+  return (Lk + kBN - 1) / kBN;
+}
+
+__device__ __forceinline__ int unit_cost(int kind, int u, int Lq, int Lk, bool causal) {
+  if (kind == kListFwd)
+    return kv_tiles_for_q_tile(2 * u, Lq, Lk, causal) + kv_tiles_for_q_tile(2 * u + 1, Lq, Lk, causal);
+  if (kind == kListDq) return kv_tiles_for_q_tile(u, Lq, Lk, causal);
+  int first, count;
+  q_tiles_for_kv_tile(u, Lq, Lk, causal, &first, &count);
+  return count;
+}
+
+// Exclusive scan of hist[] in descending cost order: base[c] = sum_{c' > c} hist[c'].
+// 1024 threads, kCostBuckets = 2048 buckets (two per thread).  Returns the total.
+__device__ int scan_desc(const int* hist, int* base) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // thread tid owns descending positions r = 2*tid, 2*tid+1  (bucket c = kCostBuckets-1-r)
+  const int c0 = kCostBuckets - 1 - 2 * tid, c1 = c0 - 1;
+  const int v0 = hist[c0], v1 = hist[c1];
+  int x = v0 + v1;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_sums[lane] = wi - w;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + incl - x;
+  base[c0] = excl;
+  base[c1] = excl + v0;
+  __syncthreads();
+  int total = base[0] + hist[0];
+  return total;
+}
+
+__device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_t cap, int* count_out,
+                          int* hist, int* base) {
+  const int tid = threadIdx.x;
+  const bool causal = p.causal != 0;
+  for (int c = tid; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
+    const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
+    const int n = list_units(kind, Lq, Lk);
+    for (int u = 0; u < n; ++u) {
+      const int c = min(unit_cost(kind, u, Lq, Lk, causal), kCostBuckets - 1);
+      atomicAdd(&hist[c], p.H);
+    }
+  }
+  __syncthreads();
+  const int total = scan_desc(hist, base);
+  if (total > cap) {  // cannot happen for valid offsets (capacities are upper bounds)
+    if (tid == 0) {
+      atomicCAS(&reinterpret_cast<WsHeader*>(p.ws)->status, 0, int(JFA_ERR_WORKSPACE));
+      *count_out = 0;
+    }
+    return;
+  }
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
+    const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
+    const int n = list_units(kind, Lq, Lk);
+    for (int u = 0; u < n; ++u) {
+      const int cost = unit_cost(kind, u, Lq, Lk, causal);
+      const int c = min(cost, kCostBuckets - 1);
+      const int pos = atomicAdd(&base[c], p.H);
+      for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u, cost};
+    }
+  }
+  if (tid == 0) *count_out = total;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanMaps maps, PlanParams p) {
+  __shared__ int hist[kCostBuckets];
+  __shared__ int base[kCostBuckets];
+  const int tid = threadIdx.x;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+  if (tid == 0) hdr->status = 0;
+
+  // ---- bias table pre-scaled to log2 units (the kernels work with exp2)
+  if (p.bias) {
+    float* b2 = reinterpret_cast<float*>(p.ws + p.L.bias2);
+    for (int i = tid; i < p.H * p.nb; i += blockDim.x) b2[i] = p.bias[i] * 1.4426950408889634f;
+  }
+
+  // ---- validate offsets
+  int bad = 0;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int64_t lq = p.q_off[b + 1] - p.q_off[b];
+    const int64_t lk = p.kv_off[b + 1] - p.kv_off[b];
+    if (lq < 0 || lk < 0 || lq > (int64_t(1) << 30) || lk > (int64_t(1) << 30)) bad = 1;
+  }
+  if (tid == 0) {
+    if (p.q_off[0] != 0 || p.kv_off[0] != 0 || p.q_off[p.B] != p.total_q || p.kv_off[p.B] != p.total_kv)
+      bad = 1;
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (tid == 0) {
+      hdr->status = int(JFA_ERR_BAD_OFFSETS);
+      hdr->n_fwd = hdr->n_dq = hdr->n_dkv = 0;
+    }
+    return;
+  }
+
+  // ---- per-sequence tensor maps: copy the template, point it at the sequence's first
+  //      row and clip its row extent to the sequence length.
+  CUtensorMap* out_maps = reinterpret_cast<CUtensorMap*>(p.ws + p.L.maps);
+  for (int idx = tid; idx < p.B * kNumMapSlots; idx += blockDim.x) {
+    const int b = idx / kNumMapSlots, slot = idx % kNumMapSlots;
+    if (!maps.used[slot]) continue;
+    const bool is_q_side = (slot == kMapQ || slot == kMapDO);
+    const int64_t row0 = is_q_side ? p.q_off[b] : p.kv_off[b];
+    const int64_t len = (is_q_side ? p.q_off[b + 1] : p.kv_off[b + 1]) - row0;
+    CUtensorMap* dst = out_maps + idx;
+    const uint4* src = reinterpret_cast<const uint4*>(&maps.tmpl[slot]);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d4[i] = src[i];
+    tmap_replace_address(dst, static_cast<const uint8_t*>(maps.base[slot]) + row0 * int64_t(maps.row_bytes[slot]));
+    tmap_replace_dim1(dst, uint32_t(len > 0 ? len : 1));
+  }
+  tmap_release();
+
+  // ---- work lists
+  if (!p.backward) {
+    emit_list(p, kListFwd, reinterpret_cast<WorkItem*>(p.ws + p.L.fwd), p.L.cap_fwd, &hdr->n_fwd, hist, base);
+  } else {
+    emit_list(p, kListDkv, reinterpret_cast<WorkItem*>(p.ws + p.L.dkv), p.L.cap_dkv, &hdr->n_dkv, hist,
+              base);
+    emit_list(p, kListDq, reinterpret_cast<WorkItem*>(p.ws + p.L.dq), p.L.cap_dq, &hdr->n_dq, hist, base);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const WsLayout& L, bool backward,
+                        cudaStream_t stream) {
+  PlanParams p;
+  p.q_off = pr.q_off;
+  p.kv_off = pr.kv_off;
+  p.B = pr.B;
+  p.H = pr.H;
+  p.total_q = pr.total_q;
+  p.total_kv = pr.total_kv;
+  p.causal = pr.causal;
+  p.backward = backward ? 1 : 0;
+  p.ws = static_cast<uint8_t*>(ws);
+  p.L = L;
+  p.bias = pr.bias_table;
+  p.nb = pr.num_buckets;
+  plan_kernel<<<1, 1024, 0, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace jfa

@@ -1,0 +1,255 @@
+"""Python binding of the C ABI in include/jfa.h (argument marshalling only).
+
+Every step of the attention runs in the library's CUDA kernels; this module only
+checks tensors, allocates outputs and workspace through PyTorch's allocator, and
+passes raw device pointers plus the current CUDA stream.  There is no CPU path:
+without the built library, or with CPU tensors, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+JFA_OK = 0
+STATUS_NAMES = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_WORKSPACE",
+                4: "JFA_ERR_CUDA", 5: "JFA_ERR_BAD_OFFSETS", 6: "JFA_ERR_TIMEOUT"}
+
+# Every symbol include/jfa.h declares.
+EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_backward", "jfa_check_status",
+                    "jfa_status_string", "jfa_last_launch_count", "jfa_last_error", "jfa_timing_enable",
+                    "jfa_timing_read")
+KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+
+
+class JfaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        detail = ""
+        if status == 4:
+            try:
+                detail = " -- " + load_library(build_if_missing=False).jfa_last_error().decode()
+            except Exception:
+                pass
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)}){detail}")
+        self.status = status
+
+
+class _Bias(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("num_buckets", ctypes.c_int),
+                ("center", ctypes.c_int)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load the in-tree shared library (building it first if asked and needed)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB_PATH
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"jagged attention library not built ({path} missing); run build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.jfa_workspace_size.argtypes = [i32, i32, i32, i64, i64, i32]
+    lib.jfa_workspace_size.restype = sz
+    lib.jfa_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, ctypes.POINTER(_Bias), f32, i32,
+                                vp, vp, vp, sz, vp]
+    lib.jfa_forward.restype = i32
+    lib.jfa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64,
+                                 ctypes.POINTER(_Bias), f32, i32, vp, vp, vp, vp, sz, vp]
+    lib.jfa_backward.restype = i32
+    lib.jfa_check_status.argtypes = [vp, vp]
+    lib.jfa_check_status.restype = i32
+    lib.jfa_status_string.argtypes = [i32]
+    lib.jfa_status_string.restype = ctypes.c_char_p
+    lib.jfa_last_launch_count.argtypes = []
+    lib.jfa_last_launch_count.restype = i32
+    lib.jfa_last_error.argtypes = []
+    lib.jfa_last_error.restype = ctypes.c_char_p
+    lib.jfa_timing_enable.argtypes = [i32]
+    lib.jfa_timing_enable.restype = i32
+    lib.jfa_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i32]
+    lib.jfa_timing_read.restype = i32
+    _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library(build_if_missing=False).jfa_status_string(int(status)).decode()
+    except Exception:  # library not loadable: fall back to the enum name
+        return STATUS_NAMES.get(status, "unknown")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_values(name, t, rows=None, H=None, d=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 3 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [T, H, d] tensor")
+    if H is not None and (t.shape[1] != H or t.shape[2] != d):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [*, {H}, {d}]")
+    if rows is not None and t.shape[0] != rows:
+        raise ValueError(f"{name} has {t.shape[0]} rows, expected {rows}")
+
+
+def _check_offsets(name, off):
+    if not isinstance(off, torch.Tensor) or not off.is_cuda or off.dtype != torch.int64 or off.dim() != 1 \
+            or not off.is_contiguous() or off.numel() < 2:
+        raise ValueError(f"{name} must be a contiguous int64 CUDA tensor [B+1] with B >= 1")
+
+
+def _bias_struct(bias, center, H):
+    if bias is None:
+        return None, None
+    if not bias.is_cuda or bias.dtype != torch.float32 or bias.dim() != 2 or bias.shape[0] != H:
+        raise ValueError("bias must be a float32 CUDA tensor [H, num_buckets]")
+    bias = bias.contiguous()
+    return _Bias(1, bias.data_ptr(), bias.shape[1], int(center)), bias
+
+
+def workspace_size(B, H, d, total_q, total_kv, backward) -> int:
+    return int(load_library().jfa_workspace_size(B, H, d, total_q, total_kv, 1 if backward else 0))
+
+
+def _workspace(nbytes, device):
+    # 256-byte alignment is guaranteed by the caching allocator
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,
+                out=None, lse=None, workspace=None, stream=None):
+    """out, lse = jfa_forward(...): the C-ABI forward on PyTorch-allocated device memory.
+
+    q: bf16 [Tq, H, d]; k, v: bf16 [Tk, H, d]; offsets: int64 [B+1] on the device.
+    bias: optional fp32 [H, num_buckets] relative-position table (bucket j - i + bias_center).
+    Returns out bf16 [Tq, H, d] and lse fp32 [H, Tq].  The call is asynchronous on
+    the current stream; device-side errors are reported by jfa_check_status(workspace).
+    """
+    lib = load_library()
+    _check_values("q", q)
+    Tq, H, d = q.shape
+    _check_values("k", k, H=H, d=d)
+    _check_values("v", v, rows=k.shape[0], H=H, d=d)
+    _check_offsets("q_offsets", q_offsets)
+    _check_offsets("kv_offsets", kv_offsets)
+    B = q_offsets.numel() - 1
+    if kv_offsets.numel() != B + 1:
+        raise ValueError("q_offsets and kv_offsets must have the same length")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    bstruct, bias_keep = _bias_struct(bias, bias_center, H)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    nbytes = int(lib.jfa_workspace_size(B, H, d, Tq, k.shape[0], 0))
+    if workspace is None:
+        workspace = _workspace(nbytes, q.device)
+    st = lib.jfa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), q_offsets.data_ptr(), kv_offsets.data_ptr(),
+                         B, H, d, Tq, k.shape[0], ctypes.byref(bstruct) if bstruct is not None else None,
+                         scale, 1 if causal else 0, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), _stream_handle(stream))
+    if st != JFA_OK:
+        raise JfaError(st, "jfa_forward")
+    del bias_keep
+    return out, lse, workspace
+
+
+def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None,
+                 causal=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dq, dk, dv = jfa_backward(...): gradients of sum(dout * out) (bias held constant)."""
+    lib = load_library()
+    _check_values("q", q)
+    Tq, H, d = q.shape
+    for name, t, rows in (("dout", dout, Tq), ("out", out, Tq), ("k", k, None), ("v", v, k.shape[0])):
+        _check_values(name, t, rows=rows, H=H, d=d)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, Tq) or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [H, Tq]")
+    _check_offsets("q_offsets", q_offsets)
+    _check_offsets("kv_offsets", kv_offsets)
+    B = q_offsets.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    bstruct, bias_keep = _bias_struct(bias, bias_center, H)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = int(lib.jfa_workspace_size(B, H, d, Tq, k.shape[0], 1))
+    if workspace is None:
+        workspace = _workspace(nbytes, q.device)
+    st = lib.jfa_backward(dout.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), q_offsets.data_ptr(), kv_offsets.data_ptr(), B, H, d, Tq, k.shape[0],
+                          ctypes.byref(bstruct) if bstruct is not None else None, scale, 1 if causal else 0,
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                          _stream_handle(stream))
+    if st != JFA_OK:
+        raise JfaError(st, "jfa_backward")
+    del bias_keep
+    return dq, dk, dv, workspace
+
+
+def jfa_check_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status of the last call."""
+    return int(load_library().jfa_check_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+def jfa_last_launch_count() -> int:
+    return int(load_library().jfa_last_launch_count())
+
+
+def jfa_timing_enable(on: bool) -> None:
+    load_library().jfa_timing_enable(1 if on else 0)
+
+
+def jfa_timing_read() -> dict:
+    """{kind: (total_ms, launches)} for the launches recorded since the last read."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    st = load_library().jfa_timing_read(ms, cnt, n)
+    if st != JFA_OK:
+        raise JfaError(st, "jfa_timing_read")
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+class JaggedAttention(torch.autograd.Function):
+    """Differentiable jagged attention: out = JaggedAttention.apply(q, k, v, q_offsets,
+    kv_offsets, bias, bias_center, scale, causal).  lse is saved for the backward; the
+    bias table gets no gradient."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False):
+        out, lse, _ = jfa_forward(q, k, v, q_offsets, kv_offsets, bias, bias_center, scale, causal)
+        ctx.save_for_backward(q, k, v, out, lse, q_offsets, kv_offsets, bias)
+        ctx.cfg = (bias_center, scale, causal)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse, q_offsets, kv_offsets, bias = ctx.saved_tensors
+        bias_center, scale, causal = ctx.cfg
+        dq, dk, dv, _ = jfa_backward(dout.contiguous(), q, k, v, out, lse, q_offsets, kv_offsets, bias,
+                                     bias_center, scale, causal)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def jagged_attention(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False):
+    return JaggedAttention.apply(q, k, v, q_offsets, kv_offsets, bias, bias_center, scale, causal)

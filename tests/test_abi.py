@@ -1,0 +1,88 @@
+"""The C-ABI library: builds, loads without a GPU, exports every symbol include/jfa.h
+declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import jagged_attention_recsys_jfa_gb300 as jfa
+from jagged_attention_recsys_jfa_gb300 import build as jbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "jfa.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(jfa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(jfa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = jfa.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {jbuild.LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", out), f"{name} not exported"
+
+
+def test_library_has_no_libcuda_link_dependency():
+    deps = os.popen(f"ldd {jbuild.LIB_PATH}").read()
+    assert "libcuda.so" not in deps
+
+
+def test_workspace_size():
+    lib = jfa.load_library()
+    f = lib.jfa_workspace_size
+    assert f(0, 8, 128, 10, 10, 0) == 0          # B < 1
+    assert f(4, 8, 96, 10, 10, 0) == 0           # unsupported head dim
+    a = f(4, 8, 128, 1000, 1000, 0)
+    b = f(4, 8, 128, 1000, 1000, 1)
+    assert a > 0 and b > a and a % 256 == 0 and b % 256 == 0
+    assert f(4, 8, 128, 100000, 1000, 1) > b     # grows with the row count
+
+
+def _fwd(lib, **over):
+    args = dict(q=16, k=16, v=16, qo=16, ko=16, B=2, H=2, d=64, tq=10, tk=10, bias=None, scale=0.125,
+                causal=0, out=16, lse=16, ws=256, wsb=1 << 30, stream=None)
+    args.update(over)
+    return lib.jfa_forward(args["q"], args["k"], args["v"], args["qo"], args["ko"], args["B"], args["H"],
+                           args["d"], args["tq"], args["tk"], args["bias"], args["scale"], args["causal"],
+                           args["out"], args["lse"], args["ws"], args["wsb"], args["stream"])
+
+
+def test_host_argument_checks_return_before_any_device_work():
+    lib = jfa.load_library()
+    assert _fwd(lib, d=96) == 2                     # JFA_ERR_UNSUPPORTED
+    assert _fwd(lib, B=0) == 1                      # JFA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == 1
+    assert _fwd(lib, scale=float("nan")) == 1
+    assert _fwd(lib, q=18) == 1                     # misaligned
+    assert _fwd(lib, qo=None) == 1
+    assert _fwd(lib, ws=None) == 3                  # JFA_ERR_WORKSPACE
+    assert _fwd(lib, ws=128) == 3                   # misaligned workspace
+    assert _fwd(lib, wsb=100) == 3                  # too small
+    bad_bias = jfa.jfa._Bias(7, 16, 16, 0)
+    assert _fwd(lib, bias=ctypes.byref(bad_bias)) == 2
+    big_bias = jfa.jfa._Bias(1, 16, 100000, 0)
+    assert _fwd(lib, bias=ctypes.byref(big_bias)) == 1
+
+
+def test_status_strings():
+    lib = jfa.load_library()
+    for code in range(7):
+        assert lib.jfa_status_string(code)
+    assert b"unknown" in lib.jfa_status_string(99)
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    off = torch.tensor([0, 4], dtype=torch.int64)
+    with pytest.raises(ValueError):
+        jfa.jfa_forward(q, q, q, off, off)

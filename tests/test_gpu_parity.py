@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on the
+same seeded bf16 inputs -- element by element at oracle-sized cases (several tiles
+and ragged tails), sampled (sequence, head) pairs at the full workload sizes."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.jfa_oracle as orc
+from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, JaggedConfig, make_batch
+from parity_utils import compare_grads, compare_out_lse, gpu_run, oracle_full, rel_frob, GRAD_RTOL
+
+pytestmark = pytest.mark.gpu
+
+CUDA = torch.cuda.is_available()
+
+
+def small(name, batch, **kw):
+    """The named workload's shape (heads, head dim, bias, causality, length law) at a
+    batch size the oracle finishes in seconds."""
+    return dataclasses.replace(CONFIGS[name], batch=batch, **kw)
+
+
+# ----------------------------------------------------------------------------- full comparison
+FULL_CASES = {
+    "tiny": CONFIGS["tiny"],
+    "gem_self_b12": small("gem_self", 12),
+    "cross_b10": small("cross", 10, kv_lengths=("uniform", 256, 1200)),
+    "biased_causal_b8": small("biased_causal", 8),
+    "longtail_causal_b8": small("longtail_causal", 8, lengths=("lognormal", 300.0, 1.2, 16, 1500)),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL_CASES))
+def test_parity_elementwise(name):
+    batch = make_batch(FULL_CASES[name], device="cuda")
+    res = gpu_run(batch)
+    ref = oracle_full(batch)
+    compare_out_lse(res["out"], res["lse"], ref["out"], ref["lse"], name)
+    compare_grads(res, ref, name)
+
+
+EDGE = {
+    # lengths around tile boundaries, length 1, exact multiples
+    "boundaries_d128": (dict(heads=2, head_dim=128), [1, 127, 128, 129, 255, 256, 257], None, False, False),
+    "boundaries_d64_causal": (dict(heads=3, head_dim=64), [1, 127, 128, 129, 256, 300], None, True, False),
+    # empty sequences on either side
+    "empty_seqs": (dict(heads=2, head_dim=128), [0, 5, 0, 130, 7], [3, 0, 0, 200, 1], False, False),
+    "empty_seqs_causal_bias": (dict(heads=2, head_dim=64), [0, 5, 140, 7], [3, 0, 140, 9], True, True),
+    # unequal lengths with causal bottom-right alignment (rows that see no key)
+    "causal_lq_gt_lk": (dict(heads=2, head_dim=128), [300, 64, 129], [40, 1, 128], True, False),
+    "causal_lq_lt_lk": (dict(heads=2, head_dim=64), [40, 1, 128], [300, 64, 129], True, False),
+    "cross_noncausal_bias": (dict(heads=2, head_dim=128), [33, 1, 200], [500, 2, 129], False, True),
+    # one long sequence with many tiles
+    "long_single_d128": (dict(heads=1, head_dim=128), [1500], None, False, False),
+    "long_single_causal_d64": (dict(heads=2, head_dim=64), [1100], None, True, True),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_parity_edges(name):
+    shape, lq, lk, causal, bias = EDGE[name]
+    cfg = JaggedConfig(name, len(lq), shape["heads"], shape["head_dim"], ("uniform", 1, 1), causal=causal,
+                       bias_buckets=4096 if bias else 0, bias_center=2048 if bias else 0)
+    batch = make_batch(cfg, device="cuda", q_lengths=lq, kv_lengths=lk)
+    res = gpu_run(batch)
+    ref = oracle_full(batch)
+    # edge cases include 1- and 2-key rows where |O| is a single value row (up to ~4):
+    # the output's own bf16 rounding is allowed on top of the bound there
+    compare_out_lse(res["out"], res["lse"], ref["out"], ref["lse"], name, with_rounding=True)
+    compare_grads(res, ref, name)
+
+
+def test_subtraction_adversarial_row():
+    """One key scoring -6 next to 127 zero-padded columns: the running max is the
+    padded zeros' 0, and l - n_pad*exp2(-m) cancels 127 of the 127.0025 summed.  The
+    fp32 sum keeps Sum(real) to about ulp(127) = 7.6e-6 absolute, i.e. ~3e-3 relative
+    here, so this row is held to a bound derived from that (not the workload bound)
+    and its errors are reported."""
+    cfg = JaggedConfig("adv", 1, 1, 64, ("uniform", 1, 1), causal=False)
+    batch = make_batch(cfg, device="cuda", q_lengths=[4], kv_lengths=[1])
+    batch.k.zero_()
+    batch.k[0, 0, 0] = 1.0
+    batch.q.zero_()
+    batch.q[:, 0, 0] = -48.0   # scale 1/8: score -6
+    res = gpu_run(batch, backward=False)
+    ref = oracle_full(batch, backward=False)
+    out_err = float(np.abs(res["out"].double().cpu().numpy() - ref["out"]).max())
+    lse_err = float(np.abs(res["lse"].double().cpu().numpy() - ref["lse"]).max())
+    print(f"adversarial subtraction row: max|out err| = {out_err:.3g}, max|lse err| = {lse_err:.3g}")
+    assert out_err <= 2e-2 and lse_err <= 1e-2
+
+
+def test_autograd_function_matches_oracle():
+    from jagged_attention_recsys_jfa_gb300 import jagged_attention
+    batch = make_batch(small("gem_self", 3, head_dim=64, heads=2), device="cuda")
+    q = batch.q.clone().requires_grad_(True)
+    k = batch.k.clone().requires_grad_(True)
+    v = batch.v.clone().requires_grad_(True)
+    out = jagged_attention(q, k, v, batch.q_offsets, batch.kv_offsets, None, 0, batch.cfg.scale, False)
+    out.backward(batch.dout)
+    ref = oracle_full(batch)
+    compare_out_lse(out, ref["lse"], ref["out"], ref["lse"], "autograd")
+    compare_grads({"dq": q.grad, "dk": k.grad, "dv": v.grad}, ref, "autograd")
+
+
+def test_results_deterministic_across_calls():
+    batch = make_batch(small("biased_causal", 6), device="cuda")
+    a = gpu_run(batch)
+    b = gpu_run(batch)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_bad_offsets_reported_on_device():
+    from jagged_attention_recsys_jfa_gb300 import jfa_check_status, jfa_forward
+    batch = make_batch(small("gem_self", 4, head_dim=64), device="cuda")
+    bad = batch.q_offsets.clone()
+    bad[2] = bad[1] - 1  # not monotone
+    _, _, ws = jfa_forward(batch.q, batch.k, batch.v, bad, batch.kv_offsets, None, 0, batch.cfg.scale, False)
+    assert jfa_check_status(ws) == 5   # JFA_ERR_BAD_OFFSETS
+    # the library is still usable afterwards
+    res = gpu_run(batch, backward=False)
+    assert torch.isfinite(res["out"].float()).all()
+
+
+# ----------------------------------------------------------------------------- full sizes
+def _sample_pairs(batch, n, rng):
+    B = batch.q_lengths.numel()
+    lq = batch.q_lengths.numpy()
+    order = np.argsort(-lq)
+    picks = {int(order[0]), int(order[-1])}  # longest and shortest
+    while len(picks) < min(n, B):
+        picks.add(int(rng.integers(B)))
+    return [(b, int(rng.integers(batch.cfg.heads))) for b in sorted(picks)]
+
+
+@pytest.mark.parametrize("name", ["gem_self", "cross", "biased_causal", "longtail_causal"])
+def test_parity_full_size_sampled(name):
+    """The full workload in the launch configuration the benchmark times; the oracle
+    recomputes sampled (sequence, head) pairs one by one."""
+    batch = make_batch(CONFIGS[name], device="cuda")
+    res = gpu_run(batch)
+    cfg = batch.cfg
+    rng = np.random.default_rng(0)
+    qo = batch.q_offsets.cpu().numpy()
+    ko = batch.kv_offsets.cpu().numpy()
+    for b, h in _sample_pairs(batch, 6, rng):
+        o, lse, dq, dk, dv = orc.sequence_reference(
+            b, h, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, cfg.scale, cfg.causal,
+            batch.bias, cfg.bias_center if batch.bias is not None else 0, dout=batch.dout)
+        sl_q, sl_k = slice(qo[b], qo[b + 1]), slice(ko[b], ko[b + 1])
+        compare_out_lse(res["out"][sl_q, h], res["lse"][h, sl_q], o, lse, f"{name} b={b} h={h}")
+        for gname, g, ref in (("dq", res["dq"][sl_q, h], dq), ("dk", res["dk"][sl_k, h], dk),
+                              ("dv", res["dv"][sl_k, h], dv)):
+            e = rel_frob(g, ref)
+            assert e <= GRAD_RTOL, f"{name} b={b} h={h} {gname} rel err {e:.3g}"
+    # properties at full size: finite everywhere, lse >= max visible score is implied by
+    # out being a convex combination: |out| <= max |v| per (row, head)
+    assert torch.isfinite(res["out"].float()).all()
+    for g in ("dq", "dk", "dv"):
+        assert torch.isfinite(res[g].float()).all(), g
