@@ -96,6 +96,28 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
                         int causal, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                         jfa_stream_t stream);
 
+/* Forward without a workspace, for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this entry point.  Hosts such as inference-runtime
+ * plugins and services on a fixed, pre-planned memory arena give a kernel library
+ * only its inputs and outputs and must not call cudaMalloc on their hot path (it can
+ * synchronise the device and breaks the arena's budget); this call runs jfa_forward
+ * with its scratch in a file-scope device array of 8 MiB that every GPU loading the
+ * library holds until exit.  Arguments and results are those of jfa_forward.
+ * - Sizes whose workspace (jfa_workspace_size(..., 0)) exceeds 8 MiB are rejected with
+ *   JFA_ERR_WORKSPACE before anything is enqueued.
+ * - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * - Every call on a device shares the one array: calls whose work overlaps on the GPU
+ *   (e.g. on two streams) race and must be serialised by the caller.  Each call
+ *   rewrites all of the scratch it reads, so no clearing is needed between calls.
+ * - Device-detected errors (bad offsets, wait timeout) land in the shared array and are
+ *   not reported to the caller; use jfa_forward with a workspace to read them. */
+jfa_status jfa_forward_noalloc(const void* q, const void* k, const void* v, const int64_t* q_offsets,
+                               const int64_t* kv_offsets, int B, int H, int d, int64_t total_q, int64_t total_kv,
+                               const jfa_bias* bias, float scale, int causal, void* out, float* lse,
+                               jfa_stream_t stream);
+
 /* Synchronises `stream`, then returns the device status word of the last call that
  * used `workspace` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT) and clears it. */
 jfa_status jfa_check_status(void* workspace, jfa_stream_t stream);

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
                 4: "JFA_ERR_CUDA", 5: "JFA_ERR_BAD_OFFSETS", 6: "JFA_ERR_TIMEOUT"}
 
 # Every symbol include/jfa.h declares.
-EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_backward", "jfa_check_status",
+EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_forward_noalloc", "jfa_backward", "jfa_check_status",
                     "jfa_status_string", "jfa_last_launch_count", "jfa_last_error", "jfa_timing_enable",
                     "jfa_timing_read")
 KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
@@ -68,6 +68,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.jfa_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, ctypes.POINTER(_Bias), f32, i32,
                                 vp, vp, vp, sz, vp]
     lib.jfa_forward.restype = i32
+    lib.jfa_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, ctypes.POINTER(_Bias), f32,
+                                        i32, vp, vp, vp]
+    lib.jfa_forward_noalloc.restype = i32
     lib.jfa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64,
                                  ctypes.POINTER(_Bias), f32, i32, vp, vp, vp, vp, sz, vp]
     lib.jfa_backward.restype = i32
