@@ -61,7 +61,7 @@ typedef enum {
   JFA_ERR_TIMEOUT = 6      /* device: a bounded pipeline wait ran out; outputs unspecified */
 } jfa_status;
 
-/* Additive attention bias ("custom attention biases", "Jagged Flash Attention
+/* Additive attention bias (the user-defined biases of "Jagged Flash Attention
  * (JFA)", Definition).  kind 0 = none.  kind 1 = per-head relative-position table:
  *   beta_h(i, j) = table[h * num_buckets + clamp(j - i + center, 0, num_buckets - 1)]
  * with i, j local 0-based positions; added after scaling.  `table` is a device
@@ -84,8 +84,8 @@ jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_
                        const jfa_bias* bias, float scale, int causal, void* out, float* lse, void* workspace,
                        size_t workspace_bytes, jfa_stream_t stream);
 
-/* Backward of sum(dout * out) w.r.t. q, k, v ("efficient backward passes",
- * "Jagged Flash Attention (JFA)", Definition; split scheme of "Four generations"
+/* Backward of sum(dout * out) w.r.t. q, k, v (the backward pass listed among JFA's
+ * features, "Jagged Flash Attention (JFA)", Definition; split scheme of "Four generations"
  * item 2: dK/dV computed per key/value block, dQ in a separate pass that owns each
  * dQ tile, no atomics).  out and lse must be the forward's results for the same
  * inputs.  The bias is a constant (no bias gradient).  dq, dk, dv are bf16 with the

@@ -77,9 +77,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// SM count of the current device.  Also binds the device's primary context to the
+// calling thread (cudaSetDevice initialises it), which the driver-level tensor-map
+// encoder needs on threads that have made no CUDA call yet (e.g. autograd workers).
 int sm_count() {
   int dev = 0, n = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
     cuda_fail(e, "device query");
@@ -198,7 +202,7 @@ jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_
   }
   {
     KernelTimer t(JFA_KERNEL_PLAN, s);
-    JFA_CHECK_LAUNCH(launch_plan(pr, maps, workspace, L, false, s), "planner launch");
+    JFA_CHECK_LAUNCH(launch_plan(pr, maps, workspace, L, false, nsm, s), "planner launch");
   }
   {
     KernelTimer t(JFA_KERNEL_FORWARD, s);
@@ -250,11 +254,11 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
   }
   {
     KernelTimer t(JFA_KERNEL_PLAN, s);
-    JFA_CHECK_LAUNCH(launch_plan(pr, maps, workspace, L, true, s), "planner launch");
+    JFA_CHECK_LAUNCH(launch_plan(pr, maps, workspace, L, true, nsm, s), "planner launch");
   }
   {
     KernelTimer t(JFA_KERNEL_BWD_PREPROCESS, s);
-    JFA_CHECK_LAUNCH(launch_bwd_preprocess(pr, dout, out, workspace, L, s), "backward preprocess launch");
+    JFA_CHECK_LAUNCH(launch_bwd_preprocess(pr, dout, out, lse, workspace, L, nsm, s), "backward preprocess launch");
   }
   {
     KernelTimer t(JFA_KERNEL_BWD_DKDV, s);

@@ -26,6 +26,8 @@ namespace jfa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kRegsLoad = 104, kRegsCompute = 200;
+static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds the launch allocation");
 
 struct BwdParams {
   const int64_t* q_off;
@@ -40,8 +42,10 @@ struct BwdParams {
   const WorkItem* items;
   const int* n_items;
   int* status;
-  const float* lse;    // [H][total_q]
-  const float* delta;  // [H][total_q]
+  const float* lse2;    // [H][qpad_cap]  lse * log2(e), padded per sequence to 128 rows
+  const float* delta;   // [H][qpad_cap]  D, same layout
+  const int64_t* qpad;  // [B+1] sequence offsets in the padded vectors
+  int64_t qpad_cap;
   __nv_bfloat16* g0;   // dK (dK/dV pass) or dQ (dQ pass)
   __nv_bfloat16* g1;   // dV (dK/dV pass)
 };
@@ -56,37 +60,68 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- preprocess
-__global__ void delta_kernel(const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ out,
-                             float* __restrict__ delta, int64_t total_q, int H, int d) {
-  const int64_t n = total_q * H;
-  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < n;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t row = idx / H;
-    const int h = int(idx - row * H);
-    const uint4* a = reinterpret_cast<const uint4*>(dout + idx * d);
-    const uint4* b = reinterpret_cast<const uint4*>(out + idx * d);
-    float acc = 0.f;
-    for (int c = 0; c < d / 8; ++c) {
-      const uint4 x = __ldg(a + c), y = __ldg(b + c);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+// For every query tile of the dQ work list: D_i = sum_c dO_ic O_ic and lse_i * log2(e)
+// (+inf where lse = -inf, so exp2(s - lse) = 0 for a row that sees no key) into the
+// 128-row-padded per-query vectors, zeros on padding rows.  One warp per row, the lanes
+// across the head dimension (coalesced 2*d-byte rows).
+struct PreParams {
+  const int64_t* q_off;
+  int H;
+  int64_t total_q;
+  const WorkItem* items;
+  const int* n_items;
+  const int64_t* qpad;
+  int64_t qpad_cap;
+  const __nv_bfloat16* dout;
+  const __nv_bfloat16* out;
+  const float* lse;
+  float* lse2;
+  float* delta;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *p.n_items;
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+    const WorkItem it = p.items[idx];
+    const int64_t qo = p.q_off[it.b];
+    const int Lq = int(p.q_off[it.b + 1] - qo);
+    const int64_t pad0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
+    for (int t = it.u0; t < it.u1; ++t) {
+      for (int r = warp; r < kBM; r += 8) {
+        const int i = t * kBM + r;
+        float acc = 0.f, l2 = 0.f;
+        if (i < Lq) {
+          const int64_t e0 = ((qo + i) * p.H + it.h) * int64_t(D);
+          if (D == 128) {
+            const uint2 a = __ldg(reinterpret_cast<const uint2*>(p.dout + e0) + lane);
+            const uint2 b = __ldg(reinterpret_cast<const uint2*>(p.out + e0) + lane);
+            acc = fmaf(bf16lo(a.x), bf16lo(b.x),
+                       fmaf(bf16hi(a.x), bf16hi(b.x), fmaf(bf16lo(a.y), bf16lo(b.y), bf16hi(a.y) * bf16hi(b.y))));
+          } else {
+            const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(p.dout + e0) + lane);
+            const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(p.out + e0) + lane);
+            acc = fmaf(bf16lo(a), bf16lo(b), bf16hi(a) * bf16hi(b));
+          }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[t]));
-        const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[t]));
-        acc = fmaf(xf.x, yf.x, acc);
-        acc = fmaf(xf.y, yf.y, acc);
+          for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
+          l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+        }
+        if (lane == 0) {
+          p.delta[pad0 + i] = acc;
+          p.lse2[pad0 + i] = l2;
+        }
       }
     }
-    delta[int64_t(h) * total_q + row] = acc;
   }
 }
 
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kBoxes = D / 64;
   static constexpr int kStages = D == 128 ? 2 : 3;  // ring stages, each two tiles
-  static constexpr int kThreads = 320;
   static constexpr uint32_t kColS = 0, kColP = 128, kColA0 = 256, kColA1 = 256 + D;
   // resident pair (K,V or Q,dO) + ring of pairs + per-stage lse/D vectors
   static constexpr int kSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes + kStages * 2 * 128 * 4 + 1024;
@@ -99,13 +134,17 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m, ui
   for (int c = 0; c < D / 64; ++c) tma_load_2d(dst + c * 16384, m, bar, col0 + c * 64, row0);
 }
 
-// 32 columns from TMEM -> floats.
-__device__ __forceinline__ void ld_cols32(uint32_t taddr, float* x) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
+// 64 columns from TMEM -> floats, both loads in flight before one wait.
+__device__ __forceinline__ void ld_cols64(uint32_t taddr, float* x) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32(taddr, r0);
+  tmem_ld32(taddr + 32, r1);
   tmem_ld_wait();
 #pragma unroll
-  for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(r[c]);
+  for (int c = 0; c < 32; ++c) {
+    x[c] = __uint_as_float(r0[c]);
+    x[32 + c] = __uint_as_float(r1[c]);
+  }
 }
 
 // Store 64 fp32 values as 32 packed bf16x2 TMEM columns.
@@ -140,7 +179,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
 
 // ================================================================== dK / dV pass
 template <int D, bool kBias>
-__global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,73 +223,49 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
   volatile int* abort_flag = &abort_sh;
   const bool causal = p.causal != 0;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer warp
-    uint32_t stage_n = 0, item_n = 0;
-    bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-      const WorkItem it = p.items[idx];
-      const int64_t qo = p.q_off[it.b], ko = p.kv_off[it.b];
-      const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - ko);
-      int first, count;
-      q_tiles_for_kv_tile(it.t, Lq, Lk, causal, &first, &count);
-      if (count == 0) continue;
-      const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
-      const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
-      const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
-      const CUtensorMap* mdo = p.maps + size_t(it.b) * kNumMapSlots + kMapDO;
-      if (lane == 0) {
+  if (warp < kFirstComputeWarp) {
+   setmaxnreg_dec<kRegsLoad>();
+   if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage_n = 0, item_n = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const WorkItem wi = p.items[idx];
+        const int Lq = int(p.q_off[wi.b + 1] - p.q_off[wi.b]), Lk = int(p.kv_off[wi.b + 1] - p.kv_off[wi.b]);
+        const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
+        const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
+        const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
+        const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
         tmap_acquire(mq);
         tmap_acquire(mk);
         tmap_acquire(mv);
         tmap_acquire(mdo);
-        if (mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) {
+        // this (sequence, head)'s 128-row-padded lse2 and D vectors
+        const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + p.qpad[wi.b];
+        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+          int first, count;
+          q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+          if (count == 0) continue;
+          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
           mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
-          load_tile<D>(sK, mk, &kv_full, it.h * D, it.t * kBN);
-          load_tile<D>(sV, mv, &kv_full, it.h * D, it.t * kBN);
-        } else {
-          ok = false;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      ++item_n;
-      const float* lse_h = p.lse + int64_t(it.h) * p.total_q + qo;
-      const float* dl_h = p.delta + int64_t(it.h) * p.total_q + qo;
-      for (int i = 0; i < count; ++i) {
-        const int qt = first + i;
-        const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
-        int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(&stage_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs) ? 1 : 0;
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) { ok = false; break; }
-        // per-query vectors for this tile: lse in log2 units (+inf for rows that see no
-        // key, so exp2 gives 0) and D; 0 for rows past the sequence end
-        float* vec = sVec + e * 256;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = qt * kBM + lane + 32 * r;
-          float l2 = 0.f, dd = 0.f;
-          if (row < Lq) {
-            const float l = __ldg(lse_h + row);
-            l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
-            dd = __ldg(dl_h + row);
+          load_tile<D>(sK, mk, &kv_full, wi.h * D, kt * kBN);
+          load_tile<D>(sV, mv, &kv_full, wi.h * D, kt * kBN);
+          ++item_n;
+          for (int i = 0; i < count; ++i) {
+            const int qt = first + i;
+            const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
+            if (!mbar_wait(&stage_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+            mbar_arrive_expect_tx(&stage_full[e], 2 * C::kTileBytes + 2 * kBM * 4);
+            uint8_t* dst = sRing + e * 2 * C::kTileBytes;
+            load_tile<D>(dst, mq, &stage_full[e], wi.h * D, qt * kBM);
+            load_tile<D>(dst + C::kTileBytes, mdo, &stage_full[e], wi.h * D, qt * kBM);
+            bulk_load(sVec + e * 256, p.lse2 + vec0 + qt * kBM, kBM * 4, &stage_full[e]);
+            bulk_load(sVec + e * 256 + 128, p.delta + vec0 + qt * kBM, kBM * 4, &stage_full[e]);
+            ++stage_n;
           }
-          vec[lane + 32 * r] = l2;
-          vec[128 + lane + 32 * r] = dd;
         }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&stage_full[e], 2 * C::kTileBytes);
-          uint8_t* dst = sRing + e * 2 * C::kTileBytes;
-          load_tile<D>(dst, mq, &stage_full[e], it.h * D, qt * kBM);
-          load_tile<D>(dst + C::kTileBytes, mdo, &stage_full[e], it.h * D, qt * kBM);
-        }
-        __syncwarp();
-        ++stage_n;
       }
-    }
-    if (lane == 0) {
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       const uint32_t f = stage_n > C::kStages ? stage_n - C::kStages : 0;
       for (uint32_t n = f; n < stage_n; ++n) drain_wait(&stage_full[n % C::kStages], (n / C::kStages) & 1);
@@ -285,10 +300,11 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
                   kIdAcc, (acc || kk > 0) ? 1u : 0u);
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const WorkItem it = p.items[idx];
-        const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+       const WorkItem wi = p.items[idx];
+       const int Lq = int(p.q_off[wi.b + 1] - p.q_off[wi.b]), Lk = int(p.kv_off[wi.b + 1] - p.kv_off[wi.b]);
+       for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
         int first, count;
-        q_tiles_for_kv_tile(it.t, Lq, Lk, causal, &first, &count);
+        q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
         if (count == 0) continue;
         if (!wait(&kv_full, item_n & 1)) { ok = false; break; }
         ++item_n;
@@ -323,14 +339,17 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
         ++acc_n;
         umma_commit(&acc_full);
         umma_commit(&kv_empty);
+       }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
+  }
   } else {
+    setmaxnreg_inc<kRegsCompute>();
     // ------------------------------------------------------------ compute warpgroups
-    const int w = (warp - 2) >> 2;      // column half owned: queries [64w, 64w+64)
+    const int w = (warp - kFirstComputeWarp) >> 2;  // column half owned: queries [64w, 64w+64)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row within the tile
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
@@ -340,12 +359,13 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
     uint32_t stage_n = 0, tile_n = 0, acc_n = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-      const WorkItem it = p.items[idx];
-      const int64_t qo = p.q_off[it.b], ko = p.kv_off[it.b];
-      const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - ko);
+     const WorkItem it = p.items[idx];
+     const int64_t qo = p.q_off[it.b], ko = p.kv_off[it.b];
+     const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - ko);
+     for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
       int first, count;
-      q_tiles_for_kv_tile(it.t, Lq, Lk, causal, &first, &count);
-      const int j = it.t * kBN + row;  // local key index
+      q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+      const int j = kt * kBN + row;  // local key index
       const bool valid = j < Lk;
       __nv_bfloat16* dk_row = p.g0 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
       __nv_bfloat16* dv_row = p.g1 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
@@ -366,22 +386,35 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
         if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         float x[64];
-        ld_cols32(tS, x);
-        ld_cols32(tS + 32, x + 32);
+        ld_cols64(tS, x);
         const int i0 = qt * kBM + 64 * w;  // local query index of column 0 of this half
         if (kBias) {
           const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
           if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 - c)) - lse2[c];
+            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 - c));
           } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1))) - lse2[c];
+              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
+          }
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = reinterpret_cast<const float4*>(lse2)[c4];
+            x[4 * c4] -= l.x;
+            x[4 * c4 + 1] -= l.y;
+            x[4 * c4 + 2] -= l.z;
+            x[4 * c4 + 3] -= l.w;
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, -lse2[c]);
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = reinterpret_cast<const float4*>(lse2)[c4];
+            x[4 * c4] = fmaf(x[4 * c4], sl2, -l.x);
+            x[4 * c4 + 1] = fmaf(x[4 * c4 + 1], sl2, -l.y);
+            x[4 * c4 + 2] = fmaf(x[4 * c4 + 2], sl2, -l.z);
+            x[4 * c4 + 3] = fmaf(x[4 * c4 + 3], sl2, -l.w);
+          }
         }
         if (causal) {
           const int lim = j - diag - i0;  // columns c < lim are hidden
@@ -401,10 +434,15 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
         ++tile_n;
         tc_fence_after();
         float dp[64];
-        ld_cols32(tP, dp);
-        ld_cols32(tP + 32, dp + 32);
+        ld_cols64(tP, dp);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) dp[c] = x[c] * (dp[c] - dvec[c]);  // dS^T
+        for (int c4 = 0; c4 < 16; ++c4) {  // dS^T
+          const float4 dd = reinterpret_cast<const float4*>(dvec)[c4];
+          dp[4 * c4] = x[4 * c4] * (dp[4 * c4] - dd.x);
+          dp[4 * c4 + 1] = x[4 * c4 + 1] * (dp[4 * c4 + 1] - dd.y);
+          dp[4 * c4 + 2] = x[4 * c4 + 2] * (dp[4 * c4 + 2] - dd.z);
+          dp[4 * c4 + 3] = x[4 * c4 + 3] * (dp[4 * c4 + 3] - dd.w);
+        }
         st_bf16_64(tP, dp);
         tmem_st_wait();
         tc_fence_before();
@@ -418,6 +456,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
       store_acc_row(tmem + lane_addr + C::kColA1 + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
       tc_fence_before();
       mbar_arrive(&acc_empty);
+     }
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
   }
@@ -430,7 +469,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const BwdParams p) {
 
 // ================================================================== dQ pass
 template <int D, bool kBias>
-__global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -473,14 +512,19 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
   volatile int* abort_flag = &abort_sh;
   const bool causal = p.causal != 0;
 
-  if (warp == 0) {
+  if (warp < kFirstComputeWarp) {
+   setmaxnreg_dec<kRegsLoad>();
+   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage_n = 0, item_n = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const WorkItem it = p.items[idx];
+       const WorkItem wi = p.items[idx];
+       for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
+        WorkItem it = wi;
+        it.u0 = qt;
         const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
-        const int nkv = kv_tiles_for_q_tile(it.t, Lq, Lk, causal);
+        const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         if (nkv == 0) continue;
         const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
         const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
@@ -492,8 +536,8 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
         tmap_acquire(mdo);
         if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
-        load_tile<D>(sQ, mq, &qdo_full, it.h * D, it.t * kBM);
-        load_tile<D>(sDO, mdo, &qdo_full, it.h * D, it.t * kBM);
+        load_tile<D>(sQ, mq, &qdo_full, it.h * D, qt * kBM);
+        load_tile<D>(sDO, mdo, &qdo_full, it.h * D, qt * kBM);
         ++item_n;
         for (int jt = 0; jt < nkv; ++jt) {
           const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
@@ -504,6 +548,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
           load_tile<D>(dst + C::kTileBytes, mv, &stage_full[e], it.h * D, jt * kBN);
           ++stage_n;
         }
+       }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       const uint32_t f = stage_n > C::kStages ? stage_n - C::kStages : 0;
@@ -531,9 +576,10 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
       };
       auto ka = [&](uint32_t n) { return aR + (n % C::kStages) * 2 * C::kTileBytes; };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const WorkItem it = p.items[idx];
-        const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
-        const int nkv = kv_tiles_for_q_tile(it.t, Lq, Lk, causal);
+       const WorkItem wi = p.items[idx];
+       const int Lq = int(p.q_off[wi.b + 1] - p.q_off[wi.b]), Lk = int(p.kv_off[wi.b + 1] - p.kv_off[wi.b]);
+       for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
+        const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         if (nkv == 0) continue;
         if (!wait(&qdo_full, item_n & 1)) { ok = false; break; }
         ++item_n;
@@ -573,13 +619,16 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
         ++acc_n;
         umma_commit(&acc_full);
         umma_commit(&qdo_empty);
+       }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
+  }
   } else {
-    const int w = (warp - 2) >> 2;  // key columns [64w, 64w+64)
+    setmaxnreg_inc<kRegsCompute>();
+    const int w = (warp - kFirstComputeWarp) >> 2;  // key columns [64w, 64w+64)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
@@ -589,31 +638,29 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
     uint32_t tile_n = 0, acc_n = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-      const WorkItem it = p.items[idx];
-      const int64_t qo = p.q_off[it.b];
-      const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
-      const int nkv = kv_tiles_for_q_tile(it.t, Lq, Lk, causal);
-      const int i = it.t * kBM + row;
+     const WorkItem it = p.items[idx];
+     const int64_t qo = p.q_off[it.b];
+     const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+     const int64_t vec0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
+     for (int qt = it.u0; qt < it.u1 && ok; ++qt) {
+      const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
+      const int i = qt * kBM + row;
       const bool valid = i < Lq;
       __nv_bfloat16* dq_row = p.g0 + ((qo + i) * p.H + it.h) * int64_t(D) + w * (D / 2);
       if (nkv == 0) {
         store_acc_row(0, D / 2, 0.f, dq_row, valid, true);
         continue;
       }
-      float lse2 = 0.f, dd = 0.f;
-      if (valid) {
-        const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
-        lse2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
-        dd = __ldg(p.delta + int64_t(it.h) * p.total_q + qo + i);
-      }
+      // padded per-query vectors: 0 past the sequence end, +inf lse2 for rows that see no key
+      const float lse2 = __ldg(p.lse2 + vec0 + i);
+      const float dd = __ldg(p.delta + vec0 + i);
       const int diag = Lk - Lq;
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       for (int jt = 0; jt < nkv && ok; ++jt) {
         if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         float x[64];
-        ld_cols32(tS, x);
-        ld_cols32(tS + 32, x + 32);
+        ld_cols64(tS, x);
         tc_fence_before();
         mbar_arrive(&s_free);
         const int j0 = jt * kBN + 64 * w;  // local key index of column 0 of this half
@@ -652,8 +699,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
         ++tile_n;
         tc_fence_after();
         float dp[64];
-        ld_cols32(tP, dp);
-        ld_cols32(tP + 32, dp + 32);
+        ld_cols64(tP, dp);
 #pragma unroll
         for (int c = 0; c < 64; ++c) dp[c] = x[c] * (dp[c] - dd);  // dS
         st_bf16_64(tP, dp);
@@ -668,6 +714,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const BwdParams p) {
       store_acc_row(tmem + lane_addr + C::kColA0 + w * (D / 2), D / 2, p.scale, dq_row, valid, false);
       tc_fence_before();
       mbar_arrive(&acc_empty);
+     }
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
   }
@@ -697,8 +744,11 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);
   bp.n_items = dq_pass ? &hdr->n_dq : &hdr->n_dkv;
   bp.status = &reinterpret_cast<WsHeader*>(w)->status;
-  bp.lse = lse;
+  (void)lse;
+  bp.lse2 = reinterpret_cast<const float*>(w + L.lse2);
   bp.delta = reinterpret_cast<const float*>(w + L.delta);
+  bp.qpad = reinterpret_cast<const int64_t*>(w + L.qpad);
+  bp.qpad_cap = L.qpad_cap;
   bp.g0 = nullptr;
   bp.g1 = nullptr;
   return bp;
@@ -706,23 +756,36 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
 
 template <typename K>
 cudaError_t launch_big(K kern, int smem, int grid, const BwdParams& bp, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = check_launch_registers(kern);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 320, smem, stream>>>(bp);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(bp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const void* out, void* ws,
-                                  const WsLayout& L, cudaStream_t stream) {
-  const int64_t n = pr.total_q * pr.H;
-  if (n == 0) return cudaSuccess;
-  int grid = int(std::min<int64_t>((n + 255) / 256, 152 * 16));
-  delta_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(dout),
-                                         static_cast<const __nv_bfloat16*>(out),
-                                         reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.delta), pr.total_q,
-                                         pr.H, pr.d);
+cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const void* out, const float* lse,
+                                  void* ws, const WsLayout& L, int num_sms, cudaStream_t stream) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PreParams pp;
+  pp.q_off = pr.q_off;
+  pp.H = pr.H;
+  pp.total_q = pr.total_q;
+  pp.items = reinterpret_cast<const WorkItem*>(w + L.dq);
+  pp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_dq;
+  pp.qpad = reinterpret_cast<const int64_t*>(w + L.qpad);
+  pp.qpad_cap = L.qpad_cap;
+  pp.dout = static_cast<const __nv_bfloat16*>(dout);
+  pp.out = static_cast<const __nv_bfloat16*>(out);
+  pp.lse = lse;
+  pp.lse2 = reinterpret_cast<float*>(w + L.lse2);
+  pp.delta = reinterpret_cast<float*>(w + L.delta);
+  if (pr.d == 128)
+    preprocess_kernel<128><<<4 * num_sms, 256, 0, stream>>>(pp);
+  else
+    preprocess_kernel<64><<<4 * num_sms, 256, 0, stream>>>(pp);
   return cudaGetLastError();
 }
 

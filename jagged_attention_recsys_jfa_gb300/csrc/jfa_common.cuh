@@ -15,14 +15,30 @@ constexpr int kMaxBuckets = 8192;
 constexpr int kCostBuckets = 2048;  // planner's counting-sort buckets (cost clamped)
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded pipeline waits: 2 s
 
-// One unit of work for a persistent CTA.
-//   forward: (b, h, t) = query-tile pair {2t, 2t+1} of sequence b, head h
-//   dQ pass: (b, h, t) = query tile t
-//   dK/dV  : (b, h, t) = key/value tile t
-// cost = number of tile pairs visited (used only for ordering, longest first).
+// Persistent tensor-core kernels: 3 warpgroups.  Warpgroup 0 = TMA producer (warp 0),
+// tcgen05 issuer and TMEM owner (warp 1), two idle warps; warpgroups 1 and 2 = the
+// compute warps (one TMEM lane per thread).  Each kernel moves registers from warpgroup
+// 0 to the compute warpgroups with setmaxnreg; 128*load + 256*compute must not exceed
+// the launch allocation of 384 threads x 168 registers.
+constexpr int kThreads = 384;
+constexpr int kFirstComputeWarp = 4;
+constexpr uint32_t kLaunchRegs = 168;
+__host__ __device__ constexpr bool reg_split_fits(uint32_t load, uint32_t compute) {
+  return load % 8 == 0 && compute % 8 == 0 && 128 * load + 256 * compute <= kLaunchRegs * kThreads;
+}
+
+// One unit of work for a persistent CTA: the consecutive units [u0, u1) of sequence b,
+// head h, where a unit is
+//   forward: the query-tile pair {2u, 2u+1}
+//   dQ pass: query tile u
+//   dK/dV  : key/value tile u
+// The planner cuts each (sequence, head) into ranges whose cost (tile pairs visited) is
+// capped, so one CTA walks neighbouring tiles of one sequence and the shared operand
+// (K/V for the forward and dQ pass, Q/dO for dK/dV) is re-read from L2, not HBM.
 struct WorkItem {
-  int b, h, t, cost;
+  int b, h, u0, u1;
 };
+constexpr int kItemsPerCta = 4;  // target items per CTA when capping range cost
 
 // Tensor-map slots per sequence (per-sequence maps clip TMA boxes at the sequence end
 // so rows past it arrive as zeros).
@@ -34,7 +50,8 @@ struct WsHeader {
   int n_fwd;       // number of forward items
   int n_dq;        // number of dQ items
   int n_dkv;       // number of dK/dV items
-  int pad[60];
+  int64_t total_qpad;  // sum_b round_up(Lq_b, 128): rows of the padded per-query vectors
+  int pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -44,9 +61,11 @@ struct WsLayout {
   size_t dq = 0;       // WorkItem[cap_dq]
   size_t dkv = 0;      // WorkItem[cap_dkv]
   size_t bias2 = 0;    // float[H][num_buckets]  bias table pre-multiplied by log2(e)
-  size_t delta = 0;    // float[H][total_q]   (backward: D_i = rowsum(dO * O))
+  size_t qpad = 0;     // int64[B+1]  backward: offsets of each sequence in the padded vectors
+  size_t lse2 = 0;     // float[H][qpad_cap]  backward: lse * log2(e) (+inf if -inf), 0 on padding
+  size_t delta = 0;    // float[H][qpad_cap]  backward: D_i = rowsum(dO * O), 0 on padding
   size_t total = 0;
-  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0;
+  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0, qpad_cap = 0;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -71,8 +90,13 @@ __host__ __device__ inline WsLayout make_layout(int B, int H, int64_t total_q, i
     L.cap_dkv = int64_t(H) * (total_kv / 128 + B + 1);
     L.dkv = align_up(off, 16);
     off = L.dkv + size_t(L.cap_dkv) * sizeof(WorkItem);
+    L.qpad = align_up(off, 256);
+    off = L.qpad + size_t(B + 1) * sizeof(int64_t);
+    L.qpad_cap = int64_t(align_up(size_t(total_q) + size_t(kBM) * B, kBM));  // rows per head, 512-B aligned
+    L.lse2 = align_up(off, 256);
+    off = L.lse2 + size_t(H) * size_t(L.qpad_cap) * sizeof(float);
     L.delta = align_up(off, 256);
-    off = L.delta + size_t(H) * size_t(total_q) * sizeof(float);
+    off = L.delta + size_t(H) * size_t(L.qpad_cap) * sizeof(float);
   }
   L.total = align_up(off, 256);
   return L;

@@ -33,6 +33,8 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kRegsLoad = 120, kRegsCompute = 192;
+static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds the launch allocation");
 
 struct FwdParams {
   const int64_t* q_off;
@@ -57,7 +59,6 @@ struct FwdCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemBytes = 2 * kTileBytes + kStages * kTileBytes + 1024;
-  static constexpr int kThreads = 320;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 };
 
@@ -69,12 +70,12 @@ struct ItemInfo {
   bool has1;
 };
 
-__device__ __forceinline__ ItemInfo decode(const FwdParams& p, int idx) {
-  const WorkItem it = p.items[idx];
+// Unit u (query-tile pair {2u, 2u+1}) of work item `it`.
+__device__ __forceinline__ ItemInfo decode(const FwdParams& p, const WorkItem& it, int u) {
   ItemInfo r;
   r.b = it.b;
   r.h = it.h;
-  r.t0 = 2 * it.t;
+  r.t0 = 2 * u;
   r.t1 = r.t0 + 1;
   r.qo = p.q_off[it.b];
   r.ko = p.kv_off[it.b];
@@ -98,7 +99,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool kBias>
-__global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -139,13 +140,17 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
   const int n_items = *p.n_items;
   volatile int* abort_flag = &abort_sh;
 
-  if (warp == 0) {
+  if (warp < kFirstComputeWarp) {
+   setmaxnreg_dec<kRegsLoad>();
+   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t ring_n = 0, item_n = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const ItemInfo it = decode(p, idx);
+       const WorkItem wi = p.items[idx];
+       for (int u = wi.u0; u < wi.u1 && ok; ++u) {
+        const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
         const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
@@ -174,6 +179,7 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
             ++ring_n;
           }
         }
+       }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       // drain: every copy this thread started has landed before the CTA can exit
@@ -192,7 +198,9 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
       uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0};
       bool ok = true;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const ItemInfo it = decode(p, idx);
+       const WorkItem wi = p.items[idx];
+       for (int u = wi.u0; u < wi.u1 && ok; ++u) {
+        const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const int nkv[2] = {it.nkv0, it.nkv1};
         if (!mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
@@ -200,21 +208,22 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
         tc_fence_after();
         int s_left = it.nkv0 + it.nkv1;
         auto issue_S = [&](int s, uint32_t e) {
-          const uint32_t qa = sQ_addr + s * C::kTileBytes, ka = sR_addr + e * C::kTileBytes;
+          // descriptor start addresses are in 16-byte units in the low bits: step by adding
+          const uint64_t qd = sdesc_sw128(sQ_addr + s * C::kTileBytes, 16, 1024);
+          const uint64_t kd = sdesc_sw128(sR_addr + e * C::kTileBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_ss(tmem + colS[s], sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(ka + o, 16, 1024), kIdS,
-                    kk > 0);
+            const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            umma_ss(tmem + colS[s], qd + o, kd + o, kIdS, kk > 0);
           }
           umma_commit(&s_full[s]);
           if (--s_left == 0) umma_commit(&q_empty);
         };
         auto issue_PV = [&](int s, uint32_t e, bool acc) {
-          const uint32_t va = sR_addr + e * C::kTileBytes;
+          const uint64_t vd = sdesc_sw128(sR_addr + e * C::kTileBytes, 16384, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdPV,
+            umma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, vd + uint32_t(kk * 2048 >> 4), kIdPV,
                     (acc || kk > 0) ? 1u : 0u);
         };
         auto wait_full = [&](uint32_t n) -> bool {
@@ -252,14 +261,17 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
           if (j + 1 < it.njt) umma_commit(&kv_empty[nk % C::kStages]);
         }
         ring_n = n0 + 2 * it.njt;
+       }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
+  }
   } else {
+    setmaxnreg_inc<kRegsCompute>();
     // ------------------------------------------------------------ softmax warpgroups
-    const int s = (warp - 2) >> 2;
+    const int s = (warp - kFirstComputeWarp) >> 2;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
@@ -269,7 +281,9 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
     uint32_t s_n = 0, o_n = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-      const ItemInfo it = decode(p, idx);
+     const WorkItem wi = p.items[idx];
+     for (int u = wi.u0; u < wi.u1 && ok; ++u) {
+      const ItemInfo it = decode(p, wi, u);
       const int t = s ? it.t1 : it.t0;
       if (t * kBM >= it.Lq) continue;
       const int nkv = s ? it.nkv1 : it.nkv0;
@@ -295,13 +309,19 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
         tc_fence_after();
         float x[128];
         {
-          uint32_t r[32];
+          // all four loads in flight before a single wait
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(tS + 0, r0);
+          tmem_ld32(tS + 32, r1);
+          tmem_ld32(tS + 64, r2);
+          tmem_ld32(tS + 96, r3);
+          tmem_ld_wait();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            tmem_ld32(tS + cc * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[cc * 32 + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 32; ++c) {
+            x[c] = __uint_as_float(r0[c]);
+            x[32 + c] = __uint_as_float(r1[c]);
+            x[64 + c] = __uint_as_float(r2[c]);
+            x[96 + c] = __uint_as_float(r3[c]);
           }
         }
         const int kv0 = j * kBN;
@@ -329,29 +349,25 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
               if (c > lim) x[c] = -INFINITY;
           }
         }
-        float mx = x[0];
+        // row max as 8 independent chains, then a short tree
+        float mx8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+        for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_tile = kBias ? mx : mx * sl2;
         // raise the reference max only when it grows by more than 2^8
         const bool need = m_tile > m + kRescaleThreshold;
         const float m_new = need ? m_tile : m;
         const float alpha = need ? ex2_approx(m - m_new) : 1.f;  // m = -inf gives 0
-        if (__any_sync(0xffffffffu, need) && j > 0) {
-          uint32_t r[32];
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            tmem_ld32(tO + cc * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(tO + cc * 32, r);
-          }
-        }
         l *= alpha;
         m = m_new;
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        float sum = 0.f;
+        // row sum as 4 independent chains, in column order within each (real columns
+        // precede padded ones, which keeps the subtraction below well conditioned)
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
@@ -360,16 +376,30 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
             const float a = kBias ? x[cc * 32 + 2 * t2] - m_use : fmaf(x[cc * 32 + 2 * t2], sl2, -m_use);
             const float b = kBias ? x[cc * 32 + 2 * t2 + 1] - m_use : fmaf(x[cc * 32 + 2 * t2 + 1], sl2, -m_use);
             const float pa = ex2_approx(a), pb = ex2_approx(b);
-            sum += pa + pb;
+            sum4[cc] += pa + pb;
             pk[t2] = pack_bf16x2(pa, pb);
           }
           tmem_st16(tS + cc * 16, pk);
         }
+        float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         if (last && !p.causal && kv0 + kBN > it.Lk) {
           // subtraction scheme: padded keys scored exactly 0, each added exp2(0 - m_use)
           sum -= float(kv0 + kBN - it.Lk) * ex2_approx(-m_use);
         }
         l += sum;
+        // O still holds the sum over earlier tiles (their PV MMAs completed before this
+        // tile's S did); rescale it now that the S registers are free
+        if (__any_sync(0xffffffffu, need) && j > 0) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tO + cc * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            tmem_st32(tO + cc * 32, r);
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[s]);
@@ -399,6 +429,7 @@ __global__ void __launch_bounds__(320, 1) fwd_kernel(const FwdParams p) {
       }
       if (valid_row) *lrow = live ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
+     }
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
   }
@@ -413,9 +444,11 @@ template <int D, bool kBias>
 cudaError_t launch_fwd_t(const FwdParams& fp, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fwd_kernel<D, kBias>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = check_launch_registers(kern);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(fp);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(fp);
   return cudaGetLastError();
 }
 

@@ -25,16 +25,32 @@ struct PlanMaps {
   int used[kNumMapSlots];
 };
 
+// setmaxnreg.inc waits until the registers it asks for are free, so a kernel that
+// rebalances registers must be launched with the full allocation the split assumes.
+// Checked once per kernel before its first launch: a build that lowered the kernel's
+// register count is refused (cudaErrorInvalidConfiguration) instead of launched.
+template <typename K>
+cudaError_t check_launch_registers(K kern) {
+  static int verdict = -1;  // -1 unknown, 0 ok, 1 refused
+  if (verdict < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    verdict = fa.numRegs >= int(kLaunchRegs) ? 0 : 1;
+  }
+  return verdict == 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 // Launch the planner: validates offsets, writes per-sequence tensor maps and the
 // longest-first work lists for the forward (backward = false) or the two backward passes.
 cudaError_t launch_plan(const Problem& p, const PlanMaps& maps, void* ws, const WsLayout& L, bool backward,
-                        cudaStream_t stream);
+                        int num_sms, cudaStream_t stream);
 
 cudaError_t launch_forward(const Problem& p, void* ws, const WsLayout& L, void* out, float* lse,
                            int num_sms, cudaStream_t stream);
 
-cudaError_t launch_bwd_preprocess(const Problem& p, const void* dout, const void* out, void* ws,
-                                  const WsLayout& L, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const Problem& p, const void* dout, const void* out, const float* lse,
+                                  void* ws, const WsLayout& L, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dk,
                             void* dv, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dq,

@@ -17,6 +17,7 @@ struct PlanParams {
   int B, H;
   int64_t total_q, total_kv;
   int causal, backward;
+  int grid;  // persistent CTAs of the kernels that consume the lists
   uint8_t* ws;
   WsLayout L;
   const float* bias;  // [H][nb] or nullptr
@@ -41,56 +42,96 @@ __device__ __forceinline__ int unit_cost(int kind, int u, int Lq, int Lk, bool c
   return count;
 }
 
-// Exclusive scan of hist[] in descending cost order: base[c] = sum_{c' > c} hist[c'].
-// 1024 threads, kCostBuckets = 2048 buckets (two per thread).  Returns the total.
-__device__ int scan_desc(const int* hist, int* base) {
-  __shared__ int warp_sums[32];
+// Block-wide inclusive scan of one 64-bit value per thread (blockDim.x == 1024).
+__device__ long long block_scan_incl(long long v, long long* total) {
+  __shared__ long long warp_sums[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // thread tid owns descending positions r = 2*tid, 2*tid+1  (bucket c = kCostBuckets-1-r)
-  const int c0 = kCostBuckets - 1 - 2 * tid, c1 = c0 - 1;
-  const int v0 = hist[c0], v1 = hist[c1];
-  int x = v0 + v1;
-  int incl = x;
+  long long incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
-    int wi = w;
+    const long long w = warp_sums[lane];
+    long long wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      const long long y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
-    warp_sums[lane] = wi - w;  // exclusive prefix of warp totals
+    warp_sums[lane] = wi - w;
+    if (lane == 31) *total = wi;
   }
   __syncthreads();
-  const int excl = warp_sums[warp] + incl - x;
+  const long long r = warp_sums[warp] + incl;
+  __syncthreads();
+  return r;
+}
+
+// Exclusive scan of hist[] in descending cost order: base[c] = sum_{c' > c} hist[c'].
+// 1024 threads, kCostBuckets = 2048 buckets (two per thread).  Returns the total.
+__device__ int scan_desc(const int* hist, int* base) {
+  __shared__ long long total;
+  const int tid = threadIdx.x;
+  // thread tid owns descending positions r = 2*tid, 2*tid+1  (bucket c = kCostBuckets-1-r)
+  const int c0 = kCostBuckets - 1 - 2 * tid, c1 = c0 - 1;
+  const int v0 = hist[c0], v1 = hist[c1];
+  const long long incl = block_scan_incl(v0 + v1, &total);
+  const int excl = int(incl) - (v0 + v1);
   base[c0] = excl;
   base[c1] = excl + v0;
   __syncthreads();
-  int total = base[0] + hist[0];
-  return total;
+  return int(total);
+}
+
+// Walk the units of one sequence, cutting them into consecutive ranges whose summed
+// cost stays <= cap (a unit costlier than cap forms its own range); calls f(u0, u1, cost).
+template <typename F>
+__device__ void for_each_range(int kind, int Lq, int Lk, bool causal, long long cap, F&& f) {
+  const int n = list_units(kind, Lq, Lk);
+  int start = 0;
+  long long acc = 0;
+  for (int u = 0; u < n; ++u) {
+    const int c = unit_cost(kind, u, Lq, Lk, causal);
+    if (u > start && acc + c > cap) {
+      f(start, u, acc);
+      start = u;
+      acc = 0;
+    }
+    acc += c;
+  }
+  if (n > 0) f(start, n, acc);
 }
 
 __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_t cap, int* count_out,
                           int* hist, int* base) {
+  __shared__ long long total_cost;
   const int tid = threadIdx.x;
   const bool causal = p.causal != 0;
+  // total work, to cap range cost at about 1/kItemsPerCta of a CTA's share
+  long long local = 0;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
+    const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
+    const int n = list_units(kind, Lq, Lk);
+    for (int u = 0; u < n; ++u) local += unit_cost(kind, u, Lq, Lk, causal);
+  }
+  block_scan_incl(local, &total_cost);
+  const long long share = (total_cost * p.H + (long long)kItemsPerCta * p.grid - 1) /
+                          ((long long)kItemsPerCta * p.grid);
+  const long long range_cap = share > 1 ? share : 1;
+
   for (int c = tid; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
   __syncthreads();
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
-    const int n = list_units(kind, Lq, Lk);
-    for (int u = 0; u < n; ++u) {
-      const int c = min(unit_cost(kind, u, Lq, Lk, causal), kCostBuckets - 1);
-      atomicAdd(&hist[c], p.H);
-    }
+    for_each_range(kind, Lq, Lk, causal, range_cap, [&](int, int, long long cost) {
+      atomicAdd(&hist[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
+    });
   }
   __syncthreads();
   const int total = scan_desc(hist, base);
@@ -104,16 +145,32 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
-    const int n = list_units(kind, Lq, Lk);
-    for (int u = 0; u < n; ++u) {
-      const int cost = unit_cost(kind, u, Lq, Lk, causal);
-      const int c = min(cost, kCostBuckets - 1);
-      const int pos = atomicAdd(&base[c], p.H);
-      for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u, cost};
-    }
+    for_each_range(kind, Lq, Lk, causal, range_cap, [&](int u0, int u1, long long cost) {
+      const int pos = atomicAdd(&base[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
+      for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u0, u1};
+    });
   }
   if (tid == 0) *count_out = total;
   __syncthreads();
+}
+
+// Backward: offsets of each sequence in the 128-row-padded per-query vectors.
+__device__ void write_qpad(const PlanParams& p) {
+  __shared__ long long chunk_total;
+  int64_t* qpad = reinterpret_cast<int64_t*>(p.ws + p.L.qpad);
+  long long carry = 0;
+  for (int b0 = 0; b0 < p.B; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    long long v = 0;
+    if (b < p.B) v = ((p.q_off[b + 1] - p.q_off[b]) + kBM - 1) / kBM * kBM;
+    const long long incl = block_scan_incl(v, &chunk_total);
+    if (b < p.B) qpad[b] = carry + incl - v;
+    carry += chunk_total;
+  }
+  if (threadIdx.x == 0) {
+    qpad[p.B] = carry;
+    reinterpret_cast<WsHeader*>(p.ws)->total_qpad = carry;
+  }
 }
 
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanMaps maps, PlanParams p) {
@@ -172,6 +229,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   if (!p.backward) {
     emit_list(p, kListFwd, reinterpret_cast<WorkItem*>(p.ws + p.L.fwd), p.L.cap_fwd, &hdr->n_fwd, hist, base);
   } else {
+    write_qpad(p);
     emit_list(p, kListDkv, reinterpret_cast<WorkItem*>(p.ws + p.L.dkv), p.L.cap_dkv, &hdr->n_dkv, hist,
               base);
     emit_list(p, kListDq, reinterpret_cast<WorkItem*>(p.ws + p.L.dq), p.L.cap_dq, &hdr->n_dq, hist, base);
@@ -181,7 +239,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
 }  // namespace
 
 cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const WsLayout& L, bool backward,
-                        cudaStream_t stream) {
+                        int num_sms, cudaStream_t stream) {
   PlanParams p;
   p.q_off = pr.q_off;
   p.kv_off = pr.kv_off;
@@ -191,6 +249,7 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   p.total_kv = pr.total_kv;
   p.causal = pr.causal;
   p.backward = backward ? 1 : 0;
+  p.grid = num_sms;
   p.ws = static_cast<uint8_t*>(ws);
   p.L = L;
   p.bias = pr.bias_table;

@@ -5,11 +5,11 @@ holds none of the attention arithmetic.  Both the CPU oracle and the CUDA path
 consume what it returns, so it is the single source of inputs for parity.
 
 Workloads (sequence-length mixes, head counts, head dims) follow the jagged
-recommendation workloads described on "Jagged Flash Attention (JFA)"
-(Definition: lengths "from hundreds to tens of thousands", asymmetric query and
-key/value lengths, custom attention biases; Results: jagged sparsity about 0.5).
-Production length distributions are not public; the uniform and log-normal mixes
-below stand in for them.
+recommendation workloads that "Jagged Flash Attention (JFA)" describes (Definition:
+user sequences from a few hundred up to tens of thousands of tokens, query and
+key/value lengths that differ, an additive bias; Results: jaggedness around one
+half).  Production length distributions are not public; the uniform and log-normal
+mixes below stand in for them.
 
 Draw order (one generator per call): lengths -> q -> k -> v -> bias -> dout.
 Values are float32 normal samples rounded to bfloat16 (round to nearest even);

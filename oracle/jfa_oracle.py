@@ -6,19 +6,20 @@ may import it; the library itself never calls it and has no CPU fallback.
 
 What it computes (plain definitions, no tiling, no fusion):
 
-* Exact softmax attention per jagged sequence -- "exact" attention as in the
+* Exact softmax attention per jagged sequence -- exact in the sense of the
   FlashAttention lineage that "TLX-Optimized Jagged Flash Attention" builds on
   (section "Why Jagged Flash Attention Deserves Attention": tiling plus online
   softmax never changes the result) -- applied directly to variable-length
   sequences packed as values plus int64 offsets ("Jagged Flash Attention (JFA)",
   Definition), with asymmetric query/key lengths and an additive per-head bias.
-* The backward of the same function (the "efficient backward passes" of the
-  Definition; the gradient formulas are the standard ones of FlashAttention-2).
+* The backward of the same function (the Definition lists a backward pass among
+  JFA's features; the gradient formulas are the standard ones of FlashAttention-2).
 * Two independent formulations used to pin the first one: brute-force padded
   dense attention with a -inf mask (the masking that "Four generations" item 1
   replaces), and a step-by-step float64 emulation of the tiled online softmax
   with zero-padded tails and the subtraction correction ("Four generations"
-  item 1: zero the padded Q/K rows, subtract the extra exponents).
+  item 1: padded rows enter as zeros and their exponentials are taken back out of
+  the row sum).
 
 Readings where the pages are silent (each also listed in the design notes):
 
