@@ -256,8 +256,8 @@ def run_jfa(args, rank, world, device):
     dq, dk, dv = torch.empty_like(batch.q), torch.empty_like(batch.k), torch.empty_like(batch.v)
     B, H, d = batch.q_lengths.numel(), cfg.heads, cfg.head_dim
     Tq, Tk = batch.q.shape[0], batch.k.shape[0]
-    ws_f = torch.empty(jfa.workspace_size(B, H, d, Tq, Tk, False), dtype=torch.uint8, device=device)
-    ws_b = torch.empty(jfa.workspace_size(B, H, d, Tq, Tk, True), dtype=torch.uint8, device=device)
+    ws_f = jfa.new_workspace(B, H, d, Tq, Tk, False, device)
+    ws_b = jfa.new_workspace(B, H, d, Tq, Tk, True, device)
 
     def fwd(q=batch.q, k=batch.k, v=batch.v, qo=batch.q_offsets, ko=batch.kv_offsets):
         jfa.jfa_forward(q, k, v, qo, ko, batch.bias, center, cfg.scale, cfg.causal, out=out, lse=lse,
@@ -270,8 +270,8 @@ def run_jfa(args, rank, world, device):
     for _ in range(args.warmup):
         fwd()
         bwd()
-    st = jfa.jfa_check_status(ws_f) or jfa.jfa_check_status(ws_b)
-    if st != 0:
+    st = (jfa.jfa_check_status(ws_f), jfa.jfa_check_status(ws_b))
+    if st != (0, 0):
         raise RuntimeError(f"device status {st} after warm-up")
     torch.cuda.synchronize()
 
@@ -311,9 +311,9 @@ def run_jfa(args, rank, world, device):
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    st = jfa.jfa_check_status(ws_f) or jfa.jfa_check_status(ws_b)
-    if st != 0:
-        raise RuntimeError(f"device status {st} in the timed region")
+    st = (jfa.jfa_check_status(ws_f), jfa.jfa_check_status(ws_b))
+    if st != (0, 0):
+        raise RuntimeError(f"device status {st} in the timed region (first error since warm-up)")
 
     # max over ranks of the timed region, sum of work over ranks
     t_local = torch.tensor([total_ms], dtype=torch.float64, device=device)

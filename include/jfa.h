@@ -28,13 +28,14 @@
  * The library allocates nothing, keeps no state between calls (one process-wide
  * cache of driver entry points aside), and enqueues all work asynchronously on
  * `stream`.  Scratch memory is the caller's `workspace` (size from
- * jfa_workspace_size, 256-byte aligned).  Calls sharing a workspace must not overlap.
+ * jfa_workspace_size, 256-byte aligned, and its first 256 bytes zero before its first
+ * use -- jfa_check_status keeps them so).  Calls sharing a workspace must not overlap.
  *
  * Errors.  Argument errors detectable on the host are returned synchronously and
  * enqueue nothing.  Errors found on the device (malformed offsets, a bounded
- * pipeline wait that ran out) are written to a status word in the workspace; read
- * it with jfa_check_status (which synchronises the stream).  On a device error the
- * outputs are unspecified.
+ * pipeline wait that ran out) are recorded in a status word in the workspace, the first
+ * one sticking until jfa_check_status (which synchronises the stream) reads and clears
+ * it.  On a device error the outputs of that call are unspecified.
  *
  * Requirements.  d in {64, 128}; H >= 1; B >= 1; every tensor pointer 16-byte
  * aligned; an sm_100-family GPU (built for sm_103a).
@@ -118,8 +119,9 @@ jfa_status jfa_forward_noalloc(const void* q, const void* k, const void* v, cons
                                const jfa_bias* bias, float scale, int causal, void* out, float* lse,
                                jfa_stream_t stream);
 
-/* Synchronises `stream`, then returns the device status word of the last call that
- * used `workspace` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT) and clears it. */
+/* Synchronises `stream`, then returns the first device-side error recorded in
+ * `workspace` since the previous jfa_check_status (JFA_OK if none; else
+ * JFA_ERR_BAD_OFFSETS, JFA_ERR_TIMEOUT or JFA_ERR_WORKSPACE) and clears it. */
 jfa_status jfa_check_status(void* workspace, jfa_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */

@@ -89,29 +89,43 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
     const int Lq = int(p.q_off[it.b + 1] - qo);
     const int64_t pad0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
     for (int t = it.u0; t < it.u1; ++t) {
-      for (int r = warp; r < kBM; r += 8) {
-        const int i = t * kBM + r;
-        float acc = 0.f, l2 = 0.f;
-        if (i < Lq) {
-          const int64_t e0 = ((qo + i) * p.H + it.h) * int64_t(D);
-          if (D == 128) {
-            const uint2 a = __ldg(reinterpret_cast<const uint2*>(p.dout + e0) + lane);
-            const uint2 b = __ldg(reinterpret_cast<const uint2*>(p.out + e0) + lane);
-            acc = fmaf(bf16lo(a.x), bf16lo(b.x),
-                       fmaf(bf16hi(a.x), bf16hi(b.x), fmaf(bf16lo(a.y), bf16lo(b.y), bf16hi(a.y) * bf16hi(b.y))));
-          } else {
-            const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(p.dout + e0) + lane);
-            const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(p.out + e0) + lane);
-            acc = fmaf(bf16lo(a), bf16lo(b), bf16hi(a) * bf16hi(b));
-          }
+      // 8 warps x 16 rows; each warp keeps 4 rows' loads in flight
+      for (int rb = 0; rb < kBM / 8; rb += 4) {
+        float acc[4], l2[4];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-          const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
-          l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+        for (int k = 0; k < 4; ++k) {
+          const int i = t * kBM + warp + 8 * (rb + k);
+          acc[k] = 0.f;
+          l2[k] = 0.f;
+          if (i < Lq) {
+            const int64_t e0 = ((qo + i) * p.H + it.h) * int64_t(D);
+            if (D == 128) {
+              const uint2 a = __ldg(reinterpret_cast<const uint2*>(p.dout + e0) + lane);
+              const uint2 b = __ldg(reinterpret_cast<const uint2*>(p.out + e0) + lane);
+              acc[k] = fmaf(bf16lo(a.x), bf16lo(b.x),
+                            fmaf(bf16hi(a.x), bf16hi(b.x), fmaf(bf16lo(a.y), bf16lo(b.y), bf16hi(a.y) * bf16hi(b.y))));
+            } else {
+              const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(p.dout + e0) + lane);
+              const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(p.out + e0) + lane);
+              acc[k] = fmaf(bf16lo(a), bf16lo(b), bf16hi(a) * bf16hi(b));
+            }
+            const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
+            l2[k] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+          }
         }
-        if (lane == 0) {
-          p.delta[pad0 + i] = acc;
-          p.lse2[pad0 + i] = l2;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+        }
+        if (lane < 4) {
+          float a = acc[0], l = l2[0];
+#pragma unroll
+          for (int k = 1; k < 4; ++k)
+            if (lane == k) a = acc[k], l = l2[k];
+          const int i = t * kBM + warp + 8 * (rb + lane);
+          p.delta[pad0 + i] = a;
+          p.lse2[pad0 + i] = l;
         }
       }
     }
@@ -121,10 +135,15 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = D == 128 ? 2 : 3;  // ring stages, each two tiles
+  static constexpr int kRingDkdv = D == 128 ? 4 : 8;  // single-tile ring entries
+  static constexpr int kRingDq = D == 128 ? 5 : 8;
+  static constexpr int kVecSlots = 4;                  // dK/dV: per-query-tile lse2 / D vectors
+  // dK/dV pass: S^T, dP^T, dK, dV.   dQ pass: S, dP (two buffers), dQ.
   static constexpr uint32_t kColS = 0, kColP = 128, kColA0 = 256, kColA1 = 256 + D;
-  // resident pair (K,V or Q,dO) + ring of pairs + per-stage lse/D vectors
-  static constexpr int kSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes + kStages * 2 * 128 * 4 + 1024;
+  static constexpr uint32_t kColP1 = 256, kColDQ = 384;
+  static constexpr int kSmemDkdv = 2 * kTileBytes + kRingDkdv * kTileBytes + kVecSlots * 1024 + 1024;
+  static constexpr int kSmemDq = 2 * kTileBytes + kRingDq * kTileBytes + 1024;
+  static_assert(kSmemDkdv <= 232448 && kSmemDq <= 232448, "shared memory per CTA");
 };
 
 // Load one row-tile (128 rows x D columns, D/64 boxes of 16 KB) through a tensor map.
@@ -178,18 +197,23 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
 }
 
 // ================================================================== dK / dV pass
+// Ring of single tiles, filled in the order dO_i, Q_i for the query tiles i of each key
+// tile: dO_i is released after dV(i) and Q_i after dK(i), i.e. in fill order.  Each Q_i
+// brings its tile's lse2 and D vectors (vector slot = query tile count mod kVecSlots; a
+// slot is refilled only after dK of its previous tile completed).
 template <int D, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
+  constexpr int R = C::kRingDkdv;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kTileBytes;
-  uint8_t* sRing = smem + 2 * C::kTileBytes;  // stage s: Q at 2s, dO at 2s+1
-  float* sVec = reinterpret_cast<float*>(sRing + C::kStages * 2 * C::kTileBytes);  // [stage][2][128]: lse2, D
+  uint8_t* sRing = smem + 2 * C::kTileBytes;
+  float* sVec = reinterpret_cast<float*>(sRing + R * C::kTileBytes);  // [kVecSlots][2][128]: lse2, D
 
   __shared__ uint64_t kv_full, kv_empty, st_full, dpt_full, p_full, ds_full, acc_full, acc_empty, mma_done;
-  __shared__ uint64_t stage_full[C::kStages], stage_empty[C::kStages];
+  __shared__ uint64_t ring_full[R], ring_empty[R];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -205,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, 256);
     mbar_init(&mma_done, 1);
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&stage_full[i], 1);
-      mbar_init(&stage_empty[i], 1);
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
     }
     fence_mbar_init();
   }
@@ -222,17 +246,35 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
   const int n_items = *p.n_items;
   volatile int* abort_flag = &abort_sh;
   const bool causal = p.causal != 0;
+  auto seq_len = [&](int b, int* Lq, int* Lk) {
+    *Lq = int(p.q_off[b + 1] - p.q_off[b]);
+    *Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
+  };
 
   if (warp < kFirstComputeWarp) {
    setmaxnreg_dec<kRegsLoad>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t stage_n = 0, item_n = 0;
+      uint32_t ring_n = 0, item_n = 0, qtile_n = 0;
       bool ok = true;
+      auto fill = [&](const CUtensorMap* m, int col, int row, const float* l2src, const float* dsrc) {
+        const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes + (l2src ? 2 * kBM * 4 : 0));
+        load_tile<D>(sRing + e * C::kTileBytes, m, &ring_full[e], col, row);
+        if (l2src) {
+          float* v = sVec + (qtile_n % C::kVecSlots) * 256;
+          bulk_load(v, l2src, kBM * 4, &ring_full[e]);
+          bulk_load(v + 128, dsrc, kBM * 4, &ring_full[e]);
+        }
+        ++ring_n;
+        return true;
+      };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         const WorkItem wi = p.items[idx];
-        const int Lq = int(p.q_off[wi.b + 1] - p.q_off[wi.b]), Lk = int(p.kv_off[wi.b + 1] - p.kv_off[wi.b]);
+        int Lq, Lk;
+        seq_len(wi.b, &Lq, &Lk);
         const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
         const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
         const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
@@ -241,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         tmap_acquire(mk);
         tmap_acquire(mv);
         tmap_acquire(mdo);
-        // this (sequence, head)'s 128-row-padded lse2 and D vectors
         const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + p.qpad[wi.b];
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
@@ -252,90 +293,103 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
           load_tile<D>(sK, mk, &kv_full, wi.h * D, kt * kBN);
           load_tile<D>(sV, mv, &kv_full, wi.h * D, kt * kBN);
           ++item_n;
-          for (int i = 0; i < count; ++i) {
+          // the next key tile of this range is loaded only once this one is done:
+          // pull it into L2 now
+          if (kt + 1 < wi.u1) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              tma_prefetch_2d(mk, wi.h * D + c * 64, (kt + 1) * kBN);
+              tma_prefetch_2d(mv, wi.h * D + c * 64, (kt + 1) * kBN);
+            }
+          }
+          for (int i = 0; i < count && ok; ++i) {
             const int qt = first + i;
-            const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
-            if (!mbar_wait(&stage_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-            mbar_arrive_expect_tx(&stage_full[e], 2 * C::kTileBytes + 2 * kBM * 4);
-            uint8_t* dst = sRing + e * 2 * C::kTileBytes;
-            load_tile<D>(dst, mq, &stage_full[e], wi.h * D, qt * kBM);
-            load_tile<D>(dst + C::kTileBytes, mdo, &stage_full[e], wi.h * D, qt * kBM);
-            bulk_load(sVec + e * 256, p.lse2 + vec0 + qt * kBM, kBM * 4, &stage_full[e]);
-            bulk_load(sVec + e * 256 + 128, p.delta + vec0 + qt * kBM, kBM * 4, &stage_full[e]);
-            ++stage_n;
+            if (!fill(mdo, wi.h * D, qt * kBM, nullptr, nullptr)) { ok = false; break; }
+            if (!fill(mq, wi.h * D, qt * kBM, p.lse2 + vec0 + qt * kBM, p.delta + vec0 + qt * kBM)) {
+              ok = false;
+              break;
+            }
+            ++qtile_n;
           }
         }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
-      const uint32_t f = stage_n > C::kStages ? stage_n - C::kStages : 0;
-      for (uint32_t n = f; n < stage_n; ++n) drain_wait(&stage_full[n % C::kStages], (n / C::kStages) & 1);
+      const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
+      for (uint32_t n = f; n < ring_n; ++n) drain_wait(&ring_full[n % R], (n / R) & 1);
       if (item_n > 0) drain_wait(&kv_full, (item_n - 1) & 1);
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(sRing);
-      uint32_t stage_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
+      uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
         if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
         tc_fence_after();
         return true;
       };
+      auto wait_ring = [&](uint32_t n) { return wait(&ring_full[n % R], (n / R) & 1); };
+      auto ra = [&](uint32_t n) { return aR + (n % R) * C::kTileBytes; };
       // S^T (or dP^T) = A_tile(keys x D) * B_tile(queries x D)^T, both K-major
       auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
+        const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + dcol, sdesc_sw128(a + o, 16, 1024), sdesc_sw128(b + o, 16, 1024), kIdS, kk > 0);
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
         }
       };
       // acc(keys x D) += X^T (TMEM bf16, keys x 128 queries, two 64-column halves) * B(queries x D, MN-major)
       auto mma_acc = [&](uint32_t dcol, uint32_t xcol, uint32_t b, bool acc) {
+        const uint64_t bd = sdesc_sw128(b, 16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(b + kk * 2048, 16384, 1024),
-                  kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * 64 + (kk & 3) * 8, bd + uint32_t(kk * 2048 >> 4), kIdAcc,
+                  (acc || kk > 0) ? 1u : 0u);
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
        const WorkItem wi = p.items[idx];
-       const int Lq = int(p.q_off[wi.b + 1] - p.q_off[wi.b]), Lk = int(p.kv_off[wi.b + 1] - p.kv_off[wi.b]);
+       int Lq, Lk;
+       seq_len(wi.b, &Lq, &Lk);
        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
         int first, count;
         q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
         if (count == 0) continue;
         if (!wait(&kv_full, item_n & 1)) { ok = false; break; }
         ++item_n;
-        const uint32_t s0 = stage_n;
-        auto qa = [&](uint32_t n) { return aR + (n % C::kStages) * 2 * C::kTileBytes; };
-        if (!wait(&stage_full[s0 % C::kStages], (s0 / C::kStages) & 1)) { ok = false; break; }
-        mma_nt(C::kColS, aK, qa(s0));
+        const uint32_t n0 = ring_n;  // dO_i at n0 + 2i, Q_i at n0 + 2i + 1
+        if (!wait_ring(n0 + 1)) { ok = false; break; }
+        mma_nt(C::kColS, aK, ra(n0 + 1));
         umma_commit(&st_full);
-        mma_nt(C::kColP, aV, qa(s0) + C::kTileBytes);
+        if (!wait_ring(n0)) { ok = false; break; }
+        mma_nt(C::kColP, aV, ra(n0));
         umma_commit(&dpt_full);
         for (int i = 0; i < count && ok; ++i) {
-          const uint32_t n = s0 + i;
+          const uint32_t nd = n0 + 2 * i, nq = nd + 1;
           if (!wait(&p_full, tile_n & 1)) { ok = false; break; }
           if (i == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
-          mma_acc(C::kColA1, C::kColS, qa(n) + C::kTileBytes, i > 0);  // dV += P^T dO
+          mma_acc(C::kColA1, C::kColS, ra(nd), i > 0);  // dV += P^T dO
+          umma_commit(&ring_empty[nd % R]);
           if (i + 1 < count) {
-            if (!wait(&stage_full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1)) { ok = false; break; }
-            mma_nt(C::kColS, aK, qa(n + 1));
+            if (!wait_ring(nq + 2)) { ok = false; break; }
+            mma_nt(C::kColS, aK, ra(nq + 2));
             umma_commit(&st_full);
           }
           if (!wait(&ds_full, tile_n & 1)) { ok = false; break; }
           ++tile_n;
-          mma_acc(C::kColA0, C::kColP, qa(n), i > 0);  // dK += dS^T Q
-          umma_commit(&stage_empty[n % C::kStages]);
+          mma_acc(C::kColA0, C::kColP, ra(nq), i > 0);  // dK += dS^T Q
+          umma_commit(&ring_empty[nq % R]);
           if (i + 1 < count) {
-            mma_nt(C::kColP, aV, qa(n + 1) + C::kTileBytes);
+            if (!wait_ring(nd + 2)) { ok = false; break; }
+            mma_nt(C::kColP, aV, ra(nd + 2));
             umma_commit(&dpt_full);
           }
         }
         if (!ok) break;
-        stage_n = s0 + count;
+        ring_n = n0 + 2 * count;
         ++acc_n;
         umma_commit(&acc_full);
         umma_commit(&kv_empty);
@@ -345,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
-  }
+   }
   } else {
     setmaxnreg_inc<kRegsCompute>();
     // ------------------------------------------------------------ compute warpgroups
@@ -356,12 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
     const float sl2 = p.scale_log2;
-    uint32_t stage_n = 0, tile_n = 0, acc_n = 0;
+    uint32_t ring_n = 0, tile_n = 0, acc_n = 0, qtile_n = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
      const WorkItem it = p.items[idx];
-     const int64_t qo = p.q_off[it.b], ko = p.kv_off[it.b];
-     const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - ko);
+     const int64_t ko = p.kv_off[it.b];
+     int Lq, Lk;
+     seq_len(it.b, &Lq, &Lk);
      for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
       int first, count;
       q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
@@ -378,11 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       for (int i = 0; i < count && ok; ++i) {
         const int qt = first + i;
-        const uint32_t e = stage_n % C::kStages;
-        if (!mbar_wait(&stage_full[e], (stage_n / C::kStages) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-        ++stage_n;
-        const float* lse2 = sVec + e * 256 + 64 * w;
-        const float* dvec = sVec + e * 256 + 128 + 64 * w;
+        // Q_i's ring slot carries this tile's lse2 / D vectors: wait for it
+        const uint32_t nq = ring_n + 1;
+        if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ring_n += 2;
+        const float* vec = sVec + (qtile_n % C::kVecSlots) * 256;
+        ++qtile_n;
+        const float* lse2 = vec + 64 * w;
+        const float* dvec = vec + 128 + 64 * w;
         if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         float x[64];
@@ -468,17 +526,26 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
 }
 
 // ================================================================== dQ pass
+// Ring of single tiles, filled V_j, K_j per key tile: V_j is released after dP(j), K_j
+// after dQ(j), i.e. in fill order.  S and dP of the next key tile are issued as soon as
+// the warpgroups hold S in registers, so the dP/dS buffer alternates by tile parity.
 template <int D, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
+  constexpr int R = C::kRingDq;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + C::kTileBytes;
-  uint8_t* sRing = smem + 2 * C::kTileBytes;  // stage s: K at 2s, V at 2s+1
+  uint8_t* sRing = smem + 2 * C::kTileBytes;
 
-  __shared__ uint64_t qdo_full, qdo_empty, s_full, s_free, dp_full, ds_full, acc_full, acc_empty, mma_done;
-  __shared__ uint64_t stage_full[C::kStages], stage_empty[C::kStages];
+  __shared__ uint64_t qdo_full, qdo_empty, s_full, s_free, acc_full, acc_empty, mma_done;
+  // dp_full / ds_full of global tile g live at index g & 1: dP(g+1) is issued before dQ(g)
+  // waits for dS(g), so one warpgroup may finish tile g+1 while the other still works on
+  // tile g (never further: S(g+2) waits for both warpgroups' s_free(g+1)); separate
+  // barriers per tile parity keep their arrivals apart.
+  __shared__ uint64_t dp_full[2], ds_full[2];
+  __shared__ uint64_t ring_full[R], ring_empty[R];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -489,14 +556,16 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     mbar_init(&qdo_empty, 1);
     mbar_init(&s_full, 1);
     mbar_init(&s_free, 256);
-    mbar_init(&dp_full, 1);
-    mbar_init(&ds_full, 256);
+    mbar_init(&dp_full[0], 1);
+    mbar_init(&dp_full[1], 1);
+    mbar_init(&ds_full[0], 256);
+    mbar_init(&ds_full[1], 256);
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, 256);
     mbar_init(&mma_done, 1);
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&stage_full[i], 1);
-      mbar_init(&stage_empty[i], 1);
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
     }
     fence_mbar_init();
   }
@@ -511,111 +580,134 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   const int n_items = *p.n_items;
   volatile int* abort_flag = &abort_sh;
   const bool causal = p.causal != 0;
+  auto colP = [](uint32_t g) { return (g & 1) ? C::kColP1 : C::kColP; };
+  auto seq_len = [&](int b, int* Lq, int* Lk) {
+    *Lq = int(p.q_off[b + 1] - p.q_off[b]);
+    *Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
+  };
 
   if (warp < kFirstComputeWarp) {
    setmaxnreg_dec<kRegsLoad>();
    if (warp == 0) {
     if (lane == 0) {
-      uint32_t stage_n = 0, item_n = 0;
+      uint32_t ring_n = 0, item_n = 0;
       bool ok = true;
+      auto fill = [&](const CUtensorMap* m, int col, int row) {
+        const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
+        load_tile<D>(sRing + e * C::kTileBytes, m, &ring_full[e], col, row);
+        ++ring_n;
+        return true;
+      };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
        const WorkItem wi = p.items[idx];
+       int Lq, Lk;
+       seq_len(wi.b, &Lq, &Lk);
+       const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
+       const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
+       const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
+       const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
+       tmap_acquire(mq);
+       tmap_acquire(mk);
+       tmap_acquire(mv);
+       tmap_acquire(mdo);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
-        WorkItem it = wi;
-        it.u0 = qt;
-        const int Lq = int(p.q_off[it.b + 1] - p.q_off[it.b]), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         if (nkv == 0) continue;
-        const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
-        const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
-        const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
-        const CUtensorMap* mdo = p.maps + size_t(it.b) * kNumMapSlots + kMapDO;
-        tmap_acquire(mq);
-        tmap_acquire(mk);
-        tmap_acquire(mv);
-        tmap_acquire(mdo);
         if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
-        load_tile<D>(sQ, mq, &qdo_full, it.h * D, qt * kBM);
-        load_tile<D>(sDO, mdo, &qdo_full, it.h * D, qt * kBM);
+        load_tile<D>(sQ, mq, &qdo_full, wi.h * D, qt * kBM);
+        load_tile<D>(sDO, mdo, &qdo_full, wi.h * D, qt * kBM);
         ++item_n;
-        for (int jt = 0; jt < nkv; ++jt) {
-          const uint32_t e = stage_n % C::kStages, ph = (stage_n / C::kStages) & 1;
-          if (!mbar_wait(&stage_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-          mbar_arrive_expect_tx(&stage_full[e], 2 * C::kTileBytes);
-          uint8_t* dst = sRing + e * 2 * C::kTileBytes;
-          load_tile<D>(dst, mk, &stage_full[e], it.h * D, jt * kBN);
-          load_tile<D>(dst + C::kTileBytes, mv, &stage_full[e], it.h * D, jt * kBN);
-          ++stage_n;
+        // the next query tile of this range is loaded only once this one is done:
+        // pull it into L2 now
+        if (qt + 1 < wi.u1) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_2d(mq, wi.h * D + c * 64, (qt + 1) * kBM);
+            tma_prefetch_2d(mdo, wi.h * D + c * 64, (qt + 1) * kBM);
+          }
+        }
+        for (int jt = 0; jt < nkv && ok; ++jt) {
+          if (!fill(mv, wi.h * D, jt * kBN) || !fill(mk, wi.h * D, jt * kBN)) { ok = false; break; }
         }
        }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
-      const uint32_t f = stage_n > C::kStages ? stage_n - C::kStages : 0;
-      for (uint32_t n = f; n < stage_n; ++n) drain_wait(&stage_full[n % C::kStages], (n / C::kStages) & 1);
+      const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
+      for (uint32_t n = f; n < ring_n; ++n) drain_wait(&ring_full[n % R], (n / R) & 1);
       if (item_n > 0) drain_wait(&qdo_full, (item_n - 1) & 1);
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aR = smem_u32(sRing);
-      uint32_t stage_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
+      uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
         if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
         tc_fence_after();
         return true;
       };
+      auto wait_ring = [&](uint32_t n) { return wait(&ring_full[n % R], (n / R) & 1); };
+      auto ra = [&](uint32_t n) { return aR + (n % R) * C::kTileBytes; };
       auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
+        const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + dcol, sdesc_sw128(a + o, 16, 1024), sdesc_sw128(b + o, 16, 1024), kIdS, kk > 0);
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
         }
       };
-      auto ka = [&](uint32_t n) { return aR + (n % C::kStages) * 2 * C::kTileBytes; };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
        const WorkItem wi = p.items[idx];
-       const int Lq = int(p.q_off[wi.b + 1] - p.q_off[wi.b]), Lk = int(p.kv_off[wi.b + 1] - p.kv_off[wi.b]);
+       int Lq, Lk;
+       seq_len(wi.b, &Lq, &Lk);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         if (nkv == 0) continue;
         if (!wait(&qdo_full, item_n & 1)) { ok = false; break; }
         ++item_n;
-        const uint32_t s0 = stage_n;
-        if (!wait(&stage_full[s0 % C::kStages], (s0 / C::kStages) & 1)) { ok = false; break; }
-        mma_nt(C::kColS, aQ, ka(s0));
+        const uint32_t n0 = ring_n;  // V_j at n0 + 2j, K_j at n0 + 2j + 1
+        if (!wait_ring(n0 + 1)) { ok = false; break; }
+        mma_nt(C::kColS, aQ, ra(n0 + 1));
         umma_commit(&s_full);
-        mma_nt(C::kColP, aDO, ka(s0) + C::kTileBytes);
-        umma_commit(&dp_full);
+        if (!wait_ring(n0)) { ok = false; break; }
+        mma_nt(colP(tile_n), aDO, ra(n0));
+        umma_commit(&dp_full[tile_n & 1]);
+        umma_commit(&ring_empty[n0 % R]);
         for (int jt = 0; jt < nkv && ok; ++jt) {
-          const uint32_t n = s0 + jt;
+          const uint32_t g = tile_n;  // global tile index
+          const uint32_t nv = n0 + 2 * jt, nk = nv + 1;
           if (jt + 1 < nkv) {
-            if (!wait(&s_free, tile_n & 1)) { ok = false; break; }
-            if (!wait(&stage_full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1)) { ok = false; break; }
-            mma_nt(C::kColS, aQ, ka(n + 1));
+            // next S once the warpgroups hold this S in registers; next dP into the
+            // other buffer (its dS was consumed by the dQ MMA issued before)
+            if (!wait(&s_free, g & 1)) { ok = false; break; }
+            if (!wait_ring(nk + 2)) { ok = false; break; }
+            mma_nt(C::kColS, aQ, ra(nk + 2));
             umma_commit(&s_full);
+            if (!wait_ring(nv + 2)) { ok = false; break; }
+            mma_nt(colP(g + 1), aDO, ra(nv + 2));
+            umma_commit(&dp_full[(g + 1) & 1]);
+            umma_commit(&ring_empty[(nv + 2) % R]);
           }
-          if (!wait(&ds_full, tile_n & 1)) { ok = false; break; }
+          if (!wait(&ds_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
           ++tile_n;
           if (jt == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
           // dQ += dS (TMEM, queries x keys) * K (keys x D, MN-major)
-          const uint32_t kb = ka(n);
+          const uint64_t kd = sdesc_sw128(ra(nk), 16384, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(tmem + C::kColA0, tmem + C::kColP + (kk >> 2) * 64 + (kk & 3) * 8,
-                    sdesc_sw128(kb + kk * 2048, 16384, 1024), kIdAcc, (jt > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&stage_empty[n % C::kStages]);
-          if (jt + 1 < nkv) {
-            mma_nt(C::kColP, aDO, ka(n + 1) + C::kTileBytes);
-            umma_commit(&dp_full);
-          }
+            umma_ts(tmem + C::kColDQ, tmem + colP(g) + (kk >> 2) * 64 + (kk & 3) * 8, kd + uint32_t(kk * 2048 >> 4),
+                    kIdAcc, (jt > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&ring_empty[nk % R]);
         }
         if (!ok) break;
         // the last tile's s_free arrival has no consumer above: take it here
-        if (!wait(&s_free, tile_n - 1 & 1)) { ok = false; break; }
-        stage_n = s0 + nkv;
+        if (!wait(&s_free, (tile_n - 1) & 1)) { ok = false; break; }
+        ring_n = n0 + 2 * nkv;
         ++acc_n;
         umma_commit(&acc_full);
         umma_commit(&qdo_empty);
@@ -625,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
-  }
+   }
   } else {
     setmaxnreg_inc<kRegsCompute>();
     const int w = (warp - kFirstComputeWarp) >> 2;  // key columns [64w, 64w+64)
@@ -633,14 +725,14 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
-    const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
     const float sl2 = p.scale_log2;
     uint32_t tile_n = 0, acc_n = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
      const WorkItem it = p.items[idx];
      const int64_t qo = p.q_off[it.b];
-     const int Lq = int(p.q_off[it.b + 1] - qo), Lk = int(p.kv_off[it.b + 1] - p.kv_off[it.b]);
+     int Lq, Lk;
+     seq_len(it.b, &Lq, &Lk);
      const int64_t vec0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
      for (int qt = it.u0; qt < it.u1 && ok; ++qt) {
       const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
@@ -695,7 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         }
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P
-        if (!mbar_wait(&dp_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        const uint32_t g = tile_n;
+        const uint32_t tP = tmem + lane_addr + colP(g) + 64 * w;
+        if (!mbar_wait(&dp_full[g & 1], (g >> 1) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
         float dp[64];
@@ -705,13 +799,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         st_bf16_64(tP, dp);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&ds_full);
+        mbar_arrive(&ds_full[g & 1]);
       }
       if (!ok) break;
       if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
-      store_acc_row(tmem + lane_addr + C::kColA0 + w * (D / 2), D / 2, p.scale, dq_row, valid, false);
+      store_acc_row(tmem + lane_addr + C::kColDQ + w * (D / 2), D / 2, p.scale, dq_row, valid, false);
       tc_fence_before();
       mbar_arrive(&acc_empty);
      }
@@ -783,9 +877,9 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   pp.lse2 = reinterpret_cast<float*>(w + L.lse2);
   pp.delta = reinterpret_cast<float*>(w + L.delta);
   if (pr.d == 128)
-    preprocess_kernel<128><<<4 * num_sms, 256, 0, stream>>>(pp);
+    preprocess_kernel<128><<<8 * num_sms, 256, 0, stream>>>(pp);
   else
-    preprocess_kernel<64><<<4 * num_sms, 256, 0, stream>>>(pp);
+    preprocess_kernel<64><<<8 * num_sms, 256, 0, stream>>>(pp);
   return cudaGetLastError();
 }
 
@@ -796,10 +890,10 @@ cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const
   bp.g1 = static_cast<__nv_bfloat16*>(dv);
   const bool bias = pr.bias_table != nullptr;
   if (pr.d == 128)
-    return bias ? launch_big(dkdv_kernel<128, true>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream)
-                : launch_big(dkdv_kernel<128, false>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream);
-  return bias ? launch_big(dkdv_kernel<64, true>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream)
-              : launch_big(dkdv_kernel<64, false>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream);
+    return bias ? launch_big(dkdv_kernel<128, true>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream)
+                : launch_big(dkdv_kernel<128, false>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream);
+  return bias ? launch_big(dkdv_kernel<64, true>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream)
+              : launch_big(dkdv_kernel<64, false>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream);
 }
 
 cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, int num_sms,
@@ -808,10 +902,10 @@ cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const W
   bp.g0 = static_cast<__nv_bfloat16*>(dq);
   const bool bias = pr.bias_table != nullptr;
   if (pr.d == 128)
-    return bias ? launch_big(dq_kernel<128, true>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream)
-                : launch_big(dq_kernel<128, false>, BwdCfg<128>::kSmemBytes, num_sms, bp, stream);
-  return bias ? launch_big(dq_kernel<64, true>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream)
-              : launch_big(dq_kernel<64, false>, BwdCfg<64>::kSmemBytes, num_sms, bp, stream);
+    return bias ? launch_big(dq_kernel<128, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
+                : launch_big(dq_kernel<128, false>, BwdCfg<128>::kSmemDq, num_sms, bp, stream);
+  return bias ? launch_big(dq_kernel<64, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
+              : launch_big(dq_kernel<64, false>, BwdCfg<64>::kSmemDq, num_sms, bp, stream);
 }
 
 }  // namespace jfa

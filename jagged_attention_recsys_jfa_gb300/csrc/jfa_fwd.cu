@@ -166,6 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           if (it.has1) tma_load_2d(sQ + C::kTileBytes + c * 16384, mq, &q_full, it.h * D + c * 64, it.t1 * kBM);
         }
         ++item_n;
+        // the next query-tile pair of this range loads only after this pair's last S
+        // MMA: pull it into L2 now
+        if (u + 1 < wi.u1) {
+#pragma unroll
+          for (int c = 0; c < C::kBoxes; ++c)
+            for (int t = 2 * (u + 1); t < 2 * (u + 1) + 2 && t * kBM < it.Lq; ++t)
+              tma_prefetch_2d(mq, it.h * D + c * 64, t * kBM);
+        }
         for (int j = 0; j < it.njt && ok; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
@@ -412,15 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       const bool live = l > 0.f;
       const float inv_l = live ? 1.f / l : 0.f;
       const float m_use = (m == -INFINITY) ? 0.f : m;
+      // all of the row's O columns in flight before one wait
+      uint32_t o_r[D / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, o_r[cc]);
+      tmem_ld_wait();
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tO + cc * 32, r);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int t2 = 0; t2 < 16; ++t2)
-          pk[t2] = pack_bf16x2(__uint_as_float(r[2 * t2]) * inv_l, __uint_as_float(r[2 * t2 + 1]) * inv_l);
+          pk[t2] = pack_bf16x2(__uint_as_float(o_r[cc][2 * t2]) * inv_l, __uint_as_float(o_r[cc][2 * t2 + 1]) * inv_l);
         if (valid_row) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll

@@ -178,7 +178,6 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   __shared__ int base[kCostBuckets];
   const int tid = threadIdx.x;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
-  if (tid == 0) hdr->status = 0;
 
   // ---- bias table pre-scaled to log2 units (the kernels work with exp2)
   if (p.bias) {
@@ -200,7 +199,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) {
-      hdr->status = int(JFA_ERR_BAD_OFFSETS);
+      atomicCAS(&hdr->status, 0, int(JFA_ERR_BAD_OFFSETS));
       hdr->n_fwd = hdr->n_dq = hdr->n_dkv = 0;
     }
     return;

@@ -134,9 +134,15 @@ def workspace_size(B, H, d, total_q, total_kv, backward) -> int:
     return int(load_library().jfa_workspace_size(B, H, d, total_q, total_kv, 1 if backward else 0))
 
 
+def new_workspace(B, H, d, total_q, total_kv, backward, device) -> torch.Tensor:
+    """A zero-initialised workspace for jfa_forward (backward=False) or jfa_backward."""
+    return _workspace(workspace_size(B, H, d, total_q, total_kv, backward), device)
+
+
 def _workspace(nbytes, device):
-    # 256-byte alignment is guaranteed by the caching allocator
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    # 256-byte alignment is guaranteed by the caching allocator; the status header must
+    # start zeroed
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,
