@@ -147,6 +147,15 @@ enum { JFA_KERNEL_PLAN = 0, JFA_KERNEL_FORWARD = 1, JFA_KERNEL_BWD_PREPROCESS = 
 jfa_status jfa_timing_enable(int on);
 jfa_status jfa_timing_read(double* ms, int* launches, int n_kinds);
 
+/* Developer tracing (not part of the attention itself).  With a non-NULL device buffer,
+ * kernels of `kernel_kind` (JFA_KERNEL_*) launched afterwards record the pipeline events
+ * of their first CTA: uint64 entries (SM clock << 16 | role << 8 | event id) in five
+ * regions of bytes/40 entries, one per warp role (0 streaming TMA producer, 1 MMA issuer,
+ * 2 and 3 the two compute warpgroups, 4 resident-tile loader); each launch overwrites
+ * them; unused entries are left as they were.  A NULL buffer or a kind outside [0, JFA_NUM_KERNEL_KINDS) turns tracing off.
+ * Process-wide; returns JFA_ERR_INVALID_ARG for a buffer too small or not 8-byte aligned. */
+jfa_status jfa_trace_configure(void* device_buffer, size_t bytes, int kernel_kind);
+
 #ifdef __cplusplus
 }
 #endif

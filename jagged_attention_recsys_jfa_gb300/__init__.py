@@ -12,6 +12,8 @@ from .jfa import (  # noqa: F401
     jfa_last_launch_count,
     jfa_timing_enable,
     jfa_timing_read,
+    jfa_trace_configure,
+    decode_trace,
     KERNEL_KINDS,
     library_path,
     load_library,

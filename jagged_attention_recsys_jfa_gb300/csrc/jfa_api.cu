@@ -39,6 +39,11 @@ std::mutex g_timing_mu;
 bool g_timing_on = false;
 std::vector<TimingRec> g_timing;
 
+// ---- optional developer tracing (one kernel kind at a time)
+std::mutex g_trace_mu;
+TraceBuf g_trace = {nullptr, 0};
+int g_trace_kind = -1;
+
 struct KernelTimer {
   int kind;
   cudaStream_t stream;
@@ -147,6 +152,8 @@ Problem make_problem(int B, int H, int d, int64_t total_q, int64_t total_kv, con
   p.bias_table = has_bias ? bias->table : nullptr;
   p.num_buckets = has_bias ? bias->num_buckets : 0;
   p.center = has_bias ? bias->center : 0;
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  for (int k = 0; k < 5; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
   return p;
 }
 
@@ -298,6 +305,20 @@ const char* jfa_status_string(jfa_status s) {
 int jfa_last_launch_count(void) { return g_last_launches; }
 
 const char* jfa_last_error(void) { return g_last_error; }
+
+jfa_status jfa_trace_configure(void* device_buffer, size_t bytes, int kernel_kind) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  if (!device_buffer || kernel_kind < 0 || kernel_kind >= JFA_NUM_KERNEL_KINDS) {
+    g_trace = TraceBuf{nullptr, 0};
+    g_trace_kind = -1;
+    return JFA_OK;
+  }
+  const size_t cap = bytes / (sizeof(unsigned long long) * kTraceRoles);
+  if (cap == 0 || (reinterpret_cast<uintptr_t>(device_buffer) & 7u) != 0) return JFA_ERR_INVALID_ARG;
+  g_trace = TraceBuf{static_cast<unsigned long long*>(device_buffer), int(cap > (1u << 30) ? (1u << 30) : cap)};
+  g_trace_kind = kernel_kind;
+  return JFA_OK;
+}
 
 jfa_status jfa_timing_enable(int on) {
   std::lock_guard<std::mutex> g(g_timing_mu);

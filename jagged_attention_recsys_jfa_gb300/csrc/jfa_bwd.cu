@@ -48,6 +48,7 @@ struct BwdParams {
   int64_t qpad_cap;
   __nv_bfloat16* g0;   // dK (dK/dV pass) or dQ (dQ pass)
   __nv_bfloat16* g1;   // dV (dK/dV pass)
+  TraceBuf trace;
 };
 
 __device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
@@ -189,9 +190,8 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
     for (int t = 0; t < 16; ++t)
       pk[t] = zero ? 0u : pack_bf16x2(__uint_as_float(r[2 * t]) * mul, __uint_as_float(r[2 * t + 1]) * mul);
     if (valid) {
-      uint4* o = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) o[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+      st_global_v8(dst + cc * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+      st_global_v8(dst + cc * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
     }
   }
 }
@@ -253,14 +253,52 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
 
   if (warp < kFirstComputeWarp) {
    setmaxnreg_dec<kRegsLoad>();
-   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+   if (warp == 2) {
+    // ------------------------------------------------------------ K/V loader
+    // Its own warp, so a key tile's K/V load starts as soon as the previous tile's last
+    // dP^T MMA frees the buffers, whatever the ring producer is waiting on.
     if (lane == 0) {
-      uint32_t ring_n = 0, item_n = 0, qtile_n = 0;
+      uint32_t item_n = 0, tn = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const WorkItem wi = p.items[idx];
+        int Lq, Lk;
+        seq_len(wi.b, &Lq, &Lk);
+        const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
+        const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
+        tmap_acquire(mk);
+        tmap_acquire(mv);
+        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+          int first, count;
+          q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+          if (count == 0) continue;
+          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+          trace_event(p.trace, kTraceLoader, tn, 1);
+          mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
+          load_tile<D>(sK, mk, &kv_full, wi.h * D, kt * kBN);
+          load_tile<D>(sV, mv, &kv_full, wi.h * D, kt * kBN);
+          ++item_n;
+          if (kt + 1 < wi.u1) {  // pull the next key tile of this range into L2 meanwhile
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              tma_prefetch_2d(mk, wi.h * D + c * 64, (kt + 1) * kBN);
+              tma_prefetch_2d(mv, wi.h * D + c * 64, (kt + 1) * kBN);
+            }
+          }
+        }
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      if (item_n > 0) drain_wait(&kv_full, (item_n - 1) & 1);
+    }
+   } else if (warp == 0) {
+    // ------------------------------------------------------------ dO / Q ring producer
+    if (lane == 0) {
+      uint32_t ring_n = 0, qtile_n = 0, tn = 0;
       bool ok = true;
       auto fill = [&](const CUtensorMap* m, int col, int row, const float* l2src, const float* dsrc) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
         if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes + (l2src ? 2 * kBM * 4 : 0));
         load_tile<D>(sRing + e * C::kTileBytes, m, &ring_full[e], col, row);
         if (l2src) {
@@ -276,32 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         int Lq, Lk;
         seq_len(wi.b, &Lq, &Lk);
         const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
-        const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
-        const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
         const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
         tmap_acquire(mq);
-        tmap_acquire(mk);
-        tmap_acquire(mv);
         tmap_acquire(mdo);
         const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + p.qpad[wi.b];
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
           q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
-          if (count == 0) continue;
-          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-          mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
-          load_tile<D>(sK, mk, &kv_full, wi.h * D, kt * kBN);
-          load_tile<D>(sV, mv, &kv_full, wi.h * D, kt * kBN);
-          ++item_n;
-          // the next key tile of this range is loaded only once this one is done:
-          // pull it into L2 now
-          if (kt + 1 < wi.u1) {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              tma_prefetch_2d(mk, wi.h * D + c * 64, (kt + 1) * kBN);
-              tma_prefetch_2d(mv, wi.h * D + c * 64, (kt + 1) * kBN);
-            }
-          }
           for (int i = 0; i < count && ok; ++i) {
             const int qt = first + i;
             if (!fill(mdo, wi.h * D, qt * kBM, nullptr, nullptr)) { ok = false; break; }
@@ -316,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
       for (uint32_t n = f; n < ring_n; ++n) drain_wait(&ring_full[n % R], (n / R) & 1);
-      if (item_n > 0) drain_wait(&kv_full, (item_n - 1) & 1);
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -324,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(sRing);
-      uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
+      uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
         if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
@@ -360,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         if (count == 0) continue;
         if (!wait(&kv_full, item_n & 1)) { ok = false; break; }
         ++item_n;
+        trace_event(p.trace, kTraceMma, tn, 10);
         const uint32_t n0 = ring_n;  // dO_i at n0 + 2i, Q_i at n0 + 2i + 1
         if (!wait_ring(n0 + 1)) { ok = false; break; }
         mma_nt(C::kColS, aK, ra(n0 + 1));
@@ -367,32 +386,41 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         if (!wait_ring(n0)) { ok = false; break; }
         mma_nt(C::kColP, aV, ra(n0));
         umma_commit(&dpt_full);
+        // K and V are read only by S^T and dP^T: once the last dP^T is issued the loader
+        // may bring in the next key tile while dV / dK of this one still run
+        if (count == 1) umma_commit(&kv_empty);
         for (int i = 0; i < count && ok; ++i) {
           const uint32_t nd = n0 + 2 * i, nq = nd + 1;
           if (!wait(&p_full, tile_n & 1)) { ok = false; break; }
+          trace_event(p.trace, kTraceMma, tn, 11);
           if (i == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
           mma_acc(C::kColA1, C::kColS, ra(nd), i > 0);  // dV += P^T dO
           umma_commit(&ring_empty[nd % R]);
+          trace_event(p.trace, kTraceMma, tn, 12);
           if (i + 1 < count) {
             if (!wait_ring(nq + 2)) { ok = false; break; }
             mma_nt(C::kColS, aK, ra(nq + 2));
             umma_commit(&st_full);
+            trace_event(p.trace, kTraceMma, tn, 13);
           }
           if (!wait(&ds_full, tile_n & 1)) { ok = false; break; }
+          trace_event(p.trace, kTraceMma, tn, 14);
           ++tile_n;
           mma_acc(C::kColA0, C::kColP, ra(nq), i > 0);  // dK += dS^T Q
           umma_commit(&ring_empty[nq % R]);
+          trace_event(p.trace, kTraceMma, tn, 15);
           if (i + 1 < count) {
             if (!wait_ring(nd + 2)) { ok = false; break; }
             mma_nt(C::kColP, aV, ra(nd + 2));
             umma_commit(&dpt_full);
+            if (i + 2 == count) umma_commit(&kv_empty);
+            trace_event(p.trace, kTraceMma, tn, 16);
           }
         }
         if (!ok) break;
         ring_n = n0 + 2 * count;
         ++acc_n;
         umma_commit(&acc_full);
-        umma_commit(&kv_empty);
        }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
@@ -410,7 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
     const float sl2 = p.scale_log2;
-    uint32_t ring_n = 0, tile_n = 0, acc_n = 0, qtile_n = 0;
+    uint32_t ring_n = 0, tile_n = 0, acc_n = 0, qtile_n = 0, tn = 0;
+    const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
      const WorkItem it = p.items[idx];
@@ -443,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         const float* dvec = vec + 128 + 64 * w;
         if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
         float x[64];
         ld_cols64(tS, x);
         const int i0 = qt * kBM + 64 * w;  // local query index of column 0 of this half
@@ -488,9 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full);
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
         if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
         float dp[64];
         ld_cols64(tP, dp);
 #pragma unroll
@@ -505,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&ds_full);
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       }
       if (!ok) break;
       if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
@@ -514,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       store_acc_row(tmem + lane_addr + C::kColA1 + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
       tc_fence_before();
       mbar_arrive(&acc_empty);
+      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
      }
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
@@ -588,13 +622,48 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
 
   if (warp < kFirstComputeWarp) {
    setmaxnreg_dec<kRegsLoad>();
-   if (warp == 0) {
+   if (warp == 2) {
+    // ------------------------------------------------------------ Q / dO loader
     if (lane == 0) {
-      uint32_t ring_n = 0, item_n = 0;
+      uint32_t item_n = 0, tn = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+       const WorkItem wi = p.items[idx];
+       int Lq, Lk;
+       seq_len(wi.b, &Lq, &Lk);
+       const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
+       const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
+       tmap_acquire(mq);
+       tmap_acquire(mdo);
+       for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
+        if (kv_tiles_for_q_tile(qt, Lq, Lk, causal) == 0) continue;
+        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        trace_event(p.trace, kTraceLoader, tn, 1);
+        mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
+        load_tile<D>(sQ, mq, &qdo_full, wi.h * D, qt * kBM);
+        load_tile<D>(sDO, mdo, &qdo_full, wi.h * D, qt * kBM);
+        ++item_n;
+        if (qt + 1 < wi.u1) {  // pull the next query tile of this range into L2 meanwhile
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_2d(mq, wi.h * D + c * 64, (qt + 1) * kBM);
+            tma_prefetch_2d(mdo, wi.h * D + c * 64, (qt + 1) * kBM);
+          }
+        }
+       }
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      if (item_n > 0) drain_wait(&qdo_full, (item_n - 1) & 1);
+    }
+   } else if (warp == 0) {
+    // ------------------------------------------------------------ V / K ring producer
+    if (lane == 0) {
+      uint32_t ring_n = 0, tn = 0;
       bool ok = true;
       auto fill = [&](const CUtensorMap* m, int col, int row) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
         if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
         load_tile<D>(sRing + e * C::kTileBytes, m, &ring_full[e], col, row);
         ++ring_n;
@@ -604,31 +673,12 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
        const WorkItem wi = p.items[idx];
        int Lq, Lk;
        seq_len(wi.b, &Lq, &Lk);
-       const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
        const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
        const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
-       const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
-       tmap_acquire(mq);
        tmap_acquire(mk);
        tmap_acquire(mv);
-       tmap_acquire(mdo);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
-        if (nkv == 0) continue;
-        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-        mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
-        load_tile<D>(sQ, mq, &qdo_full, wi.h * D, qt * kBM);
-        load_tile<D>(sDO, mdo, &qdo_full, wi.h * D, qt * kBM);
-        ++item_n;
-        // the next query tile of this range is loaded only once this one is done:
-        // pull it into L2 now
-        if (qt + 1 < wi.u1) {
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            tma_prefetch_2d(mq, wi.h * D + c * 64, (qt + 1) * kBM);
-            tma_prefetch_2d(mdo, wi.h * D + c * 64, (qt + 1) * kBM);
-          }
-        }
         for (int jt = 0; jt < nkv && ok; ++jt) {
           if (!fill(mv, wi.h * D, jt * kBN) || !fill(mk, wi.h * D, jt * kBN)) { ok = false; break; }
         }
@@ -637,14 +687,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
       for (uint32_t n = f; n < ring_n; ++n) drain_wait(&ring_full[n % R], (n / R) & 1);
-      if (item_n > 0) drain_wait(&qdo_full, (item_n - 1) & 1);
     }
    } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aR = smem_u32(sRing);
-      uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0;
+      uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
         if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
@@ -670,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         if (nkv == 0) continue;
         if (!wait(&qdo_full, item_n & 1)) { ok = false; break; }
         ++item_n;
+        trace_event(p.trace, kTraceMma, tn, 10);
         const uint32_t n0 = ring_n;  // V_j at n0 + 2j, K_j at n0 + 2j + 1
         if (!wait_ring(n0 + 1)) { ok = false; break; }
         mma_nt(C::kColS, aQ, ra(n0 + 1));
@@ -678,6 +728,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         mma_nt(colP(tile_n), aDO, ra(n0));
         umma_commit(&dp_full[tile_n & 1]);
         umma_commit(&ring_empty[n0 % R]);
+        // Q and dO are read only by S and dP: once the last dP is issued the loader may
+        // bring in the next query tile while dQ of this one still runs
+        if (nkv == 1) umma_commit(&qdo_empty);
         for (int jt = 0; jt < nkv && ok; ++jt) {
           const uint32_t g = tile_n;  // global tile index
           const uint32_t nv = n0 + 2 * jt, nk = nv + 1;
@@ -685,15 +738,20 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
             // next S once the warpgroups hold this S in registers; next dP into the
             // other buffer (its dS was consumed by the dQ MMA issued before)
             if (!wait(&s_free, g & 1)) { ok = false; break; }
+            trace_event(p.trace, kTraceMma, tn, 11);
             if (!wait_ring(nk + 2)) { ok = false; break; }
             mma_nt(C::kColS, aQ, ra(nk + 2));
             umma_commit(&s_full);
+            trace_event(p.trace, kTraceMma, tn, 12);
             if (!wait_ring(nv + 2)) { ok = false; break; }
             mma_nt(colP(g + 1), aDO, ra(nv + 2));
             umma_commit(&dp_full[(g + 1) & 1]);
             umma_commit(&ring_empty[(nv + 2) % R]);
+            if (jt + 2 == nkv) umma_commit(&qdo_empty);
+            trace_event(p.trace, kTraceMma, tn, 13);
           }
           if (!wait(&ds_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
+          trace_event(p.trace, kTraceMma, tn, 14);
           ++tile_n;
           if (jt == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
           // dQ += dS (TMEM, queries x keys) * K (keys x D, MN-major)
@@ -703,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
             umma_ts(tmem + C::kColDQ, tmem + colP(g) + (kk >> 2) * 64 + (kk & 3) * 8, kd + uint32_t(kk * 2048 >> 4),
                     kIdAcc, (jt > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&ring_empty[nk % R]);
+          trace_event(p.trace, kTraceMma, tn, 15);
         }
         if (!ok) break;
         // the last tile's s_free arrival has no consumer above: take it here
@@ -710,7 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         ring_n = n0 + 2 * nkv;
         ++acc_n;
         umma_commit(&acc_full);
-        umma_commit(&qdo_empty);
        }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
@@ -726,7 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const float sl2 = p.scale_log2;
-    uint32_t tile_n = 0, acc_n = 0;
+    uint32_t tile_n = 0, acc_n = 0, tn = 0;
+    const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
      const WorkItem it = p.items[idx];
@@ -751,10 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       for (int jt = 0; jt < nkv && ok; ++jt) {
         if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
         float x[64];
         ld_cols64(tS, x);
         tc_fence_before();
         mbar_arrive(&s_free);
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
         const int j0 = jt * kBN + 64 * w;  // local key index of column 0 of this half
         const int n_real = Lk - j0;        // columns >= n_real are past the sequence end
         if (kBias) {
@@ -792,6 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         if (!mbar_wait(&dp_full[g & 1], (g >> 1) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
         float dp[64];
         ld_cols64(tP, dp);
 #pragma unroll
@@ -800,6 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&ds_full[g & 1]);
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       }
       if (!ok) break;
       if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
@@ -845,6 +908,7 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.qpad_cap = L.qpad_cap;
   bp.g0 = nullptr;
   bp.g1 = nullptr;
+  bp.trace = pr.trace[dq_pass ? JFA_KERNEL_BWD_DQ : JFA_KERNEL_BWD_DKDV];
   return bp;
 }
 

@@ -45,6 +45,31 @@ constexpr int kItemsPerCta = 4;  // target items per CTA when capping range cost
 enum MapSlot { kMapQ = 0, kMapK = 1, kMapV = 2, kMapDO = 3, kNumMapSlots = 4 };
 
 // Header at the start of the workspace.
+// Developer tracing (off unless a buffer is configured): one thread per warp role of
+// CTA 0 records (SM clock << 16 | role << 8 | event) into its own region of `cap` entries.
+enum TraceRole {
+  kTraceProducer = 0,
+  kTraceMma = 1,
+  kTraceCompute0 = 2,
+  kTraceCompute1 = 3,
+  kTraceLoader = 4,
+  kTraceRoles = 5
+};
+struct TraceBuf {
+  unsigned long long* buf;  // nullptr: tracing off
+  int cap;                  // entries per role
+};
+#ifdef __CUDACC__
+__device__ __forceinline__ void trace_event(const TraceBuf& t, int role, uint32_t& n, int ev) {
+  if (t.buf != nullptr && blockIdx.x == 0) {
+    if (n < uint32_t(t.cap))
+      t.buf[size_t(role) * t.cap + n] = (static_cast<unsigned long long>(clock64()) << 16) |
+                                        (static_cast<unsigned long long>(role) << 8) | unsigned(ev);
+    ++n;
+  }
+}
+#endif
+
 struct WsHeader {
   int status;      // jfa_status of device-side checks (0 = ok)
   int n_fwd;       // number of forward items

@@ -51,6 +51,7 @@ struct FwdParams {
   int* status;
   __nv_bfloat16* out;
   float* lse;
+  TraceBuf trace;
 };
 
 template <int D>
@@ -142,10 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
 
   if (warp < kFirstComputeWarp) {
    setmaxnreg_dec<kRegsLoad>();
-   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+   if (warp == 2) {
+    // ------------------------------------------------------------ Q loader
+    // Its own warp, so the next pair's Q load starts the moment the last S MMA of the
+    // current pair frees the buffer, whatever the K/V producer is waiting on.
     if (lane == 0) {
-      uint32_t ring_n = 0, item_n = 0;
+      uint32_t item_n = 0, tn = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
        const WorkItem wi = p.items[idx];
@@ -153,12 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
-        const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
-        const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
         tmap_acquire(mq);
-        tmap_acquire(mk);
-        tmap_acquire(mv);
         if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&q_full, (it.has1 ? 2 : 1) * C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kBoxes; ++c) {
@@ -166,19 +166,38 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           if (it.has1) tma_load_2d(sQ + C::kTileBytes + c * 16384, mq, &q_full, it.h * D + c * 64, it.t1 * kBM);
         }
         ++item_n;
-        // the next query-tile pair of this range loads only after this pair's last S
-        // MMA: pull it into L2 now
+        // pull the next pair of this range into L2 meanwhile
         if (u + 1 < wi.u1) {
 #pragma unroll
           for (int c = 0; c < C::kBoxes; ++c)
             for (int t = 2 * (u + 1); t < 2 * (u + 1) + 2 && t * kBM < it.Lq; ++t)
               tma_prefetch_2d(mq, it.h * D + c * 64, t * kBM);
         }
+       }
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      if (item_n > 0) drain_wait(&q_full, (item_n - 1) & 1);
+    }
+   } else if (warp == 0) {
+    // ------------------------------------------------------------ K/V producer
+    if (lane == 0) {
+      uint32_t ring_n = 0, tn = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+       const WorkItem wi = p.items[idx];
+       for (int u = wi.u0; u < wi.u1 && ok; ++u) {
+        const ItemInfo it = decode(p, wi, u);
+        if (it.njt == 0) continue;
+        const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
+        const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
+        tmap_acquire(mk);
+        tmap_acquire(mv);
         for (int j = 0; j < it.njt && ok; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t e = ring_n % C::kStages, ph = (ring_n / C::kStages) & 1;
             if (!mbar_wait(&kv_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+            trace_event(p.trace, kTraceProducer, tn, 2);
             mbar_arrive_expect_tx(&kv_full[e], C::kTileBytes);
             uint8_t* dst = sRing + e * C::kTileBytes;
 #pragma unroll
@@ -193,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       // drain: every copy this thread started has landed before the CTA can exit
       const uint32_t first = ring_n > C::kStages ? ring_n - C::kStages : 0;
       for (uint32_t n = first; n < ring_n; ++n) drain_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1);
-      if (item_n > 0) drain_wait(&q_full, (item_n - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -203,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       const uint32_t colS[2] = {C::kColS0, C::kColS1};
       const uint32_t colO[2] = {C::kColO0, C::kColO1};
       const uint32_t sQ_addr = smem_u32(sQ), sR_addr = smem_u32(sRing);
-      uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0};
+      uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0}, tn = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
        const WorkItem wi = p.items[idx];
@@ -214,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         if (!mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++item_n;
         tc_fence_after();
+        trace_event(p.trace, kTraceMma, tn, 10);
         int s_left = it.nkv0 + it.nkv1;
         auto issue_S = [&](int s, uint32_t e) {
           // descriptor start addresses are in 16-byte units in the low bits: step by adding
@@ -225,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             umma_ss(tmem + colS[s], qd + o, kd + o, kIdS, kk > 0);
           }
           umma_commit(&s_full[s]);
+          trace_event(p.trace, kTraceMma, tn, 16 + s);
           if (--s_left == 0) umma_commit(&q_empty);
         };
         auto issue_PV = [&](int s, uint32_t e, bool acc) {
@@ -253,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
               if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
               ++p_n[s];
               tc_fence_after();
+              trace_event(p.trace, kTraceMma, tn, 12 + s);
               issue_PV(s, nv % C::kStages, j > 0);
+              trace_event(p.trace, kTraceMma, tn, 14 + s);
               if (j == nkv[s] - 1) umma_commit(&o_full[s]);
             }
             if (j + 1 < nkv[s]) {
@@ -286,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     const uint32_t tS = tmem + lane_addr + (s ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_addr + (s ? C::kColO1 : C::kColO0);
     const float sl2 = p.scale_log2;
-    uint32_t s_n = 0, o_n = 0;
+    uint32_t s_n = 0, o_n = 0, tn = 0;
+    const bool leader = (warp & 3) == 0 && lane == 0;  // records this warpgroup's trace
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
      const WorkItem wi = p.items[idx];
@@ -315,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++s_n;
         tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 20);
         float x[128];
         {
           // all four loads in flight before a single wait
@@ -411,12 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[s]);
+        if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 21);
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, lse = ln(sum) = (m + log2 l) * ln 2
       if (!mbar_wait(&o_full[s], o_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++o_n;
       tc_fence_after();
+      if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 22);
       const bool live = l > 0.f;
       const float inv_l = live ? 1.f / l : 0.f;
       const float m_use = (m == -INFINITY) ? 0.f : m;
@@ -432,13 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         for (int t2 = 0; t2 < 16; ++t2)
           pk[t2] = pack_bf16x2(__uint_as_float(o_r[cc][2 * t2]) * inv_l, __uint_as_float(o_r[cc][2 * t2 + 1]) * inv_l);
         if (valid_row) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          st_global_v8(orow + cc * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+          st_global_v8(orow + cc * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
         }
       }
       if (valid_row) *lrow = live ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
+      if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 23);
      }
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
@@ -483,6 +509,7 @@ cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void*
   fp.status = &reinterpret_cast<WsHeader*>(w)->status;
   fp.out = static_cast<__nv_bfloat16*>(out);
   fp.lse = lse;
+  fp.trace = pr.trace[JFA_KERNEL_FORWARD];
   const int grid = num_sms;
   const bool bias = pr.bias_table != nullptr;
   if (pr.d == 128) return bias ? launch_fwd_t<128, true>(fp, grid, stream) : launch_fwd_t<128, false>(fp, grid, stream);

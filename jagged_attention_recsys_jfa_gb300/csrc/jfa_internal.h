@@ -16,6 +16,7 @@ struct Problem {
   int causal;
   const float* bias_table;  // nullptr = no bias
   int num_buckets, center;
+  TraceBuf trace[5];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
 };
 
 struct PlanMaps {

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
 # Every symbol include/jfa.h declares.
 EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_forward_noalloc", "jfa_backward", "jfa_check_status",
                     "jfa_status_string", "jfa_last_launch_count", "jfa_last_error", "jfa_timing_enable",
-                    "jfa_timing_read")
+                    "jfa_timing_read", "jfa_trace_configure")
 KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 
 
@@ -86,6 +86,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.jfa_timing_enable.restype = i32
     lib.jfa_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i32]
     lib.jfa_timing_read.restype = i32
+    lib.jfa_trace_configure.argtypes = [vp, sz, i32]
+    lib.jfa_trace_configure.restype = i32
     _LIB = lib
     return lib
 
@@ -237,6 +239,30 @@ def jfa_timing_read() -> dict:
     if st != JFA_OK:
         raise JfaError(st, "jfa_timing_read")
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def jfa_trace_configure(buffer: Optional[torch.Tensor], kernel_kind: str = "forward") -> None:
+    """Developer tracing: record pipeline events of the first CTA of every later launch of
+    `kernel_kind` into `buffer` (a CUDA int64/uint8 tensor); None turns tracing off."""
+    lib = load_library()
+    if buffer is None:
+        st = lib.jfa_trace_configure(None, 0, -1)
+    else:
+        st = lib.jfa_trace_configure(buffer.data_ptr(), buffer.numel() * buffer.element_size(),
+                                     KERNEL_KINDS.index(kernel_kind))
+    if st != JFA_OK:
+        raise JfaError(st, "jfa_trace_configure")
+
+
+def decode_trace(buffer: torch.Tensor):
+    """Split a trace buffer into per-role lists of (sm_clock, event_id), dropping unused
+    entries (the buffer should be zeroed before tracing)."""
+    raw = buffer.detach().cpu().view(torch.int64).numpy().reshape(5, -1)
+    roles = []
+    for r in range(5):
+        ent = [int(x) & 0xFFFFFFFFFFFFFFFF for x in raw[r] if int(x) != 0]
+        roles.append([(e >> 16, e & 0xFF) for e in ent])
+    return roles
 
 
 class JaggedAttention(torch.autograd.Function):
