@@ -147,6 +147,14 @@ enum { JFA_KERNEL_PLAN = 0, JFA_KERNEL_FORWARD = 1, JFA_KERNEL_BWD_PREPROCESS = 
 jfa_status jfa_timing_enable(int on);
 jfa_status jfa_timing_read(double* ms, int* launches, int n_kinds);
 
+/* Failure-detection self test (not part of the attention itself).  Enqueues one tiny
+ * kernel whose single thread waits on a pipeline barrier that nothing ever signals,
+ * through the bounded wait every kernel of this library uses; after `timeout_ns`
+ * (1 ns .. 2 s) the wait gives up and JFA_ERR_TIMEOUT is recorded in the workspace
+ * status word, readable with jfa_check_status.  Nothing faults or hangs; the context
+ * stays usable.  `workspace` needs 256 bytes (zeroed status word). */
+jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_stream_t stream);
+
 /* Developer tracing (not part of the attention itself).  With a non-NULL device buffer,
  * kernels of `kernel_kind` (JFA_KERNEL_*) launched afterwards record the pipeline events
  * of their first CTA: uint64 entries (SM clock << 16 | role << 8 | event id) in five

@@ -306,6 +306,14 @@ int jfa_last_launch_count(void) { return g_last_launches; }
 
 const char* jfa_last_error(void) { return g_last_error; }
 
+jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_stream_t stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return JFA_ERR_WORKSPACE;
+  if (timeout_ns == 0 || timeout_ns > kWaitTimeoutNs) return JFA_ERR_INVALID_ARG;
+  JFA_CHECK_LAUNCH(launch_wait_timeout_selftest(workspace, timeout_ns, reinterpret_cast<cudaStream_t>(stream)),
+                   "self-test launch");
+  return JFA_OK;
+}
+
 jfa_status jfa_trace_configure(void* device_buffer, size_t bytes, int kernel_kind) {
   std::lock_guard<std::mutex> g(g_trace_mu);
   if (!device_buffer || kernel_kind < 0 || kernel_kind >= JFA_NUM_KERNEL_KINDS) {

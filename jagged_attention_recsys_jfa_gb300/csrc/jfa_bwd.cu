@@ -90,43 +90,41 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
     const int Lq = int(p.q_off[it.b + 1] - qo);
     const int64_t pad0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
     for (int t = it.u0; t < it.u1; ++t) {
-      // 8 warps x 16 rows; each warp keeps 4 rows' loads in flight
-      for (int rb = 0; rb < kBM / 8; rb += 4) {
-        float acc[4], l2[4];
+      // 8 warps x 16 rows.  A row of one head is D/8 16-byte chunks: a warp covers
+      // 32 / (D/8) rows per load, and all of its 16 rows' loads are in flight at once.
+      constexpr int kLanesPerRow = D / 8, kRowsPerLoad = 32 / kLanesPerRow, kLoads = 16 / kRowsPerLoad;
+      const int sub = lane / kLanesPerRow, chunk = lane % kLanesPerRow;
+      float acc[kLoads];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = t * kBM + warp + 8 * (rb + k);
-          acc[k] = 0.f;
-          l2[k] = 0.f;
+      for (int k = 0; k < kLoads; ++k) {
+        const int i = t * kBM + warp * 16 + k * kRowsPerLoad + sub;
+        acc[k] = 0.f;
+        if (i < Lq) {
+          const int64_t e0 = ((qo + i) * p.H + it.h) * int64_t(D);
+          const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.dout + e0) + chunk);
+          const uint4 c = __ldg(reinterpret_cast<const uint4*>(p.out + e0) + chunk);
+          acc[k] = fmaf(bf16lo(a.x), bf16lo(c.x), bf16hi(a.x) * bf16hi(c.x)) +
+                   fmaf(bf16lo(a.y), bf16lo(c.y), bf16hi(a.y) * bf16hi(c.y)) +
+                   fmaf(bf16lo(a.z), bf16lo(c.z), bf16hi(a.z) * bf16hi(c.z)) +
+                   fmaf(bf16lo(a.w), bf16lo(c.w), bf16hi(a.w) * bf16hi(c.w));
+        }
+      }
+#pragma unroll
+      for (int o = kLanesPerRow / 2; o > 0; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+      }
+      if (chunk == 0) {
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) {
+          const int i = t * kBM + warp * 16 + k * kRowsPerLoad + sub;
+          float l2 = 0.f;
           if (i < Lq) {
-            const int64_t e0 = ((qo + i) * p.H + it.h) * int64_t(D);
-            if (D == 128) {
-              const uint2 a = __ldg(reinterpret_cast<const uint2*>(p.dout + e0) + lane);
-              const uint2 b = __ldg(reinterpret_cast<const uint2*>(p.out + e0) + lane);
-              acc[k] = fmaf(bf16lo(a.x), bf16lo(b.x),
-                            fmaf(bf16hi(a.x), bf16hi(b.x), fmaf(bf16lo(a.y), bf16lo(b.y), bf16hi(a.y) * bf16hi(b.y))));
-            } else {
-              const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(p.dout + e0) + lane);
-              const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(p.out + e0) + lane);
-              acc[k] = fmaf(bf16lo(a), bf16lo(b), bf16hi(a) * bf16hi(b));
-            }
             const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
-            l2[k] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+            l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
           }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
-        }
-        if (lane < 4) {
-          float a = acc[0], l = l2[0];
-#pragma unroll
-          for (int k = 1; k < 4; ++k)
-            if (lane == k) a = acc[k], l = l2[k];
-          const int i = t * kBM + warp + 8 * (rb + lane);
-          p.delta[pad0 + i] = a;
-          p.lse2[pad0 + i] = l;
+          p.delta[pad0 + i] = i < Lq ? acc[k] : 0.f;
+          p.lse2[pad0 + i] = l2;
         }
       }
     }

@@ -47,6 +47,8 @@ cudaError_t check_launch_registers(K kern) {
 cudaError_t launch_plan(const Problem& p, const PlanMaps& maps, void* ws, const WsLayout& L, bool backward,
                         int num_sms, cudaStream_t stream);
 
+cudaError_t launch_wait_timeout_selftest(void* ws, uint64_t timeout_ns, cudaStream_t stream);
+
 cudaError_t launch_forward(const Problem& p, void* ws, const WsLayout& L, void* out, float* lse,
                            int num_sms, cudaStream_t stream);
 

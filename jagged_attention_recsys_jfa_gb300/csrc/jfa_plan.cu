@@ -235,7 +235,26 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   }
 }
 
+// Failure-detection self test: one thread waits on an mbarrier that nothing arrives on,
+// through the same bounded wait the pipelines use; when the limit runs out it records
+// JFA_ERR_TIMEOUT in the workspace status word and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, &abort_flag, timeout_ns)) atomicCAS(status, 0, int(JFA_ERR_TIMEOUT));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(void* ws, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(&reinterpret_cast<WsHeader*>(ws)->status, timeout_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const WsLayout& L, bool backward,
                         int num_sms, cudaStream_t stream) {

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
 # Every symbol include/jfa.h declares.
 EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_forward_noalloc", "jfa_backward", "jfa_check_status",
                     "jfa_status_string", "jfa_last_launch_count", "jfa_last_error", "jfa_timing_enable",
-                    "jfa_timing_read", "jfa_trace_configure")
+                    "jfa_timing_read", "jfa_trace_configure", "jfa_selftest_wait_timeout")
 KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 
 
@@ -86,6 +86,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.jfa_timing_enable.restype = i32
     lib.jfa_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i32]
     lib.jfa_timing_read.restype = i32
+    lib.jfa_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+    lib.jfa_selftest_wait_timeout.restype = i32
     lib.jfa_trace_configure.argtypes = [vp, sz, i32]
     lib.jfa_trace_configure.restype = i32
     _LIB = lib
@@ -257,7 +259,9 @@ def jfa_trace_configure(buffer: Optional[torch.Tensor], kernel_kind: str = "forw
 def decode_trace(buffer: torch.Tensor):
     """Split a trace buffer into per-role lists of (sm_clock, event_id), dropping unused
     entries (the buffer should be zeroed before tracing)."""
-    raw = buffer.detach().cpu().view(torch.int64).numpy().reshape(5, -1)
+    flat = buffer.detach().cpu().view(torch.int64).numpy()
+    cap = flat.size // 5
+    raw = flat[:5 * cap].reshape(5, cap)
     roles = []
     for r in range(5):
         ent = [int(x) & 0xFFFFFFFFFFFFFFFF for x in raw[r] if int(x) != 0]
