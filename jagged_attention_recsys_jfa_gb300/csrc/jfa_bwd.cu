@@ -210,7 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
   uint8_t* sRing = smem + 2 * C::kTileBytes;
   float* sVec = reinterpret_cast<float*>(sRing + R * C::kTileBytes);  // [kVecSlots][2][128]: lse2, D
 
-  __shared__ uint64_t kv_full, kv_empty, st_full, dpt_full, p_full, ds_full, acc_full, acc_empty, mma_done;
+  // dV and dK hand over to the epilogue separately: dV(last) completes one MMA group
+  // before dK(last), and the next key tile's dV(0) only needs dV stored, not dK.
+  __shared__ uint64_t kv_full, kv_empty, st_full, dpt_full, p_full, ds_full, mma_done;
+  __shared__ uint64_t dv_full, dv_empty, dk_full, dk_empty;
   __shared__ uint64_t ring_full[R], ring_empty[R];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -224,8 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     mbar_init(&dpt_full, 1);
     mbar_init(&p_full, 256);
     mbar_init(&ds_full, 256);
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 256);
+    mbar_init(&dv_full, 1);
+    mbar_init(&dv_empty, 256);
+    mbar_init(&dk_full, 1);
+    mbar_init(&dk_empty, 256);
     mbar_init(&mma_done, 1);
     for (int i = 0; i < R; ++i) {
       mbar_init(&ring_full[i], 1);
@@ -391,9 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
           const uint32_t nd = n0 + 2 * i, nq = nd + 1;
           if (!wait(&p_full, tile_n & 1)) { ok = false; break; }
           trace_event(p.trace, kTraceMma, tn, 11);
-          if (i == 0 && !wait(&acc_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
+          if (i == 0 && !wait(&dv_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
           mma_acc(C::kColA1, C::kColS, ra(nd), i > 0);  // dV += P^T dO
           umma_commit(&ring_empty[nd % R]);
+          if (i + 1 == count) umma_commit(&dv_full);
           trace_event(p.trace, kTraceMma, tn, 12);
           if (i + 1 < count) {
             if (!wait_ring(nq + 2)) { ok = false; break; }
@@ -404,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
           if (!wait(&ds_full, tile_n & 1)) { ok = false; break; }
           trace_event(p.trace, kTraceMma, tn, 14);
           ++tile_n;
+          if (i == 0 && !wait(&dk_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
           mma_acc(C::kColA0, C::kColP, ra(nq), i > 0);  // dK += dS^T Q
           umma_commit(&ring_empty[nq % R]);
           trace_event(p.trace, kTraceMma, tn, 15);
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         if (!ok) break;
         ring_n = n0 + 2 * count;
         ++acc_n;
-        umma_commit(&acc_full);
+        umma_commit(&dk_full);
        }
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
@@ -538,13 +545,17 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       }
       if (!ok) break;
-      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      store_acc_row(tmem + lane_addr + C::kColA1 + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
+      tc_fence_before();
+      mbar_arrive(&dv_empty);
+      if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
       store_acc_row(tmem + lane_addr + C::kColA0 + w * (D / 2), D / 2, p.scale, dk_row, valid, false);
-      store_acc_row(tmem + lane_addr + C::kColA1 + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
       tc_fence_before();
-      mbar_arrive(&acc_empty);
+      mbar_arrive(&dk_empty);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
      }
     }

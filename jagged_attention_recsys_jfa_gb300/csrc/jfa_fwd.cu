@@ -381,14 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
               if (c > lim) x[c] = -INFINITY;
           }
         }
-        // row max as 8 independent chains, then a short tree
-        float mx8[8];
+        // row max: 4 chains of 3-input max over 32 columns each, then a short tree
+        float mx4[4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+        for (int k = 0; k < 4; ++k) {
+          float m0 = fmaxf(x[32 * k], x[32 * k + 1]);
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int c = 2; c < 32; c += 2) m0 = fmax3(m0, x[32 * k + c], x[32 * k + c + 1]);
+          mx4[k] = m0;
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_tile = kBias ? mx : mx * sl2;
         // raise the reference max only when it grows by more than 2^8
         const bool need = m_tile > m + kRescaleThreshold;
@@ -397,21 +399,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         l *= alpha;
         m = m_new;
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        // row sum as 4 independent chains, in column order within each (real columns
-        // precede padded ones, which keeps the subtraction below well conditioned)
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        // exponentials two columns per packed fp32x2 op; row sum in 4 packed chains
+        uint64_t sum2[4] = {0, 0, 0, 0};
+        {
+          const uint64_t k_scale = f2_pack(sl2, sl2), k_negm = f2_pack(-m_use, -m_use);
+          uint32_t pk[64];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int t2 = 0; t2 < 16; ++t2) {
-            const float a = kBias ? x[cc * 32 + 2 * t2] - m_use : fmaf(x[cc * 32 + 2 * t2], sl2, -m_use);
-            const float b = kBias ? x[cc * 32 + 2 * t2 + 1] - m_use : fmaf(x[cc * 32 + 2 * t2 + 1], sl2, -m_use);
+          for (int t2 = 0; t2 < 64; ++t2) {
+            const uint64_t xx = f2_pack(x[2 * t2], x[2 * t2 + 1]);
+            const uint64_t arg = kBias ? f2_add(xx, k_negm) : f2_fma(xx, k_scale, k_negm);
+            float a, b;
+            f2_unpack(arg, a, b);
             const float pa = ex2_approx(a), pb = ex2_approx(b);
-            sum4[cc] += pa + pb;
+            sum2[t2 & 3] = f2_add(sum2[t2 & 3], f2_pack(pa, pb));
             pk[t2] = pack_bf16x2(pa, pb);
           }
-          tmem_st16(tS + cc * 16, pk);
+          tmem_st64(tS, pk);
+        }
+        float sum4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float lo, hi;
+          f2_unpack(sum2[k], lo, hi);
+          sum4[k] = lo + hi;
         }
         float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         if (last && !p.causal && kv0 + kBN > it.Lk) {
