@@ -171,7 +171,7 @@ extern "C" {
 
 size_t jfa_workspace_size(int B, int H, int d, int64_t total_q, int64_t total_kv, int is_backward) {
   if (B < 1 || H < 1 || (d != 64 && d != 128) || total_q < 0 || total_kv < 0) return 0;
-  return make_layout(B, H, total_q, total_kv, is_backward != 0).total;
+  return make_layout(B, H, d, total_q, total_kv, is_backward != 0).total;
 }
 
 jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_t* q_offsets,
@@ -184,7 +184,7 @@ jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_
   if (total_q > 0 && (!q || !out || !lse || !aligned16(q) || !aligned16(out) || !aligned16(lse)))
     return JFA_ERR_INVALID_ARG;
   if (total_kv > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return JFA_ERR_INVALID_ARG;
-  const WsLayout L = make_layout(B, H, total_q, total_kv, false);
+  const WsLayout L = make_layout(B, H, d, total_q, total_kv, false);
   if ((st = check_workspace(workspace, workspace_bytes, L)) != JFA_OK) return st;
   const Problem pr = make_problem(B, H, d, total_q, total_kv, q_offsets, kv_offsets, bias, scale, causal);
   const int nsm = sm_count();
@@ -233,7 +233,7 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
   if (total_kv > 0 && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
                        !aligned16(dv)))
     return JFA_ERR_INVALID_ARG;
-  const WsLayout L = make_layout(B, H, total_q, total_kv, true);
+  const WsLayout L = make_layout(B, H, d, total_q, total_kv, true);
   if ((st = check_workspace(workspace, workspace_bytes, L)) != JFA_OK) return st;
   const Problem pr = make_problem(B, H, d, total_q, total_kv, q_offsets, kv_offsets, bias, scale, causal);
   const int nsm = sm_count();

@@ -32,7 +32,7 @@ static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds t
 struct BwdParams {
   const int64_t* q_off;
   const int64_t* kv_off;
-  int H;
+  int B, H;
   int64_t total_q, total_kv;
   float scale, scale_log2;
   int causal;
@@ -267,25 +267,35 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         const WorkItem wi = p.items[idx];
         int Lq, Lk;
         seq_len(wi.b, &Lq, &Lk);
-        const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
-        const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
-        tmap_acquire(mk);
-        tmap_acquire(mv);
+        const int64_t k0 = p.kv_off[wi.b];
+        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapK);
+        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapV);
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
           q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
           if (count == 0) continue;
+          const TileMap mk = tile_map(p.maps, p.B, kMapK, wi.b, k0, kt, p.total_kv);
+          const TileMap mv = tile_map(p.maps, p.B, kMapV, wi.b, k0, kt, p.total_kv);
+          if (mk.tail) {
+            tmap_acquire(mk.map);
+            tmap_acquire(mv.map);
+          }
           if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
           trace_event(p.trace, kTraceLoader, tn, 1);
           mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
-          load_tile<D>(sK, mk, &kv_full, wi.h * D, kt * kBN);
-          load_tile<D>(sV, mv, &kv_full, wi.h * D, kt * kBN);
+          load_tile<D>(sK, mk.map, &kv_full, wi.h * D, mk.y);
+          load_tile<D>(sV, mv.map, &kv_full, wi.h * D, mv.y);
           ++item_n;
-          if (kt + 1 < wi.u1) {  // pull the next key tile of this range into L2 meanwhile
+          // pull the next key tile of this range into L2 meanwhile (not a tile at the tensor's end)
+          if (kt + 1 < wi.u1) {
+            const TileMap nk = tile_map(p.maps, p.B, kMapK, wi.b, k0, kt + 1, p.total_kv);
+            const TileMap nv = tile_map(p.maps, p.B, kMapV, wi.b, k0, kt + 1, p.total_kv);
+            if (!nk.tail) {
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              tma_prefetch_2d(mk, wi.h * D + c * 64, (kt + 1) * kBN);
-              tma_prefetch_2d(mv, wi.h * D + c * 64, (kt + 1) * kBN);
+              for (int c = 0; c < D / 64; ++c) {
+                tma_prefetch_2d(nk.map, wi.h * D + c * 64, nk.y);
+                tma_prefetch_2d(nv.map, wi.h * D + c * 64, nv.y);
+              }
             }
           }
         }
@@ -298,12 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     if (lane == 0) {
       uint32_t ring_n = 0, qtile_n = 0, tn = 0;
       bool ok = true;
-      auto fill = [&](const CUtensorMap* m, int col, int row, const float* l2src, const float* dsrc) {
+      auto fill = [&](const TileMap& m, int col, const float* l2src, const float* dsrc) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
+        if (m.tail) tmap_acquire(m.map);
         if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
         trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes + (l2src ? 2 * kBM * 4 : 0));
-        load_tile<D>(sRing + e * C::kTileBytes, m, &ring_full[e], col, row);
+        load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
         if (l2src) {
           float* v = sVec + (qtile_n % C::kVecSlots) * 256;
           bulk_load(v, l2src, kBM * 4, &ring_full[e]);
@@ -316,18 +327,19 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         const WorkItem wi = p.items[idx];
         int Lq, Lk;
         seq_len(wi.b, &Lq, &Lk);
-        const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
-        const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
-        tmap_acquire(mq);
-        tmap_acquire(mdo);
+        const int64_t q0 = p.q_off[wi.b];
+        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapQ);
+        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapDO);
         const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + p.qpad[wi.b];
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
           q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
           for (int i = 0; i < count && ok; ++i) {
             const int qt = first + i;
-            if (!fill(mdo, wi.h * D, qt * kBM, nullptr, nullptr)) { ok = false; break; }
-            if (!fill(mq, wi.h * D, qt * kBM, p.lse2 + vec0 + qt * kBM, p.delta + vec0 + qt * kBM)) {
+            const TileMap mdo = tile_map(p.maps, p.B, kMapDO, wi.b, q0, qt, p.total_q);
+            const TileMap mq = tile_map(p.maps, p.B, kMapQ, wi.b, q0, qt, p.total_q);
+            if (!fill(mdo, wi.h * D, nullptr, nullptr)) { ok = false; break; }
+            if (!fill(mq, wi.h * D, p.lse2 + vec0 + qt * kBM, p.delta + vec0 + qt * kBM)) {
               ok = false;
               break;
             }
@@ -640,23 +652,33 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
        const WorkItem wi = p.items[idx];
        int Lq, Lk;
        seq_len(wi.b, &Lq, &Lk);
-       const CUtensorMap* mq = p.maps + size_t(wi.b) * kNumMapSlots + kMapQ;
-       const CUtensorMap* mdo = p.maps + size_t(wi.b) * kNumMapSlots + kMapDO;
-       tmap_acquire(mq);
-       tmap_acquire(mdo);
+       const int64_t q0 = p.q_off[wi.b];
+       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapQ);
+       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapDO);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         if (kv_tiles_for_q_tile(qt, Lq, Lk, causal) == 0) continue;
+        const TileMap mq = tile_map(p.maps, p.B, kMapQ, wi.b, q0, qt, p.total_q);
+        const TileMap mdo = tile_map(p.maps, p.B, kMapDO, wi.b, q0, qt, p.total_q);
+        if (mq.tail) {
+          tmap_acquire(mq.map);
+          tmap_acquire(mdo.map);
+        }
         if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
-        load_tile<D>(sQ, mq, &qdo_full, wi.h * D, qt * kBM);
-        load_tile<D>(sDO, mdo, &qdo_full, wi.h * D, qt * kBM);
+        load_tile<D>(sQ, mq.map, &qdo_full, wi.h * D, mq.y);
+        load_tile<D>(sDO, mdo.map, &qdo_full, wi.h * D, mdo.y);
         ++item_n;
-        if (qt + 1 < wi.u1) {  // pull the next query tile of this range into L2 meanwhile
+        // pull the next query tile of this range into L2 meanwhile (not a tile at the tensor's end)
+        if (qt + 1 < wi.u1) {
+          const TileMap nq = tile_map(p.maps, p.B, kMapQ, wi.b, q0, qt + 1, p.total_q);
+          const TileMap ndo = tile_map(p.maps, p.B, kMapDO, wi.b, q0, qt + 1, p.total_q);
+          if (!nq.tail) {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            tma_prefetch_2d(mq, wi.h * D + c * 64, (qt + 1) * kBM);
-            tma_prefetch_2d(mdo, wi.h * D + c * 64, (qt + 1) * kBM);
+            for (int c = 0; c < D / 64; ++c) {
+              tma_prefetch_2d(nq.map, wi.h * D + c * 64, nq.y);
+              tma_prefetch_2d(ndo.map, wi.h * D + c * 64, ndo.y);
+            }
           }
         }
        }
@@ -669,12 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     if (lane == 0) {
       uint32_t ring_n = 0, tn = 0;
       bool ok = true;
-      auto fill = [&](const CUtensorMap* m, int col, int row) {
+      auto fill = [&](const TileMap& m, int col) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
+        if (m.tail) tmap_acquire(m.map);
         if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
         trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
-        load_tile<D>(sRing + e * C::kTileBytes, m, &ring_full[e], col, row);
+        load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
         ++ring_n;
         return true;
       };
@@ -682,14 +705,15 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
        const WorkItem wi = p.items[idx];
        int Lq, Lk;
        seq_len(wi.b, &Lq, &Lk);
-       const CUtensorMap* mk = p.maps + size_t(wi.b) * kNumMapSlots + kMapK;
-       const CUtensorMap* mv = p.maps + size_t(wi.b) * kNumMapSlots + kMapV;
-       tmap_acquire(mk);
-       tmap_acquire(mv);
+       const int64_t k0 = p.kv_off[wi.b];
+       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapK);
+       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapV);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         for (int jt = 0; jt < nkv && ok; ++jt) {
-          if (!fill(mv, wi.h * D, jt * kBN) || !fill(mk, wi.h * D, jt * kBN)) { ok = false; break; }
+          const TileMap mv = tile_map(p.maps, p.B, kMapV, wi.b, k0, jt, p.total_kv);
+          const TileMap mk = tile_map(p.maps, p.B, kMapK, wi.b, k0, jt, p.total_kv);
+          if (!fill(mv, wi.h * D) || !fill(mk, wi.h * D)) { ok = false; break; }
         }
        }
       }
@@ -896,6 +920,7 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   BwdParams bp;
   bp.q_off = pr.q_off;
   bp.kv_off = pr.kv_off;
+  bp.B = pr.B;
   bp.H = pr.H;
   bp.total_q = pr.total_q;
   bp.total_kv = pr.total_kv;

@@ -44,6 +44,16 @@ constexpr int kItemsPerCta = 4;  // target items per CTA when capping range cost
 // so rows past it arrive as zeros).
 enum MapSlot { kMapQ = 0, kMapK = 1, kMapV = 2, kMapDO = 3, kNumMapSlots = 4 };
 
+// A map whose row extent was shortened on the device still has the TMA unit READ every
+// row of a box from memory (the rows past the extent are only zero-filled in shared
+// memory), so a box at the tail of the last sequence would read up to 127 rows past the
+// end of the caller's tensor.  Boxes that would cross a tensor's last row therefore load
+// from a workspace copy of its last 128 rows followed by 128 rows of slack, through
+// "tail maps": one per possible start row of such a box (start - (total - 128) is in
+// [1, 127]), stored after the per-sequence maps.
+constexpr int kTailRows = 2 * kBM;  // rows per tensor in the workspace tail copy
+constexpr int kTailMaps = kBM;      // tail maps per tensor
+
 // Header at the start of the workspace.
 // Developer tracing (off unless a buffer is configured): one thread per warp role of
 // CTA 0 records (SM clock << 16 | role << 8 | event) into its own region of `cap` entries.
@@ -81,7 +91,9 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct WsLayout {
-  size_t maps = 0;     // CUtensorMap[B][kNumMapSlots]
+  size_t maps = 0;       // CUtensorMap[B][kNumMapSlots], then CUtensorMap[kNumMapSlots][kTailMaps]
+  size_t tail = 0;       // per used slot: kTailRows rows of the tensor's row pitch (tail copies)
+  size_t row_bytes = 0;  // H * d * 2, the row pitch of q, k, v, dout
   size_t fwd = 0;      // WorkItem[cap_fwd]
   size_t dq = 0;       // WorkItem[cap_dq]
   size_t dkv = 0;      // WorkItem[cap_dkv]
@@ -97,12 +109,15 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 
 // Capacities are upper bounds on the item counts for any offsets with these totals:
 //   sum_b ceil(ceil(L_b/128)/2) <= total/256 + B,  sum_b ceil(L_b/128) <= total/128 + B.
-__host__ __device__ inline WsLayout make_layout(int B, int H, int64_t total_q, int64_t total_kv,
+__host__ __device__ inline WsLayout make_layout(int B, int H, int d, int64_t total_q, int64_t total_kv,
                                                 bool backward) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
   L.maps = align_up(off, 128);
-  off = L.maps + size_t(B) * kNumMapSlots * 128;
+  off = L.maps + (size_t(B) + kTailMaps) * kNumMapSlots * 128;
+  L.row_bytes = size_t(H) * size_t(d) * 2;
+  L.tail = align_up(off, 1024);
+  off = L.tail + size_t(backward ? 4 : 3) * kTailRows * L.row_bytes;
   L.cap_fwd = int64_t(H) * (total_q / 256 + B + 1);
   L.fwd = align_up(off, 16);
   off = L.fwd + size_t(L.cap_fwd) * sizeof(WorkItem);
@@ -160,5 +175,24 @@ __host__ __device__ inline void q_tiles_for_kv_tile(int t, int Lq, int Lk, bool 
   *first = i_min / kBM;
   *count = nq - *first;
 }
+
+#ifdef __CUDACC__
+// The tensor map and box row coordinate that load row tile `t` of a sequence starting at
+// row `row0` of a tensor with `total` rows: the sequence's own map, or the tail map when
+// the 128-row box would reach past the tensor's last row (such a tile is always the
+// sequence's last; its tail map points at the tile's first row, so the box starts at 0).
+struct TileMap {
+  const CUtensorMap* map;
+  int y;
+  bool tail;
+};
+__device__ __forceinline__ TileMap tile_map(const CUtensorMap* maps, int B, int slot, int b, int64_t row0, int t,
+                                            int64_t total) {
+  const int64_t g0 = row0 + int64_t(t) * kBM;
+  if (g0 + kBM > total)
+    return {maps + size_t(B) * kNumMapSlots + size_t(slot) * kTailMaps + size_t(g0 + kBM - total), 0, true};
+  return {maps + size_t(b) * kNumMapSlots + slot, t * kBM, false};
+}
+#endif
 
 }  // namespace jfa

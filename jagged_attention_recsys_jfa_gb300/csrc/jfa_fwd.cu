@@ -39,8 +39,8 @@ static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds t
 struct FwdParams {
   const int64_t* q_off;
   const int64_t* kv_off;
-  int H;
-  int64_t total_q;
+  int B, H;
+  int64_t total_q, total_kv;
   float scale_log2;      // scale * log2(e), > 0
   int causal;
   const float* bias2;    // [H][num_buckets] bias * log2(e), or nullptr
@@ -155,23 +155,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
-        const CUtensorMap* mq = p.maps + size_t(it.b) * kNumMapSlots + kMapQ;
-        tmap_acquire(mq);
+        const TileMap q0 = tile_map(p.maps, p.B, kMapQ, it.b, it.qo, it.t0, p.total_q);
+        const TileMap q1 = it.has1 ? tile_map(p.maps, p.B, kMapQ, it.b, it.qo, it.t1, p.total_q) : q0;
+        tmap_acquire(q0.map);
+        if (q1.map != q0.map) tmap_acquire(q1.map);
         if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&q_full, (it.has1 ? 2 : 1) * C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kBoxes; ++c) {
-          tma_load_2d(sQ + c * 16384, mq, &q_full, it.h * D + c * 64, it.t0 * kBM);
-          if (it.has1) tma_load_2d(sQ + C::kTileBytes + c * 16384, mq, &q_full, it.h * D + c * 64, it.t1 * kBM);
+          tma_load_2d(sQ + c * 16384, q0.map, &q_full, it.h * D + c * 64, q0.y);
+          if (it.has1) tma_load_2d(sQ + C::kTileBytes + c * 16384, q1.map, &q_full, it.h * D + c * 64, q1.y);
         }
         ++item_n;
-        // pull the next pair of this range into L2 meanwhile
+        // pull the next pair of this range into L2 meanwhile (not a tile at the tensor's end)
         if (u + 1 < wi.u1) {
+          for (int t = 2 * (u + 1); t < 2 * (u + 1) + 2 && t * kBM < it.Lq; ++t) {
+            const TileMap qn = tile_map(p.maps, p.B, kMapQ, it.b, it.qo, t, p.total_q);
+            if (qn.tail) continue;
 #pragma unroll
-          for (int c = 0; c < C::kBoxes; ++c)
-            for (int t = 2 * (u + 1); t < 2 * (u + 1) + 2 && t * kBM < it.Lq; ++t)
-              tma_prefetch_2d(mq, it.h * D + c * 64, t * kBM);
+            for (int c = 0; c < C::kBoxes; ++c) tma_prefetch_2d(qn.map, it.h * D + c * 64, qn.y);
+          }
         }
        }
       }
@@ -188,11 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
-        const CUtensorMap* mk = p.maps + size_t(it.b) * kNumMapSlots + kMapK;
-        const CUtensorMap* mv = p.maps + size_t(it.b) * kNumMapSlots + kMapV;
-        tmap_acquire(mk);
-        tmap_acquire(mv);
+        tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapK);
+        tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapV);
         for (int j = 0; j < it.njt && ok; ++j) {
+          const TileMap mk = tile_map(p.maps, p.B, kMapK, it.b, it.ko, j, p.total_kv);
+          const TileMap mv = tile_map(p.maps, p.B, kMapV, it.b, it.ko, j, p.total_kv);
+          if (mk.tail) {
+            tmap_acquire(mk.map);
+            tmap_acquire(mv.map);
+          }
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t e = ring_n % C::kStages, ph = (ring_n / C::kStages) & 1;
@@ -202,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             uint8_t* dst = sRing + e * C::kTileBytes;
 #pragma unroll
             for (int c = 0; c < C::kBoxes; ++c)
-              tma_load_2d(dst + c * 16384, kv ? mv : mk, &kv_full[e], it.h * D + c * 64, j * kBN);
+              tma_load_2d(dst + c * 16384, kv ? mv.map : mk.map, &kv_full[e], it.h * D + c * 64, mk.y);
             ++ring_n;
           }
         }
@@ -506,8 +514,10 @@ cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void*
   FwdParams fp;
   fp.q_off = pr.q_off;
   fp.kv_off = pr.kv_off;
+  fp.B = pr.B;
   fp.H = pr.H;
   fp.total_q = pr.total_q;
+  fp.total_kv = pr.total_kv;
   fp.scale_log2 = pr.scale * kLog2e;
   fp.causal = pr.causal;
   fp.bias2 = pr.bias_table ? reinterpret_cast<const float*>(w + L.bias2) : nullptr;

@@ -205,8 +205,25 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     return;
   }
 
+  // ---- tail copies: the last min(128, total) rows of each tensor, which the boxes that
+  //      would otherwise read past the tensor's last row load from instead
+  const size_t rb = p.L.row_bytes;
+  for (int slot = 0; slot < kNumMapSlots; ++slot) {
+    if (!maps.used[slot]) continue;
+    const int64_t total = (slot == kMapQ || slot == kMapDO) ? p.total_q : p.total_kv;
+    if (total <= 0) continue;
+    const int64_t n = total < kBM ? total : kBM;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(maps.base[slot]) +
+                                                      size_t(total - n) * rb);
+    uint4* dst = reinterpret_cast<uint4*>(p.ws + p.L.tail + size_t(slot) * kTailRows * rb);
+    const size_t nvec = size_t(n) * rb / 16;
+    for (size_t i = tid; i < nvec; i += blockDim.x) dst[i] = src[i];
+  }
+
   // ---- per-sequence tensor maps: copy the template, point it at the sequence's first
-  //      row and clip its row extent to the sequence length.
+  //      row and clip its row extent to the sequence length.  A sequence whose last tile
+  //      would reach past the tensor's last row also gets a tail map over the tail copy,
+  //      pointed at that tile's first row and clipped to the tile's rows.
   CUtensorMap* out_maps = reinterpret_cast<CUtensorMap*>(p.ws + p.L.maps);
   for (int idx = tid; idx < p.B * kNumMapSlots; idx += blockDim.x) {
     const int b = idx / kNumMapSlots, slot = idx % kNumMapSlots;
@@ -214,13 +231,25 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     const bool is_q_side = (slot == kMapQ || slot == kMapDO);
     const int64_t row0 = is_q_side ? p.q_off[b] : p.kv_off[b];
     const int64_t len = (is_q_side ? p.q_off[b + 1] : p.kv_off[b + 1]) - row0;
-    CUtensorMap* dst = out_maps + idx;
     const uint4* src = reinterpret_cast<const uint4*>(&maps.tmpl[slot]);
+    CUtensorMap* dst = out_maps + idx;
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int i = 0; i < 8; ++i) d4[i] = src[i];
-    tmap_replace_address(dst, static_cast<const uint8_t*>(maps.base[slot]) + row0 * int64_t(maps.row_bytes[slot]));
+    tmap_replace_address(dst, static_cast<const uint8_t*>(maps.base[slot]) + row0 * int64_t(rb));
     tmap_replace_dim1(dst, uint32_t(len > 0 ? len : 1));
+    if (len <= 0) continue;
+    const int64_t total = is_q_side ? p.total_q : p.total_kv;
+    const int64_t g0 = row0 + (len - 1) / kBM * kBM;  // first row of the sequence's last tile
+    if (g0 + kBM > total) {
+      const int64_t n = total < kBM ? total : kBM;  // rows in the tail copy; it starts at row total - n
+      CUtensorMap* tdst = out_maps + size_t(p.B) * kNumMapSlots + size_t(slot) * kTailMaps + size_t(g0 + kBM - total);
+      uint4* t4 = reinterpret_cast<uint4*>(tdst);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t4[i] = src[i];
+      tmap_replace_address(tdst, p.ws + p.L.tail + size_t(slot) * kTailRows * rb + size_t(g0 - (total - n)) * rb);
+      tmap_replace_dim1(tdst, uint32_t(row0 + len - g0));
+    }
   }
   tmap_release();
 

@@ -52,6 +52,12 @@ EDGE = {
     "causal_lq_gt_lk": (dict(heads=2, head_dim=128), [300, 64, 129], [40, 1, 128], True, False),
     "causal_lq_lt_lk": (dict(heads=2, head_dim=64), [40, 1, 128], [300, 64, 129], True, False),
     "cross_noncausal_bias": (dict(heads=2, head_dim=128), [33, 1, 200], [500, 2, 129], False, True),
+    # last tiles of several sequences reach past the tensor's last row (tail maps): the
+    # clipped rows of an earlier sequence's box hold a later sequence's keys, which must
+    # still arrive as zeros; totals below one tile; trailing empty sequences
+    "tail_two_crossing": (dict(heads=2, head_dim=128), [200, 1], [130, 70], False, False),
+    "tail_trailing_empty": (dict(heads=2, head_dim=128), [90, 0, 0], [260, 0, 0], False, False),
+    "tail_crossing_causal_bias_d64": (dict(heads=3, head_dim=64), [129, 3, 0], [131, 0, 2], True, True),
     # one long sequence with many tiles
     "long_single_d128": (dict(heads=1, head_dim=128), [1500], None, False, False),
     "long_single_causal_d64": (dict(heads=2, head_dim=64), [1100], None, True, True),
