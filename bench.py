@@ -419,12 +419,29 @@ def run_jfa(args, rank, world, device):
     return res
 
 
+def kernel_source_hash():
+    """Hash of the kernel sources; DRAM counters taken from other sources are stale."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "jagged_attention_recsys_jfa_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                    glob.glob(os.path.join(csrc, "*.h"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if one matches."""
+    """DRAM bytes (read + write) per launch from the committed ncu summary, if one matches
+    this workload and was taken on the kernel sources as they are now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
+        if t.get("source_sha") != kernel_source_hash():
+            return None
         return t.get(workload, {}).get(kernel)
     except Exception:
         return None
