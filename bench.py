@@ -65,6 +65,20 @@ def workload_flops(batch):
     return {"pairs": P, "fwd": 4.0 * dH * P, "bwd": 10.0 * dH * P, "dkdv": 8.0 * dH * P, "dq": 2.0 * dH * P}
 
 
+def workload_bytes(batch):
+    """Algorithmic DRAM bytes per launch of each kernel: every input read once, every
+    output written once (the per-query lse / D vectors on 128-row-padded rows)."""
+    H, d = batch.cfg.heads, batch.cfg.head_dim
+    row = 2.0 * H * d
+    Tq, Tk = float(batch.q_lengths.sum()), float(batch.kv_lengths.sum())
+    qpad = float(((batch.q_lengths + 127) // 128 * 128).sum())
+    vec = 8.0 * H * qpad  # lse*log2(e) and D, fp32
+    return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq,
+            "bwd_preprocess": 2 * Tq * row + 4.0 * H * Tq + vec,
+            "bwd_dkdv": (2 * Tq + 2 * Tk) * row + vec + 2 * Tk * row,
+            "bwd_dq": (2 * Tq + 2 * Tk) * row + vec + Tq * row}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -364,15 +378,30 @@ def run_jfa(args, rank, world, device):
     kinds = {k: v for k, v in per_kernel.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
     algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"]}
+    algo_bytes = workload_bytes(batch)
     ms_dom, n_dom = kinds[dom]
+    t_dom = ms_dom / n_dom / 1e3
     traffic = load_traffic(dom, name)
-    if dom in algo:
-        achieved = algo[dom] / (ms_dom / n_dom / 1e3) / 1e12
+    # the binding roof: tensor when the kernel's algorithmic flops per byte reach the
+    # ridge of the measured peaks, else HBM
+    ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    if dom in algo and algo[dom] / algo_bytes[dom] >= ridge:
+        achieved = algo[dom] / t_dom / 1e12
         peak = float(peaks["bf16_tflops"])
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                     "peak_source": f"{peak_src} bf16 dense (burst)",
-                    "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)}
+                    "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
+                    "flop_per_byte": round(algo[dom] / algo_bytes[dom], 1), "ridge": round(ridge, 1)}
+    elif dom in algo_bytes:
+        achieved = algo_bytes[dom] / t_dom / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "peak_source": f"{peak_src} HBM copy",
+                    "algorithmic_bytes": algo_bytes[dom],
+                    "flop_per_byte": round(algo[dom] / algo_bytes[dom], 1) if dom in algo else None,
+                    "ridge": round(ridge, 1)}
     else:
         roofline = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": float(peaks["hbm_gbs"]),
                     "unit": "GB/s", "frac": None, "traffic": traffic}
@@ -381,6 +410,9 @@ def run_jfa(args, rank, world, device):
     for k, f in algo.items():
         if k in kernels:
             kernels[k]["algorithmic_tflops"] = round(f / (kernels[k]["ms_per_launch"] / 1e3) / 1e12, 1)
+    for k, nb in algo_bytes.items():
+        if k in kernels:
+            kernels[k]["algorithmic_gbs"] = round(nb / (kernels[k]["ms_per_launch"] / 1e3) / 1e9, 1)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:

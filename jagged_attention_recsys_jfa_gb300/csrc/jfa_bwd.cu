@@ -21,6 +21,7 @@
 
 #include "jfa_internal.h"
 #include "sm100_ptx.cuh"
+#include "jfa_sched.cuh"
 
 namespace jfa {
 namespace {
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
   __shared__ uint64_t ring_full[R], ring_empty[R];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ MetaRing meta;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
+    meta_init(meta);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -262,14 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     // dP^T MMA frees the buffers, whatever the ring producer is waiting on.
     if (lane == 0) {
       uint32_t item_n = 0, tn = 0;
+      int acq_b = -1;  // sequence whose maps this thread has acquired
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const WorkItem wi = p.items[idx];
-        int Lq, Lk;
-        seq_len(wi.b, &Lq, &Lk);
-        const int64_t k0 = p.kv_off[wi.b];
-        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapK);
-        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapV);
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+        const int Lq = wi.Lq, Lk = wi.Lk;
+        const int64_t k0 = wi.ko;
+        acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
           q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
@@ -286,19 +290,27 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
           load_tile<D>(sK, mk.map, &kv_full, wi.h * D, mk.y);
           load_tile<D>(sV, mv.map, &kv_full, wi.h * D, mv.y);
           ++item_n;
-          // pull the next key tile of this range into L2 meanwhile (not a tile at the tensor's end)
-          if (kt + 1 < wi.u1) {
-            const TileMap nk = tile_map(p.maps, p.B, kMapK, wi.b, k0, kt + 1, p.total_kv);
-            const TileMap nv = tile_map(p.maps, p.B, kMapV, wi.b, k0, kt + 1, p.total_kv);
-            if (!nk.tail) {
-#pragma unroll
-              for (int c = 0; c < D / 64; ++c) {
-                tma_prefetch_2d(nk.map, wi.h * D + c * 64, nk.y);
-                tma_prefetch_2d(nv.map, wi.h * D + c * 64, nv.y);
+          // pull the next key tile into L2 meanwhile: the next of this range, else the first
+          // of this CTA's next item
+          {
+            int nb = -1, nh = 0, nt = 0;
+            if (kt + 1 < wi.u1) {
+              nb = wi.b, nh = wi.h, nt = kt + 1;
+            } else if (idx + int(gridDim.x) < n_items) {
+              const WorkItem wn = p.items[idx + gridDim.x];
+              nb = wn.b, nh = wn.h, nt = wn.u0;
+            }
+            if (nb >= 0) {
+              const int64_t nko = p.kv_off[nb];
+              acquire_seq_maps(p.maps, nb, kMapK, kMapV, acq_b, true);
+              if (nt * kBN < int(p.kv_off[nb + 1] - nko)) {
+                prefetch_tile<D / 64>(p.maps, p.B, kMapK, nb, nko, nt, p.total_kv, nh * D);
+                prefetch_tile<D / 64>(p.maps, p.B, kMapV, nb, nko, nt, p.total_kv, nh * D);
               }
             }
           }
         }
+        if (ok) meta_release(meta, item_k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       if (item_n > 0) drain_wait(&kv_full, (item_n - 1) & 1);
@@ -307,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     // ------------------------------------------------------------ dO / Q ring producer
     if (lane == 0) {
       uint32_t ring_n = 0, qtile_n = 0, tn = 0;
+      int acq_b = -1;  // sequence whose maps this thread has acquired
       bool ok = true;
       auto fill = [&](const TileMap& m, int col, const float* l2src, const float* dsrc) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
@@ -323,17 +336,30 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         ++ring_n;
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-        const WorkItem wi = p.items[idx];
-        int Lq, Lk;
-        seq_len(wi.b, &Lq, &Lk);
-        const int64_t q0 = p.q_off[wi.b];
-        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapQ);
-        tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapDO);
-        const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + p.qpad[wi.b];
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+        const int Lq = wi.Lq, Lk = wi.Lk;
+        const int64_t q0 = wi.qo;
+        acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
+        const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + wi.qp;
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
           q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+          if (kt + 1 == wi.u1 && idx + int(gridDim.x) < n_items) {
+            // pull the first query tiles of this CTA's next item into L2 meanwhile
+            const WorkItem wn = p.items[idx + gridDim.x];
+            int nLq, nLk, nfirst, ncount;
+            seq_len(wn.b, &nLq, &nLk);
+            q_tiles_for_kv_tile(wn.u0, nLq, nLk, causal, &nfirst, &ncount);
+            const int64_t nqo = p.q_off[wn.b];
+            acquire_seq_maps(p.maps, wn.b, kMapQ, kMapDO, acq_b, true);
+            for (int t = nfirst; t < nfirst + min(ncount, 2); ++t) {
+              prefetch_tile<D / 64>(p.maps, p.B, kMapDO, wn.b, nqo, t, p.total_q, wn.h * D);
+              prefetch_tile<D / 64>(p.maps, p.B, kMapQ, wn.b, nqo, t, p.total_q, wn.h * D);
+            }
+          }
           for (int i = 0; i < count && ok; ++i) {
             const int qt = first + i;
             const TileMap mdo = tile_map(p.maps, p.B, kMapDO, wi.b, q0, qt, p.total_q);
@@ -346,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
             ++qtile_n;
           }
         }
+        if (ok) meta_release(meta, item_k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
@@ -383,10 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
           umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * 64 + (kk & 3) * 8, bd + uint32_t(kk * 2048 >> 4), kIdAcc,
                   (acc || kk > 0) ? 1u : 0u);
       };
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
-       int Lq, Lk;
-       seq_len(wi.b, &Lq, &Lk);
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+       if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       const int Lq = wi.Lq, Lk = wi.Lk;
        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
         int first, count;
         q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
@@ -439,11 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         ++acc_n;
         umma_commit(&dk_full);
        }
+       if (ok) meta_release(meta, item_k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
+   } else if (warp == 3) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
+      raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else {
     setmaxnreg_inc<kRegsCompute>();
@@ -458,11 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     uint32_t ring_n = 0, tile_n = 0, acc_n = 0, qtile_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-     const WorkItem it = p.items[idx];
-     const int64_t ko = p.kv_off[it.b];
-     int Lq, Lk;
-     seq_len(it.b, &Lq, &Lk);
+    uint32_t item_k = 0;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     const int64_t ko = it.ko;
+     const int Lq = it.Lq, Lk = it.Lk;
      for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
       int first, count;
       q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
@@ -570,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       mbar_arrive(&dk_empty);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
      }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
   }
@@ -603,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   __shared__ uint64_t ring_full[R], ring_empty[R];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ MetaRing meta;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -622,6 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
+    meta_init(meta);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -647,14 +684,15 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     // ------------------------------------------------------------ Q / dO loader
     if (lane == 0) {
       uint32_t item_n = 0, tn = 0;
+      int acq_b = -1;  // sequence whose maps this thread has acquired
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
-       int Lq, Lk;
-       seq_len(wi.b, &Lq, &Lk);
-       const int64_t q0 = p.q_off[wi.b];
-       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapQ);
-       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapDO);
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+       if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       const int Lq = wi.Lq, Lk = wi.Lk;
+       const int64_t q0 = wi.qo;
+       acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         if (kv_tiles_for_q_tile(qt, Lq, Lk, causal) == 0) continue;
         const TileMap mq = tile_map(p.maps, p.B, kMapQ, wi.b, q0, qt, p.total_q);
@@ -669,19 +707,27 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         load_tile<D>(sQ, mq.map, &qdo_full, wi.h * D, mq.y);
         load_tile<D>(sDO, mdo.map, &qdo_full, wi.h * D, mdo.y);
         ++item_n;
-        // pull the next query tile of this range into L2 meanwhile (not a tile at the tensor's end)
-        if (qt + 1 < wi.u1) {
-          const TileMap nq = tile_map(p.maps, p.B, kMapQ, wi.b, q0, qt + 1, p.total_q);
-          const TileMap ndo = tile_map(p.maps, p.B, kMapDO, wi.b, q0, qt + 1, p.total_q);
-          if (!nq.tail) {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              tma_prefetch_2d(nq.map, wi.h * D + c * 64, nq.y);
-              tma_prefetch_2d(ndo.map, wi.h * D + c * 64, ndo.y);
+        // pull the next query tile into L2 meanwhile: the next of this range, else the first
+        // of this CTA's next item
+        {
+          int nb = -1, nh = 0, nt = 0;
+          if (qt + 1 < wi.u1) {
+            nb = wi.b, nh = wi.h, nt = qt + 1;
+          } else if (idx + int(gridDim.x) < n_items) {
+            const WorkItem wn = p.items[idx + gridDim.x];
+            nb = wn.b, nh = wn.h, nt = wn.u0;
+          }
+          if (nb >= 0) {
+            const int64_t nqo = p.q_off[nb];
+            acquire_seq_maps(p.maps, nb, kMapQ, kMapDO, acq_b, true);
+            if (nt * kBM < int(p.q_off[nb + 1] - nqo)) {
+              prefetch_tile<D / 64>(p.maps, p.B, kMapQ, nb, nqo, nt, p.total_q, nh * D);
+              prefetch_tile<D / 64>(p.maps, p.B, kMapDO, nb, nqo, nt, p.total_q, nh * D);
             }
           }
         }
        }
+       if (ok) meta_release(meta, item_k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       if (item_n > 0) drain_wait(&qdo_full, (item_n - 1) & 1);
@@ -690,6 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     // ------------------------------------------------------------ V / K ring producer
     if (lane == 0) {
       uint32_t ring_n = 0, tn = 0;
+      int acq_b = -1;  // sequence whose maps this thread has acquired
       bool ok = true;
       auto fill = [&](const TileMap& m, int col) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
@@ -701,21 +748,33 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         ++ring_n;
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
-       int Lq, Lk;
-       seq_len(wi.b, &Lq, &Lk);
-       const int64_t k0 = p.kv_off[wi.b];
-       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapK);
-       tmap_acquire(p.maps + size_t(wi.b) * kNumMapSlots + kMapV);
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+       if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       const int Lq = wi.Lq, Lk = wi.Lk;
+       const int64_t k0 = wi.ko;
+       acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
+        if (qt + 1 == wi.u1 && idx + int(gridDim.x) < n_items) {
+          // pull the first key tiles of this CTA's next item into L2 meanwhile
+          const WorkItem wn = p.items[idx + gridDim.x];
+          const int64_t nko = p.kv_off[wn.b];
+          const int nLk = int(p.kv_off[wn.b + 1] - nko);
+          acquire_seq_maps(p.maps, wn.b, kMapK, kMapV, acq_b, true);
+          for (int t = 0; t < 2 && t * kBN < nLk; ++t) {
+            prefetch_tile<D / 64>(p.maps, p.B, kMapV, wn.b, nko, t, p.total_kv, wn.h * D);
+            prefetch_tile<D / 64>(p.maps, p.B, kMapK, wn.b, nko, t, p.total_kv, wn.h * D);
+          }
+        }
         for (int jt = 0; jt < nkv && ok; ++jt) {
           const TileMap mv = tile_map(p.maps, p.B, kMapV, wi.b, k0, jt, p.total_kv);
           const TileMap mk = tile_map(p.maps, p.B, kMapK, wi.b, k0, jt, p.total_kv);
           if (!fill(mv, wi.h * D) || !fill(mk, wi.h * D)) { ok = false; break; }
         }
        }
+       if (ok) meta_release(meta, item_k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
@@ -743,10 +802,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
           umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
         }
       };
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
-       int Lq, Lk;
-       seq_len(wi.b, &Lq, &Lk);
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+       if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       const int Lq = wi.Lq, Lk = wi.Lk;
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         if (nkv == 0) continue;
@@ -803,11 +863,16 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         ++acc_n;
         umma_commit(&acc_full);
        }
+       if (ok) meta_release(meta, item_k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
+   } else if (warp == 3) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
+      raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else {
     setmaxnreg_inc<kRegsCompute>();
@@ -820,12 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     uint32_t tile_n = 0, acc_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-     const WorkItem it = p.items[idx];
-     const int64_t qo = p.q_off[it.b];
-     int Lq, Lk;
-     seq_len(it.b, &Lq, &Lk);
-     const int64_t vec0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
+    uint32_t item_k = 0;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     const int64_t qo = it.qo;
+     const int Lq = it.Lq, Lk = it.Lk;
+     const int64_t vec0 = int64_t(it.h) * p.qpad_cap + it.qp;
      for (int qt = it.u0; qt < it.u1 && ok; ++qt) {
       const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
       const int i = qt * kBM + row;
@@ -905,6 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       tc_fence_before();
       mbar_arrive(&acc_empty);
      }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
   }

@@ -193,6 +193,20 @@ __device__ __forceinline__ TileMap tile_map(const CUtensorMap* maps, int B, int 
     return {maps + size_t(B) * kNumMapSlots + size_t(slot) * kTailMaps + size_t(g0 + kBM - total), 0, true};
   return {maps + size_t(b) * kNumMapSlots + slot, t * kBM, false};
 }
+
+// Pull row tile `t` of a sequence (boxes of 64 columns from column col0) into L2 ahead of
+// its load.  Tiles whose box would reach past the tensor's last row are skipped.
+template <int kBoxes>
+__device__ __forceinline__ void prefetch_tile(const CUtensorMap* maps, int B, int slot, int b, int64_t row0, int t,
+                                              int64_t total, int col0) {
+  const TileMap m = tile_map(maps, B, slot, b, row0, t, total);
+  if (m.tail) return;
+#pragma unroll
+  for (int c = 0; c < kBoxes; ++c)
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(m.map), "r"(col0 + c * 64),
+                 "r"(m.y)
+                 : "memory");
+}
 #endif
 
 }  // namespace jfa

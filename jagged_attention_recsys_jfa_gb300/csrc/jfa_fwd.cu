@@ -12,20 +12,23 @@
 //
 // How (one persistent CTA per SM, "Four generations" item 3: warp specialisation
 // plus persistent scheduling over a longest-first work list):
-//   warp 0      TMA producer: Q tile pair, then K_j, V_j into a ring of smem stages
+//   warp 0      K/V producer: K_j, V_j into a ring of smem stages (TMA)
 //   warp 1      MMA issuer:   S_s = Q_s K_j^T (tcgen05, SS, fp32 in TMEM);
 //                             O_s += P_s V_j (tcgen05, A = P from TMEM, B = V from smem)
-//   warps 2-5   softmax for query tile 0 of the pair (one TMEM lane = one query row)
-//   warps 6-9   softmax for query tile 1
+//   warp 2      Q loader: the unit's pair of query tiles
+//   warp 3      scheduler: work-item metadata into a shared-memory ring
+//   warps 4-7   softmax for query tile 0 of the pair (one TMEM lane = one query row)
+//   warps 8-11  softmax for query tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d, 256+2d).
-// P (bf16) overwrites the first 64 columns of its S region.  The issue order
-// PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) lets one tile's softmax overlap the other
-// tile's MMAs (ping-pong).  The running max is only raised (and O rescaled) when
-// it grows by more than 2^8, which keeps exp2 arguments <= 8 in between.
+// P (bf16, two per column) overwrites the first 64 columns of its S region.
+// The issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) lets one tile's softmax
+// overlap the other tile's MMAs (ping-pong).  The running max is only raised (and O
+// rescaled) when it grows by more than 2^8, which keeps exp2 arguments <= 8 in between.
 #include <cuda_bf16.h>
 
 #include "jfa_internal.h"
 #include "sm100_ptx.cuh"
+#include "jfa_sched.cuh"
 
 namespace jfa {
 namespace {
@@ -60,6 +63,7 @@ struct FwdCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kSmemBytes = 2 * kTileBytes + kStages * kTileBytes + 1024;
+  static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA (dynamic + static barriers)");
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 };
 
@@ -72,16 +76,16 @@ struct ItemInfo {
 };
 
 // Unit u (query-tile pair {2u, 2u+1}) of work item `it`.
-__device__ __forceinline__ ItemInfo decode(const FwdParams& p, const WorkItem& it, int u) {
+__device__ __forceinline__ ItemInfo decode(const FwdParams& p, const ItemMeta& it, int u) {
   ItemInfo r;
   r.b = it.b;
   r.h = it.h;
   r.t0 = 2 * u;
   r.t1 = r.t0 + 1;
-  r.qo = p.q_off[it.b];
-  r.ko = p.kv_off[it.b];
-  r.Lq = int(p.q_off[it.b + 1] - r.qo);
-  r.Lk = int(p.kv_off[it.b + 1] - r.ko);
+  r.qo = it.qo;
+  r.ko = it.ko;
+  r.Lq = it.Lq;
+  r.Lk = it.Lk;
   r.has1 = r.t1 * kBM < r.Lq;
   r.nkv0 = kv_tiles_for_q_tile(r.t0, r.Lq, r.Lk, p.causal != 0);
   r.nkv1 = r.has1 ? kv_tiles_for_q_tile(r.t1, r.Lq, r.Lk, p.causal != 0) : 0;
@@ -112,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
   __shared__ uint64_t s_full[2], p_full[2], o_full[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ MetaRing meta;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -128,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       mbar_init(&p_full[s], 128);
       mbar_init(&o_full[s], 1);
     }
+    meta_init(meta);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -150,15 +156,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     if (lane == 0) {
       uint32_t item_n = 0, tn = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
+      uint32_t k = 0;
+      // sequence whose Q map this thread has acquired: a map is acquired (and its
+      // descriptor prefetched) once, an item ahead, not before every load -- an acquire
+      // makes the next copy through the map wait for a fresh descriptor fetch
+      int acq_b = -1;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+       if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const TileMap q0 = tile_map(p.maps, p.B, kMapQ, it.b, it.qo, it.t0, p.total_q);
         const TileMap q1 = it.has1 ? tile_map(p.maps, p.B, kMapQ, it.b, it.qo, it.t1, p.total_q) : q0;
-        tmap_acquire(q0.map);
-        if (q1.map != q0.map) tmap_acquire(q1.map);
+        if (it.b != acq_b) {
+          tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapQ);
+          acq_b = it.b;
+        }
+        if (q0.tail) tmap_acquire(q0.map);
+        if (q1.tail && q1.map != q0.map) tmap_acquire(q1.map);
         if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&q_full, (it.has1 ? 2 : 1) * C::kTileBytes);
@@ -168,16 +184,31 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           if (it.has1) tma_load_2d(sQ + C::kTileBytes + c * 16384, q1.map, &q_full, it.h * D + c * 64, q1.y);
         }
         ++item_n;
-        // pull the next pair of this range into L2 meanwhile (not a tile at the tensor's end)
-        if (u + 1 < wi.u1) {
-          for (int t = 2 * (u + 1); t < 2 * (u + 1) + 2 && t * kBM < it.Lq; ++t) {
-            const TileMap qn = tile_map(p.maps, p.B, kMapQ, it.b, it.qo, t, p.total_q);
-            if (qn.tail) continue;
-#pragma unroll
-            for (int c = 0; c < C::kBoxes; ++c) tma_prefetch_2d(qn.map, it.h * D + c * 64, qn.y);
+        // pull the next pair into L2 meanwhile: the next unit of this range, else the first
+        // unit of this CTA's next item
+        {
+          int nb = -1, nh = 0, nu = 0;
+          if (u + 1 < wi.u1) {
+            nb = wi.b, nh = wi.h, nu = u + 1;
+          } else if (idx + int(gridDim.x) < n_items) {
+            const WorkItem wn = p.items[idx + gridDim.x];
+            nb = wn.b, nh = wn.h, nu = wn.u0;
+          }
+          if (nb >= 0) {
+            const int64_t nqo = p.q_off[nb];
+            const int nLq = int(p.q_off[nb + 1] - nqo);
+            if (nb != acq_b) {
+              const CUtensorMap* nm = p.maps + size_t(nb) * kNumMapSlots + kMapQ;
+              tmap_acquire(nm);
+              tmap_prefetch(nm);
+              acq_b = nb;
+            }
+            for (int t = 2 * nu; t < 2 * nu + 2 && t * kBM < nLq; ++t)
+              prefetch_tile<C::kBoxes>(p.maps, p.B, kMapQ, nb, nqo, t, p.total_q, nh * D);
           }
         }
        }
+       if (ok) meta_release(meta, k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       if (item_n > 0) drain_wait(&q_full, (item_n - 1) & 1);
@@ -187,13 +218,37 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     if (lane == 0) {
       uint32_t ring_n = 0, tn = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
+      uint32_t k = 0;
+      int acq_b = -1;  // sequence whose K / V maps this thread has acquired (see the Q loader)
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+       if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
-        tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapK);
-        tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapV);
+        if (it.b != acq_b) {
+          tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapK);
+          tmap_acquire(p.maps + size_t(it.b) * kNumMapSlots + kMapV);
+          acq_b = it.b;
+        }
+        // last unit of this item: pull the first key tiles of this CTA's next item into L2
+        if (u + 1 == wi.u1 && idx + int(gridDim.x) < n_items) {
+          const WorkItem wn = p.items[idx + gridDim.x];
+          const int64_t nko = p.kv_off[wn.b];
+          const int nLk = int(p.kv_off[wn.b + 1] - nko);
+          if (wn.b != acq_b) {
+            const CUtensorMap* nk = p.maps + size_t(wn.b) * kNumMapSlots + kMapK;
+            tmap_acquire(nk);
+            tmap_acquire(nk + (kMapV - kMapK));
+            tmap_prefetch(nk);
+            tmap_prefetch(nk + (kMapV - kMapK));
+            acq_b = wn.b;
+          }
+          for (int t = 0; t < 2 && t * kBN < nLk; ++t) {
+            prefetch_tile<C::kBoxes>(p.maps, p.B, kMapK, wn.b, nko, t, p.total_kv, wn.h * D);
+            prefetch_tile<C::kBoxes>(p.maps, p.B, kMapV, wn.b, nko, t, p.total_kv, wn.h * D);
+          }
+        }
         for (int j = 0; j < it.njt && ok; ++j) {
           const TileMap mk = tile_map(p.maps, p.B, kMapK, it.b, it.ko, j, p.total_kv);
           const TileMap mv = tile_map(p.maps, p.B, kMapV, it.b, it.ko, j, p.total_kv);
@@ -215,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           }
         }
        }
+       if (ok) meta_release(meta, k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       // drain: every copy this thread started has landed before the CTA can exit
@@ -231,8 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       const uint32_t sQ_addr = smem_u32(sQ), sR_addr = smem_u32(sRing);
       uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0}, tn = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-       const WorkItem wi = p.items[idx];
+      uint32_t k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+       if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
@@ -300,11 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         }
         ring_n = n0 + 2 * it.njt;
        }
+       if (ok) meta_release(meta, k);
       }
       if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
       umma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, nullptr, abort_flag))
+      raise_status(p.status, JFA_ERR_TIMEOUT);
   }
   } else {
     setmaxnreg_inc<kRegsCompute>();
@@ -319,8 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     uint32_t s_n = 0, o_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;  // records this warpgroup's trace
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-     const WorkItem wi = p.items[idx];
+    uint32_t k = 0;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+     if (!meta_wait_warp(meta, k, abort_flag)) { ok = false; break; }
+     const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
      for (int u = wi.u0; u < wi.u1 && ok; ++u) {
       const ItemInfo it = decode(p, wi, u);
       const int t = s ? it.t1 : it.t0;
@@ -484,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       tc_fence_before();
       if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 23);
      }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, k);
     }
     if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
   }

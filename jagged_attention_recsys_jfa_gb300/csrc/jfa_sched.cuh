@@ -1,0 +1,98 @@
+// Work-item metadata staged in shared memory.  One scheduler thread walks the CTA's
+// items (idx = blockIdx.x + k * gridDim.x) of the planner's longest-first list, loads
+// each item and its sequence's offsets from global memory, and publishes them into a
+// small ring; every role of the CTA (loaders, MMA issuer, compute warps) takes item k
+// from the ring.  The scheduler runs up to kMetaSlots items ahead, so the dependent
+// global loads (item, then offsets) are off the critical path at unit boundaries.
+#pragma once
+#include "jfa_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace jfa {
+
+constexpr int kMetaSlots = 4;
+// Arrivals that free an entry: the three single-thread roles of warpgroup 0 (streaming
+// producer, MMA issuer, resident-tile loader) and one per compute warp.
+constexpr int kMetaConsumers = 3 + (kThreads / 32 - kFirstComputeWarp);
+
+struct ItemMeta {
+  int b, h, u0, u1;   // the work item: sequence, head, unit range [u0, u1)
+  int64_t qo, ko;     // first query / key row of the sequence
+  int Lq, Lk;         // its lengths
+  int64_t qp;         // backward: first row of the sequence in the 128-row-padded vectors
+};
+
+struct MetaRing {
+  ItemMeta e[kMetaSlots];
+  uint64_t full[kMetaSlots], empty[kMetaSlots];
+};
+
+// One thread, before the CTA-wide barrier that publishes mbarrier initialisation.
+__device__ __forceinline__ void meta_init(MetaRing& r) {
+  for (int i = 0; i < kMetaSlots; ++i) {
+    mbar_init(&r.full[i], 1);
+    mbar_init(&r.empty[i], kMetaConsumers);
+  }
+}
+
+// Scheduler (one thread).  False when a bounded wait ran out (the CTA is aborting).
+__device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items, int n_items, const int64_t* q_off,
+                                             const int64_t* kv_off, const int64_t* qpad, volatile int* abort) {
+  uint32_t k = 0;
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++k) {
+    const WorkItem wi = items[idx];
+    ItemMeta m;
+    m.b = wi.b;
+    m.h = wi.h;
+    m.u0 = wi.u0;
+    m.u1 = wi.u1;
+    m.qo = q_off[wi.b];
+    m.ko = kv_off[wi.b];
+    m.Lq = int(q_off[wi.b + 1] - m.qo);
+    m.Lk = int(kv_off[wi.b + 1] - m.ko);
+    m.qp = qpad ? qpad[wi.b] : 0;
+    const uint32_t s = k % kMetaSlots;
+    if (!mbar_wait(&r.empty[s], ((k / kMetaSlots) & 1) ^ 1, abort, kWaitTimeoutNs)) return false;
+    r.e[s] = m;
+    mbar_arrive(&r.full[s]);  // release: the entry is visible to every thread that waits on it
+  }
+  return true;
+}
+
+// Entry k for a single-thread role, read in place for the item's duration and then
+// freed with meta_release.
+__device__ __forceinline__ bool meta_wait(MetaRing& r, uint32_t k, volatile int* abort) {
+  return mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, kWaitTimeoutNs);
+}
+__device__ __forceinline__ void meta_release(MetaRing& r, uint32_t k) { mbar_arrive(&r.empty[k % kMetaSlots]); }
+
+// Entry k for a whole warp (all 32 lanes call it), which reads the entry in place for
+// the item's duration and then frees it with meta_release_warp.  The lanes agree on the
+// outcome: a lane whose wait gave up has raised the abort flag, which ends the other
+// lanes' waits too.
+__device__ __forceinline__ bool meta_wait_warp(MetaRing& r, uint32_t k, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, kWaitTimeoutNs));
+}
+__device__ __forceinline__ void meta_release_warp(MetaRing& r, uint32_t k) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[k % kMetaSlots]);
+}
+
+// Tensor maps are acquired once per sequence by each thread that loads through them (and
+// an item ahead when possible, with their descriptors prefetched): an acquire makes the
+// next copy through the map wait for a fresh descriptor fetch.  `acq_b` is the sequence
+// whose maps of these two slots this thread holds.
+__device__ __forceinline__ void acquire_seq_maps(const CUtensorMap* maps, int b, int slot_a, int slot_b, int& acq_b,
+                                                 bool prefetch) {
+  if (b == acq_b) return;
+  const CUtensorMap* m = maps + size_t(b) * kNumMapSlots;
+  tmap_acquire(m + slot_a);
+  tmap_acquire(m + slot_b);
+  if (prefetch) {
+    tmap_prefetch(m + slot_a);
+    tmap_prefetch(m + slot_b);
+  }
+  acq_b = b;
+}
+
+}  // namespace jfa
