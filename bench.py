@@ -59,10 +59,26 @@ def valid_pairs(lq, lk, causal):
     return tot
 
 
+SHORT_Q = 128  # sequences with at most one query tile: backward in the fused pass
+
+
+def _split(batch):
+    short = np.asarray(batch.q_lengths) <= SHORT_Q
+    return short, ~short
+
+
 def workload_flops(batch):
-    P = valid_pairs(batch.q_lengths, batch.kv_lengths, batch.cfg.causal)
+    """Algorithmic flops: forward 4*d*H per visited pair; backward 10*d*H, of which the
+    split passes (sequences with more than one query tile) take 8 (dK/dV) and 2 (dQ) and
+    the fused pass (the others) all 10."""
+    lq, lk, causal = np.asarray(batch.q_lengths), np.asarray(batch.kv_lengths), batch.cfg.causal
+    short, long_ = _split(batch)
+    P = valid_pairs(lq, lk, causal)
+    Pl = valid_pairs(lq[long_], lk[long_], causal)
+    Ps = valid_pairs(lq[short], lk[short], causal)
     dH = batch.cfg.head_dim * batch.cfg.heads
-    return {"pairs": P, "fwd": 4.0 * dH * P, "bwd": 10.0 * dH * P, "dkdv": 8.0 * dH * P, "dq": 2.0 * dH * P}
+    return {"pairs": P, "fwd": 4.0 * dH * P, "bwd": 10.0 * dH * P, "dkdv": 8.0 * dH * Pl, "dq": 2.0 * dH * Pl,
+            "fused": 10.0 * dH * Ps}
 
 
 def workload_bytes(batch):
@@ -70,13 +86,19 @@ def workload_bytes(batch):
     output written once (the per-query lse / D vectors on 128-row-padded rows)."""
     H, d = batch.cfg.heads, batch.cfg.head_dim
     row = 2.0 * H * d
-    Tq, Tk = float(batch.q_lengths.sum()), float(batch.kv_lengths.sum())
-    qpad = float(((batch.q_lengths + 127) // 128 * 128).sum())
+    lq, lk = np.asarray(batch.q_lengths), np.asarray(batch.kv_lengths)
+    short, long_ = _split(batch)
+    Tq, Tk = float(lq.sum()), float(lk.sum())
+    qpad = float(((lq + 127) // 128 * 128).sum())
     vec = 8.0 * H * qpad  # lse*log2(e) and D, fp32
+    Tql, Tkl, Tqs, Tks = float(lq[long_].sum()), float(lk[long_].sum()), float(lq[short].sum()), float(lk[short].sum())
+    vecl = 8.0 * H * float(((lq[long_] + 127) // 128 * 128).sum())
+    vecs = vec - vecl
     return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq,
             "bwd_preprocess": 2 * Tq * row + 4.0 * H * Tq + vec,
-            "bwd_dkdv": (2 * Tq + 2 * Tk) * row + vec + 2 * Tk * row,
-            "bwd_dq": (2 * Tq + 2 * Tk) * row + vec + Tq * row}
+            "bwd_dkdv": (2 * Tql + 2 * Tkl) * row + vecl + 2 * Tkl * row,
+            "bwd_dq": (2 * Tql + 2 * Tkl) * row + vecl + Tql * row,
+            "bwd_fused": (2 * Tqs + 2 * Tks) * row + vecs + (Tqs + 2 * Tks) * row}
 
 
 def load_peaks():
@@ -377,7 +399,7 @@ def run_jfa(args, rank, world, device):
     # dominant kernel = largest share of the timed region's kernel time
     kinds = {k: v for k, v in per_kernel.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
-    algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"]}
+    algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"], "bwd_fused": fl["fused"]}
     algo_bytes = workload_bytes(batch)
     ms_dom, n_dom = kinds[dom]
     t_dom = ms_dom / n_dom / 1e3
@@ -385,7 +407,7 @@ def run_jfa(args, rank, world, device):
     # the binding roof: tensor when the kernel's algorithmic flops per byte reach the
     # ridge of the measured peaks, else HBM
     ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-    if dom in algo and algo[dom] / algo_bytes[dom] >= ridge:
+    if dom in algo and algo_bytes.get(dom, 0) > 0 and algo[dom] / algo_bytes[dom] >= ridge:
         achieved = algo[dom] / t_dom / 1e12
         peak = float(peaks["bf16_tflops"])
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
@@ -393,7 +415,7 @@ def run_jfa(args, rank, world, device):
                     "peak_source": f"{peak_src} bf16 dense (burst)",
                     "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
                     "flop_per_byte": round(algo[dom] / algo_bytes[dom], 1), "ridge": round(ridge, 1)}
-    elif dom in algo_bytes:
+    elif algo_bytes.get(dom, 0) > 0:
         achieved = algo_bytes[dom] / t_dom / 1e9
         peak = float(peaks["hbm_gbs"])
         roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,

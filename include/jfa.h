@@ -137,7 +137,7 @@ const char* jfa_last_error(void);
 
 /* Kernel kinds for per-kernel timing. */
 enum { JFA_KERNEL_PLAN = 0, JFA_KERNEL_FORWARD = 1, JFA_KERNEL_BWD_PREPROCESS = 2, JFA_KERNEL_BWD_DKDV = 3,
-       JFA_KERNEL_BWD_DQ = 4, JFA_NUM_KERNEL_KINDS = 5 };
+       JFA_KERNEL_BWD_DQ = 4, JFA_KERNEL_BWD_FUSED = 5, JFA_NUM_KERNEL_KINDS = 6 };
 
 /* Benchmark support (not part of the attention itself).  While enabled (process-wide),
  * every kernel launch is bracketed by two CUDA events recorded on the launch stream.

@@ -153,7 +153,7 @@ Problem make_problem(int B, int H, int d, int64_t total_q, int64_t total_kv, con
   p.num_buckets = has_bias ? bias->num_buckets : 0;
   p.center = has_bias ? bias->center : 0;
   std::lock_guard<std::mutex> g(g_trace_mu);
-  for (int k = 0; k < 5; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
+  for (int k = 0; k < JFA_NUM_KERNEL_KINDS; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
   return p;
 }
 
@@ -275,7 +275,11 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
     KernelTimer t(JFA_KERNEL_BWD_DQ, s);
     JFA_CHECK_LAUNCH(launch_bwd_dq(pr, lse, workspace, L, dq, nsm, s), "dQ launch");
   }
-  g_last_launches = 4;
+  {
+    KernelTimer t(JFA_KERNEL_BWD_FUSED, s);
+    JFA_CHECK_LAUNCH(launch_bwd_fused(pr, lse, workspace, L, dq, dk, dv, nsm, s), "fused short-query launch");
+  }
+  g_last_launches = 5;
   return JFA_OK;
 }
 

@@ -29,6 +29,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kRegsLoad = 104, kRegsCompute = 200;
 static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds the launch allocation");
+// the fused short-query pass: more issue state in warpgroup 0, lighter compute warps
+constexpr uint32_t kRegsLoadFused = 136, kRegsComputeFused = 184;
+static_assert(reg_split_fits(kRegsLoadFused, kRegsComputeFused), "register split exceeds the launch allocation");
 
 struct BwdParams {
   const int64_t* q_off;
@@ -47,8 +50,9 @@ struct BwdParams {
   const float* delta;   // [H][qpad_cap]  D, same layout
   const int64_t* qpad;  // [B+1] sequence offsets in the padded vectors
   int64_t qpad_cap;
-  __nv_bfloat16* g0;   // dK (dK/dV pass) or dQ (dQ pass)
-  __nv_bfloat16* g1;   // dV (dK/dV pass)
+  __nv_bfloat16* g0;   // dK (dK/dV and fused passes) or dQ (dQ pass)
+  __nv_bfloat16* g1;   // dV (dK/dV and fused passes)
+  __nv_bfloat16* g2;   // dQ (fused pass)
   TraceBuf trace;
 };
 
@@ -62,7 +66,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- preprocess
-// For every query tile of the dQ work list: D_i = sum_c dO_ic O_ic and lse_i * log2(e)
+// For every query tile of the dQ work list and of the fused list (whose sequences have
+// one query tile): D_i = sum_c dO_ic O_ic and lse_i * log2(e)
 // (+inf where lse = -inf, so exp2(s - lse) = 0 for a row that sees no key) into the
 // 128-row-padded per-query vectors, zeros on padding rows.  One warp per row, the lanes
 // across the head dimension (coalesced 2*d-byte rows).
@@ -70,8 +75,10 @@ struct PreParams {
   const int64_t* q_off;
   int H;
   int64_t total_q;
-  const WorkItem* items;
+  const WorkItem* items;    // dQ list: units are query tiles
   const int* n_items;
+  const WorkItem* items2;   // fused list: the sequence's one query tile
+  const int* n_items2;
   const int64_t* qpad;
   int64_t qpad_cap;
   const __nv_bfloat16* dout;
@@ -84,13 +91,15 @@ struct PreParams {
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = *p.n_items;
-  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
-    const WorkItem it = p.items[idx];
+  const int n1 = *p.n_items, n2 = *p.n_items2;
+  for (int idx = blockIdx.x; idx < n1 + n2; idx += gridDim.x) {
+    const bool fused = idx >= n1;
+    const WorkItem it = fused ? p.items2[idx - n1] : p.items[idx];
     const int64_t qo = p.q_off[it.b];
     const int Lq = int(p.q_off[it.b + 1] - qo);
     const int64_t pad0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
-    for (int t = it.u0; t < it.u1; ++t) {
+    const int t_lo = fused ? 0 : it.u0, t_hi = fused ? (Lq > 0 ? 1 : 0) : it.u1;
+    for (int t = t_lo; t < t_hi; ++t) {
       // 8 warps x 16 rows.  A row of one head is D/8 16-byte chunks: a warp covers
       // 32 / (D/8) rows per load, and all of its 16 rows' loads are in flight at once.
       constexpr int kLanesPerRow = D / 8, kRowsPerLoad = 32 / kLanesPerRow, kLoads = 16 / kRowsPerLoad;
@@ -143,7 +152,12 @@ struct BwdCfg {
   static constexpr uint32_t kColP1 = 256, kColDQ = 384;
   static constexpr int kSmemDkdv = 2 * kTileBytes + kRingDkdv * kTileBytes + kVecSlots * 1024 + 1024;
   static constexpr int kSmemDq = 2 * kTileBytes + kRingDq * kTileBytes + 1024;
-  static_assert(kSmemDkdv <= 232448 && kSmemDq <= 232448, "shared memory per CTA");
+  // Fused short-query pass: Q and dO resident, K/V ring, dS^T staging (keys x 128 queries,
+  // bf16), lse2 / D vectors.  TMEM: S^T [0,128), dP^T then dK [128,256), dV, dQ.
+  static constexpr int kRingFused = D == 128 ? 3 : 8;
+  static constexpr uint32_t kColFdV = 256, kColFdQ = 256 + D;
+  static constexpr int kSmemFused = 2 * kTileBytes + kRingFused * kTileBytes + 32768 + 1024 + 1024;
+  static_assert(kSmemDkdv <= 232448 && kSmemDq <= 232448 && kSmemFused + 1024 <= 232448, "shared memory per CTA");
 };
 
 // Load one row-tile (128 rows x D columns, D/64 boxes of 16 KB) through a tensor map.
@@ -982,7 +996,395 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLayout& L, bool dq_pass) {
+// ================================================================== fused short-query pass
+// For sequences whose queries fit one 128-row tile ("Four generations" item 2 splits the
+// backward to avoid atomics; with a single query tile one CTA per (sequence, head) can
+// own dQ outright): Q, dO and the tile's lse2 / D vectors stay resident while the key
+// tiles stream once.  Per visible key tile j:
+//   S^T = K_j Q^T, dP^T = V_j dO^T                  (SS, fp32 in TMEM)
+//   P^T, dS^T = P^T o (dP^T - D) by the warpgroups   (P^T -> TMEM, dS^T -> shared memory)
+//   dV_j = P^T dO (TS), dK_j = dS^T Q (SS)          (one query tile: stored directly)
+//   dQ += dS K_j (SS, dS^T read as an MN-major A)   (accumulated in TMEM, stored at the end)
+// so K and V are read once instead of once per pass, still without atomics.  Key tiles
+// the query tile cannot see (causal) get zero dK / dV rows and no MMAs.
+template <int D, bool kBias>
+__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int R = C::kRingFused;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::kTileBytes;
+  uint8_t* sRing = smem + 2 * C::kTileBytes;                 // K_j, V_j single tiles
+  uint8_t* sDS = sRing + R * C::kTileBytes;                  // dS^T: [keys][queries], two 64-query atoms
+  float* sVec = reinterpret_cast<float*>(sDS + 32768);       // lse2[128], D[128] of the query tile
+
+  __shared__ uint64_t q_full, q_empty, st_full, dpt_full, p_full, ds_full, dv_full, dv_empty, dk_full, dk_empty;
+  __shared__ uint64_t dsm_empty, dq_full, dq_empty, mma_done;
+  __shared__ uint64_t ring_full[R], ring_empty[R];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ MetaRing meta;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
+    mbar_init(&st_full, 1);
+    mbar_init(&dpt_full, 1);
+    mbar_init(&p_full, 256);
+    mbar_init(&ds_full, 256);
+    mbar_init(&dv_full, 1);
+    mbar_init(&dv_empty, 256);
+    mbar_init(&dk_full, 1);
+    mbar_init(&dk_empty, 256);
+    mbar_init(&dsm_empty, 1);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_empty, 256);
+    mbar_init(&mma_done, 1);
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
+    }
+    meta_init(meta);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n_items = *p.n_items;
+  volatile int* abort_flag = &abort_sh;
+  const bool causal = p.causal != 0;
+  // key tile kt of a sequence is visible to its (single) query tile
+  auto visible = [&](int kt, int Lq, int Lk) {
+    int first, count;
+    q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+    return count > 0;
+  };
+  auto any_visible = [&](int u0, int u1, int Lq, int Lk) {
+    for (int kt = u0; kt < u1; ++kt)
+      if (visible(kt, Lq, Lk)) return true;
+    return false;
+  };
+
+  if (warp < kFirstComputeWarp) {
+   setmaxnreg_dec<kRegsLoadFused>();
+   if (warp == 2) {
+    // ------------------------------------------------------------ Q / dO / vector loader
+    if (lane == 0) {
+      uint32_t item_n = 0, tn = 0;
+      int acq_b = -1;
+      bool ok = true;
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+        const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+        if (any_visible(wi.u0, wi.u1, wi.Lq, wi.Lk)) {
+          acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
+          const TileMap mq = tile_map(p.maps, p.B, kMapQ, wi.b, wi.qo, 0, p.total_q);
+          const TileMap mdo = tile_map(p.maps, p.B, kMapDO, wi.b, wi.qo, 0, p.total_q);
+          if (mq.tail) {
+            tmap_acquire(mq.map);
+            tmap_acquire(mdo.map);
+          }
+          const float* l2src = p.lse2 + int64_t(wi.h) * p.qpad_cap + wi.qp;
+          const float* dsrc = p.delta + int64_t(wi.h) * p.qpad_cap + wi.qp;
+          if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+          trace_event(p.trace, kTraceLoader, tn, 1);
+          mbar_arrive_expect_tx(&q_full, 2 * C::kTileBytes + 2 * kBM * 4);
+          load_tile<D>(sQ, mq.map, &q_full, wi.h * D, mq.y);
+          load_tile<D>(sDO, mdo.map, &q_full, wi.h * D, mdo.y);
+          bulk_load(sVec, l2src, kBM * 4, &q_full);
+          bulk_load(sVec + kBM, dsrc, kBM * 4, &q_full);
+          ++item_n;
+        }
+        meta_release(meta, item_k);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      if (item_n > 0) drain_wait(&q_full, (item_n - 1) & 1);
+    }
+   } else if (warp == 0) {
+    // ------------------------------------------------------------ K / V ring producer
+    if (lane == 0) {
+      uint32_t ring_n = 0, tn = 0;
+      int acq_b = -1;
+      bool ok = true;
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+        const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+          if (!visible(kt, wi.Lq, wi.Lk)) continue;
+          acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const TileMap m = tile_map(p.maps, p.B, kv ? kMapV : kMapK, wi.b, wi.ko, kt, p.total_kv);
+            if (m.tail) tmap_acquire(m.map);
+            const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
+            if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+            trace_event(p.trace, kTraceProducer, tn, 2);
+            mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
+            load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], wi.h * D, m.y);
+            ++ring_n;
+          }
+        }
+        if (ok) meta_release(meta, item_k);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
+      for (uint32_t n = f; n < ring_n; ++n) drain_wait(&ring_full[n % R], (n / R) & 1);
+    }
+   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);  // A K-major, B MN-major
+      constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, true, true);    // A (dS) and B (K) MN-major
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aR = smem_u32(sRing), aDS = smem_u32(sDS);
+      uint32_t ring_n = 0, item_n = 0, g = 0, tn = 0;
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto ra = [&](uint32_t n) { return aR + (n % R) * C::kTileBytes; };
+      // D(128 x 128) = A(128 x D) * B(128 x D)^T, both K-major (S^T, dP^T)
+      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
+        const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
+        }
+      };
+      uint32_t item_k = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+       if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+       const int Lq = wi.Lq, Lk = wi.Lk;
+       if (any_visible(wi.u0, wi.u1, Lq, Lk)) {
+        if (!wait(&q_full, item_n & 1)) { ok = false; break; }
+        if (!wait(&dq_empty, (item_n & 1) ^ 1)) { ok = false; break; }
+        trace_event(p.trace, kTraceMma, tn, 10);
+        bool first = true;
+        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+          if (!visible(kt, Lq, Lk)) continue;
+          const uint32_t nk = ring_n, nv = ring_n + 1;
+          ring_n += 2;
+          // S^T = K Q^T
+          if (!wait(&ring_full[nk % R], (nk / R) & 1)) { ok = false; break; }
+          mma_nt(C::kColS, ra(nk), aQ);
+          umma_commit(&st_full);
+          // dP^T = V dO^T, into the columns dK of the previous tile is read from
+          if (!wait(&dk_empty, (g & 1) ^ 1) || !wait(&ring_full[nv % R], (nv / R) & 1)) { ok = false; break; }
+          mma_nt(C::kColP, ra(nv), aDO);
+          umma_commit(&dpt_full);
+          umma_commit(&ring_empty[nv % R]);  // V is read by dP^T only
+          // dV = P^T dO  (P^T from TMEM: each warpgroup's 64 queries in its own S half)
+          if (!wait(&p_full, g & 1) || !wait(&dv_empty, (g & 1) ^ 1)) { ok = false; break; }
+          {
+            const uint64_t bd = sdesc_sw128(aDO, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBM / 16; ++kk)
+              umma_ts(tmem + C::kColFdV, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                      bd + uint32_t(kk * 2048 >> 4), kIdAcc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&dv_full);
+          trace_event(p.trace, kTraceMma, tn, 11);
+          // dK = dS^T Q (dS^T staged in shared memory, K-major over queries), into the
+          // dP^T columns; then dQ += dS K (the same staging read as an MN-major A)
+          if (!wait(&ds_full, g & 1)) { ok = false; break; }
+          {
+            const uint64_t ad = sdesc_sw128(aDS, 16, 1024), bd = sdesc_sw128(aQ, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBM / 16; ++kk) {
+              const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              umma_ss(tmem + C::kColP, ad + o, bd + uint32_t(kk * 2048 >> 4), kIdAcc, kk > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&dk_full);
+          {
+            const uint64_t ad = sdesc_sw128(aDS, 16384, 1024), bd = sdesc_sw128(ra(nk), 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ss(tmem + C::kColFdQ, ad + uint32_t(kk * 2048 >> 4), bd + uint32_t(kk * 2048 >> 4), kIdDq,
+                      (!first || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&dsm_empty);
+          trace_event(p.trace, kTraceMma, tn, 12);
+          umma_commit(&ring_empty[nk % R]);  // K is read by S^T and dQ
+          first = false;
+          ++g;
+        }
+        if (!ok) break;
+        umma_commit(&dq_full);
+        umma_commit(&q_empty);
+        ++item_n;
+       }
+       meta_release(meta, item_k);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      umma_commit(&mma_done);
+      drain_wait(&mma_done, 0);
+    }
+   } else if (warp == 3) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
+      raise_status(p.status, JFA_ERR_TIMEOUT);
+   }
+  } else {
+    setmaxnreg_inc<kRegsComputeFused>();
+    // ------------------------------------------------------------ compute warpgroups
+    const int w = (warp - kFirstComputeWarp) >> 2;  // queries [64w, 64w+64)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row of S^T / dP^T / dV / dK; query row of dQ
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
+    const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
+    const float sl2 = p.scale_log2;
+    const float* lse2v = sVec + 64 * w;
+    const float* dvec = sVec + kBM + 64 * w;
+    uint32_t g = 0, item_n = 0, tn = 0;
+    const bool leader = (warp & 3) == 0 && lane == 0;
+    bool ok = true;
+    uint32_t item_k = 0;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];
+     const int Lq = it.Lq, Lk = it.Lk;
+     const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
+     const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
+     const bool live = any_visible(it.u0, it.u1, Lq, Lk);
+     if (live && !__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs))) {
+       ok = false;
+       break;
+     }
+     for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
+      const int j = kt * kBN + row;  // local key index
+      const bool valid = j < Lk;
+      __nv_bfloat16* dk_row = p.g0 + ((it.ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
+      __nv_bfloat16* dv_row = p.g1 + ((it.ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
+      if (!visible(kt, Lq, Lk)) {
+        store_acc_row(0, D / 2, 0.f, dk_row, valid, true);
+        store_acc_row(0, D / 2, 0.f, dv_row, valid, true);
+        continue;
+      }
+      // ---- P^T = exp2(S^T * scale * log2e (+ bias) - lse2), 0 on padding and hidden pairs
+      if (!mbar_wait(&st_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
+      float x[64];
+      ld_cols64(tS, x);
+      const int i0 = 64 * w;  // query of column 0 of this half
+      if (kBias) {
+        const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] -= lse2v[c];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, -lse2v[c]);
+      }
+      {
+        // hidden: padded keys (whole row), padded queries, and i < j - diag when causal
+        const int lim_q = Lq - i0;                       // columns c >= lim_q are padding
+        const int lim_c = causal ? j - diag - i0 : -1;   // columns c < lim_c are hidden
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!valid || c >= lim_q || c < lim_c) x[c] = -INFINITY;
+      }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);
+      st_bf16_64(tS, x);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+      // ---- dS^T = P^T o (dP^T - D) -> shared memory (keys x queries, 128-byte swizzle)
+      if (!mbar_wait(&dpt_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      {
+        uint8_t* drow = sDS + w * 16384 + row * 128;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time
+          uint32_t r[32];
+          tmem_ld32(tP + 32 * hf, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float d8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int c = 32 * hf + 8 * ch + e;
+              d8[e] = x[c] * (__uint_as_float(r[8 * ch + e]) - dvec[c]);
+            }
+            uint4 v;
+            v.x = pack_bf16x2(d8[0], d8[1]);
+            v.y = pack_bf16x2(d8[2], d8[3]);
+            v.z = pack_bf16x2(d8[4], d8[5]);
+            v.w = pack_bf16x2(d8[6], d8[7]);
+            const int chunk = 4 * hf + ch;
+            *reinterpret_cast<uint4*>(drow + ((chunk ^ (row & 7)) << 4)) = v;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the MMAs read the staging through the async proxy
+      tc_fence_before();
+      mbar_arrive(&ds_full);
+      // ---- dV_j and dK_j rows
+      if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      store_acc_row(tmem + lane_addr + C::kColFdV + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
+      tc_fence_before();
+      mbar_arrive(&dv_empty);
+      if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      store_acc_row(tmem + lane_addr + C::kColP + w * (D / 2), D / 2, p.scale, dk_row, valid, false);
+      tc_fence_before();
+      mbar_arrive(&dk_empty);
+      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
+      ++g;
+     }
+     if (!ok) break;
+     // ---- dQ rows (TMEM lane = query): zeros when the query tile sees no key
+     {
+      const int i = row;
+      const bool qvalid = i < Lq;
+      __nv_bfloat16* dq_row = p.g2 + ((it.qo + i) * p.H + it.h) * int64_t(D) + w * (D / 2);
+      if (live) {
+        if (!mbar_wait(&dq_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        store_acc_row(tmem + lane_addr + C::kColFdQ + w * (D / 2), D / 2, p.scale, dq_row, qvalid, false);
+        tc_fence_before();
+        mbar_arrive(&dq_empty);
+        ++item_n;
+      } else {
+        store_acc_row(0, D / 2, 0.f, dq_row, qvalid, true);
+      }
+     }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+enum BwdPass { kPassDkdv = 0, kPassDq = 1, kPassFused = 2 };
+
+BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLayout& L, int pass) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   BwdParams bp;
   bp.q_off = pr.q_off;
@@ -998,9 +1400,9 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.num_buckets = pr.num_buckets;
   bp.center = pr.center;
   bp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
-  bp.items = reinterpret_cast<const WorkItem*>(w + (dq_pass ? L.dq : L.dkv));
+  bp.items = reinterpret_cast<const WorkItem*>(w + (pass == kPassDq ? L.dq : pass == kPassFused ? L.fused : L.dkv));
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);
-  bp.n_items = dq_pass ? &hdr->n_dq : &hdr->n_dkv;
+  bp.n_items = pass == kPassDq ? &hdr->n_dq : pass == kPassFused ? &hdr->n_fused : &hdr->n_dkv;
   bp.status = &reinterpret_cast<WsHeader*>(w)->status;
   (void)lse;
   bp.lse2 = reinterpret_cast<const float*>(w + L.lse2);
@@ -1009,7 +1411,8 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.qpad_cap = L.qpad_cap;
   bp.g0 = nullptr;
   bp.g1 = nullptr;
-  bp.trace = pr.trace[dq_pass ? JFA_KERNEL_BWD_DQ : JFA_KERNEL_BWD_DKDV];
+  bp.g2 = nullptr;
+  bp.trace = pr.trace[pass == kPassDq ? JFA_KERNEL_BWD_DQ : pass == kPassFused ? JFA_KERNEL_BWD_FUSED : JFA_KERNEL_BWD_DKDV];
   return bp;
 }
 
@@ -1034,6 +1437,8 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   pp.total_q = pr.total_q;
   pp.items = reinterpret_cast<const WorkItem*>(w + L.dq);
   pp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_dq;
+  pp.items2 = reinterpret_cast<const WorkItem*>(w + L.fused);
+  pp.n_items2 = &reinterpret_cast<const WsHeader*>(w)->n_fused;
   pp.qpad = reinterpret_cast<const int64_t*>(w + L.qpad);
   pp.qpad_cap = L.qpad_cap;
   pp.dout = static_cast<const __nv_bfloat16*>(dout);
@@ -1050,7 +1455,7 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
 
 cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dk, void* dv,
                             int num_sms, cudaStream_t stream) {
-  BwdParams bp = make_params(pr, lse, ws, L, false);
+  BwdParams bp = make_params(pr, lse, ws, L, kPassDkdv);
   bp.g0 = static_cast<__nv_bfloat16*>(dk);
   bp.g1 = static_cast<__nv_bfloat16*>(dv);
   const bool bias = pr.bias_table != nullptr;
@@ -1061,9 +1466,23 @@ cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const
               : launch_big(dkdv_kernel<64, false>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream);
 }
 
+cudaError_t launch_bwd_fused(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,
+                             void* dv, int num_sms, cudaStream_t stream) {
+  BwdParams bp = make_params(pr, lse, ws, L, kPassFused);
+  bp.g0 = static_cast<__nv_bfloat16*>(dk);
+  bp.g1 = static_cast<__nv_bfloat16*>(dv);
+  bp.g2 = static_cast<__nv_bfloat16*>(dq);
+  const bool bias = pr.bias_table != nullptr;
+  if (pr.d == 128)
+    return bias ? launch_big(fused_kernel<128, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
+                : launch_big(fused_kernel<128, false>, BwdCfg<128>::kSmemFused, num_sms, bp, stream);
+  return bias ? launch_big(fused_kernel<64, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
+              : launch_big(fused_kernel<64, false>, BwdCfg<64>::kSmemFused, num_sms, bp, stream);
+}
+
 cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, int num_sms,
                           cudaStream_t stream) {
-  BwdParams bp = make_params(pr, lse, ws, L, true);
+  BwdParams bp = make_params(pr, lse, ws, L, kPassDq);
   bp.g0 = static_cast<__nv_bfloat16*>(dq);
   const bool bias = pr.bias_table != nullptr;
   if (pr.d == 128)

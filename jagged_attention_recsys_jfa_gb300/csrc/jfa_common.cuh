@@ -86,7 +86,8 @@ struct WsHeader {
   int n_dq;        // number of dQ items
   int n_dkv;       // number of dK/dV items
   int64_t total_qpad;  // sum_b round_up(Lq_b, 128): rows of the padded per-query vectors
-  int pad[58];
+  int n_fused;     // number of fused short-query backward items
+  int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -97,12 +98,13 @@ struct WsLayout {
   size_t fwd = 0;      // WorkItem[cap_fwd]
   size_t dq = 0;       // WorkItem[cap_dq]
   size_t dkv = 0;      // WorkItem[cap_dkv]
+  size_t fused = 0;    // WorkItem[cap_fused]  backward: sequences whose queries fit one tile
   size_t bias2 = 0;    // float[H][num_buckets]  bias table pre-multiplied by log2(e)
   size_t qpad = 0;     // int64[B+1]  backward: offsets of each sequence in the padded vectors
   size_t lse2 = 0;     // float[H][qpad_cap]  backward: lse * log2(e) (+inf if -inf), 0 on padding
   size_t delta = 0;    // float[H][qpad_cap]  backward: D_i = rowsum(dO * O), 0 on padding
   size_t total = 0;
-  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0, qpad_cap = 0;
+  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0, cap_fused = 0, qpad_cap = 0;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -130,6 +132,9 @@ __host__ __device__ inline WsLayout make_layout(int B, int H, int d, int64_t tot
     L.cap_dkv = int64_t(H) * (total_kv / 128 + B + 1);
     L.dkv = align_up(off, 16);
     off = L.dkv + size_t(L.cap_dkv) * sizeof(WorkItem);
+    L.cap_fused = int64_t(H) * (B + 1);
+    L.fused = align_up(off, 16);
+    off = L.fused + size_t(L.cap_fused) * sizeof(WorkItem);
     L.qpad = align_up(off, 256);
     off = L.qpad + size_t(B + 1) * sizeof(int64_t);
     L.qpad_cap = int64_t(align_up(size_t(total_q) + size_t(kBM) * B, kBM));  // rows per head, 512-B aligned

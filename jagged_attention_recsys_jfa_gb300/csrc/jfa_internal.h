@@ -16,7 +16,7 @@ struct Problem {
   int causal;
   const float* bias_table;  // nullptr = no bias
   int num_buckets, center;
-  TraceBuf trace[5];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
+  TraceBuf trace[JFA_NUM_KERNEL_KINDS];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
 };
 
 struct PlanMaps {
@@ -58,5 +58,8 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const float* lse, void* ws, const 
                             void* dv, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dq,
                           int num_sms, cudaStream_t stream);
+// Sequences whose queries fit one tile: dQ, dK and dV in one pass over K and V.
+cudaError_t launch_bwd_fused(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,
+                             void* dv, int num_sms, cudaStream_t stream);
 
 }  // namespace jfa

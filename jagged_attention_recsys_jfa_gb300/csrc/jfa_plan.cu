@@ -24,16 +24,22 @@ struct PlanParams {
   int nb;
 };
 
-enum ListKind { kListFwd = 0, kListDq = 1, kListDkv = 2 };
+enum ListKind { kListFwd = 0, kListDq = 1, kListDkv = 2, kListFused = 3 };
 
+// Backward: a sequence whose queries fit one tile (Lq <= 128) is done by the fused pass
+// (one CTA per sequence and head, every key tile once); the others by the split
+// dK/dV and dQ passes.
 __device__ __forceinline__ int list_units(int kind, int Lq, int Lk) {
   const int nq = (Lq + kBM - 1) / kBM;
+  const int nk = (Lk + kBN - 1) / kBN;
   if (kind == kListFwd) return (nq + 1) / 2;
-  if (kind == kListDq) return nq;
-  return (Lk + kBN - 1) / kBN;
+  if (kind == kListFused) return Lq <= kBM ? (nk > 0 ? nk : (Lq > 0 ? 1 : 0)) : 0;
+  if (Lq <= kBM) return 0;
+  return kind == kListDq ? nq : nk;
 }
 
 __device__ __forceinline__ int unit_cost(int kind, int u, int Lq, int Lk, bool causal) {
+  if (kind == kListFused) return 1;  // a key tile (its dK / dV rows are stored even when unseen)
   if (kind == kListFwd)
     return kv_tiles_for_q_tile(2 * u, Lq, Lk, causal) + kv_tiles_for_q_tile(2 * u + 1, Lq, Lk, causal);
   if (kind == kListDq) return kv_tiles_for_q_tile(u, Lq, Lk, causal);
@@ -122,7 +128,8 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
   block_scan_incl(local, &total_cost);
   const long long share = (total_cost * p.H + (long long)kItemsPerCta * p.grid - 1) /
                           ((long long)kItemsPerCta * p.grid);
-  const long long range_cap = share > 1 ? share : 1;
+  // the fused pass owns each sequence's dQ tile: its items are never cut into ranges
+  const long long range_cap = kind == kListFused ? (1ll << 62) : (share > 1 ? share : 1);
 
   for (int c = tid; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
   __syncthreads();
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   if (bad) {
     if (tid == 0) {
       atomicCAS(&hdr->status, 0, int(JFA_ERR_BAD_OFFSETS));
-      hdr->n_fwd = hdr->n_dq = hdr->n_dkv = 0;
+      hdr->n_fwd = hdr->n_dq = hdr->n_dkv = hdr->n_fused = 0;
     }
     return;
   }
@@ -261,6 +268,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     emit_list(p, kListDkv, reinterpret_cast<WorkItem*>(p.ws + p.L.dkv), p.L.cap_dkv, &hdr->n_dkv, hist,
               base);
     emit_list(p, kListDq, reinterpret_cast<WorkItem*>(p.ws + p.L.dq), p.L.cap_dq, &hdr->n_dq, hist, base);
+    emit_list(p, kListFused, reinterpret_cast<WorkItem*>(p.ws + p.L.fused), p.L.cap_fused, &hdr->n_fused, hist,
+              base);
   }
 }
 

@@ -30,9 +30,10 @@ def test_bounded_wait_times_out_and_reports():
     compare_out_lse(res["out"], res["lse"], ref["out"], ref["lse"], "after timeout")
 
 
-@pytest.mark.parametrize("kind", ["forward", "bwd_dkdv", "bwd_dq"])
+@pytest.mark.parametrize("kind", ["forward", "bwd_dkdv", "bwd_dq", "bwd_fused"])
 def test_trace_records_ordered_events(kind):
-    batch = make_batch(CONFIGS["tiny"], device="cuda")
+    # one sequence with several query tiles (split backward passes), two with one (fused)
+    batch = make_batch(CONFIGS["tiny"], device="cuda", q_lengths=[300, 40, 7], kv_lengths=[300, 260, 9])
     buf = torch.zeros(5 * 1024, dtype=torch.int64, device="cuda")
     jfa_trace_configure(buf, kind)
     try:
