@@ -1182,11 +1182,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
           if (!wait(&ring_full[nk % R], (nk / R) & 1)) { ok = false; break; }
           mma_nt(C::kColS, ra(nk), aQ);
           umma_commit(&st_full);
+          trace_event(p.trace, kTraceMma, tn, 13);
           // dP^T = V dO^T, into the columns dK of the previous tile is read from
           if (!wait(&dk_empty, (g & 1) ^ 1) || !wait(&ring_full[nv % R], (nv / R) & 1)) { ok = false; break; }
           mma_nt(C::kColP, ra(nv), aDO);
           umma_commit(&dpt_full);
           umma_commit(&ring_empty[nv % R]);  // V is read by dP^T only
+          trace_event(p.trace, kTraceMma, tn, 14);
           // dV = P^T dO  (P^T from TMEM: each warpgroup's 64 queries in its own S half)
           if (!wait(&p_full, g & 1) || !wait(&dv_empty, (g & 1) ^ 1)) { ok = false; break; }
           {
@@ -1308,6 +1310,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full);
+      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
       // ---- dS^T = P^T o (dP^T - D) -> shared memory (keys x queries, 128-byte swizzle)
       if (!mbar_wait(&dpt_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
@@ -1340,12 +1343,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       fence_proxy_async_smem();  // the MMAs read the staging through the async proxy
       tc_fence_before();
       mbar_arrive(&ds_full);
+      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
       // ---- dV_j and dK_j rows
       if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       store_acc_row(tmem + lane_addr + C::kColFdV + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
       tc_fence_before();
       mbar_arrive(&dv_empty);
+      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       store_acc_row(tmem + lane_addr + C::kColP + w * (D / 2), D / 2, p.scale, dk_row, valid, false);
