@@ -180,19 +180,77 @@ __device__ void write_qpad(const PlanParams& p) {
   }
 }
 
+// The first CTAs validate the offsets and write one work list each (block-wide scans: the
+// forward list, or the dK/dV (with the padded query offsets), dQ and fused lists); the
+// other CTAs write the bias table, the tail copies and the tensor maps in parallel.
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanMaps maps, PlanParams p) {
   __shared__ int hist[kCostBuckets];
   __shared__ int base[kCostBuckets];
   const int tid = threadIdx.x;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
 
-  // ---- bias table pre-scaled to log2 units (the kernels work with exp2)
-  if (p.bias) {
-    float* b2 = reinterpret_cast<float*>(p.ws + p.L.bias2);
-    for (int i = tid; i < p.H * p.nb; i += blockDim.x) b2[i] = p.bias[i] * 1.4426950408889634f;
+  const int list_ctas = p.backward ? 3 : 1;
+  if (int(blockIdx.x) >= list_ctas) {
+    const size_t gt = size_t(blockIdx.x - list_ctas) * blockDim.x + tid;
+    const size_t gstride = size_t(gridDim.x - list_ctas) * blockDim.x;
+    // ---- bias table pre-scaled to log2 units (the kernels work with exp2)
+    if (p.bias) {
+      float* b2 = reinterpret_cast<float*>(p.ws + p.L.bias2);
+      for (size_t i = gt; i < size_t(p.H) * p.nb; i += gstride) b2[i] = p.bias[i] * 1.4426950408889634f;
+    }
+    // ---- tail copies: the last min(128, total) rows of each tensor, which the boxes that
+    //      would otherwise read past the tensor's last row load from instead
+    const size_t rb = p.L.row_bytes;
+    for (int slot = 0; slot < kNumMapSlots; ++slot) {
+      if (!maps.used[slot]) continue;
+      const int64_t total = (slot == kMapQ || slot == kMapDO) ? p.total_q : p.total_kv;
+      if (total <= 0) continue;
+      const int64_t n = total < kBM ? total : kBM;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(maps.base[slot]) +
+                                                        size_t(total - n) * rb);
+      uint4* dst = reinterpret_cast<uint4*>(p.ws + p.L.tail + size_t(slot) * kTailRows * rb);
+      const size_t nvec = size_t(n) * rb / 16;
+      for (size_t i = gt; i < nvec; i += gstride) dst[i] = src[i];
+    }
+    // ---- per-sequence tensor maps: copy the template, point it at the sequence's first
+    //      row and clip its row extent to the sequence length.  A sequence whose last tile
+    //      would reach past the tensor's last row also gets a tail map over the tail copy,
+    //      pointed at that tile's first row and clipped to the tile's rows.  (With invalid
+    //      offsets CTA 0 leaves every list empty, so no map is used; a tail map is only
+    //      written for a sequence inside its tensor, which keeps its index in range.)
+    CUtensorMap* out_maps = reinterpret_cast<CUtensorMap*>(p.ws + p.L.maps);
+    for (size_t idx = gt; idx < size_t(p.B) * kNumMapSlots; idx += gstride) {
+      const int b = int(idx / kNumMapSlots), slot = int(idx % kNumMapSlots);
+      if (!maps.used[slot]) continue;
+      const bool is_q_side = (slot == kMapQ || slot == kMapDO);
+      const int64_t row0 = is_q_side ? p.q_off[b] : p.kv_off[b];
+      const int64_t len = (is_q_side ? p.q_off[b + 1] : p.kv_off[b + 1]) - row0;
+      const uint4* src = reinterpret_cast<const uint4*>(&maps.tmpl[slot]);
+      CUtensorMap* dst = out_maps + idx;
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d4[i] = src[i];
+      tmap_replace_address(dst, static_cast<const uint8_t*>(maps.base[slot]) + row0 * int64_t(rb));
+      tmap_replace_dim1(dst, uint32_t(len > 0 ? len : 1));
+      const int64_t total = is_q_side ? p.total_q : p.total_kv;
+      if (len <= 0 || row0 < 0 || row0 + len > total) continue;
+      const int64_t g0 = row0 + (len - 1) / kBM * kBM;  // first row of the sequence's last tile
+      if (g0 + kBM > total) {
+        const int64_t n = total < kBM ? total : kBM;  // rows in the tail copy; it starts at row total - n
+        CUtensorMap* tdst =
+            out_maps + size_t(p.B) * kNumMapSlots + size_t(slot) * kTailMaps + size_t(g0 + kBM - total);
+        uint4* t4 = reinterpret_cast<uint4*>(tdst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t4[i] = src[i];
+        tmap_replace_address(tdst, p.ws + p.L.tail + size_t(slot) * kTailRows * rb + size_t(g0 - (total - n)) * rb);
+        tmap_replace_dim1(tdst, uint32_t(row0 + len - g0));
+      }
+    }
+    tmap_release();
+    return;
   }
 
-  // ---- validate offsets
+  // ---- list CTAs: validate offsets (each list CTA on its own, so all agree)
   int bad = 0;
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int64_t lq = p.q_off[b + 1] - p.q_off[b];
@@ -212,62 +270,16 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     return;
   }
 
-  // ---- tail copies: the last min(128, total) rows of each tensor, which the boxes that
-  //      would otherwise read past the tensor's last row load from instead
-  const size_t rb = p.L.row_bytes;
-  for (int slot = 0; slot < kNumMapSlots; ++slot) {
-    if (!maps.used[slot]) continue;
-    const int64_t total = (slot == kMapQ || slot == kMapDO) ? p.total_q : p.total_kv;
-    if (total <= 0) continue;
-    const int64_t n = total < kBM ? total : kBM;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(maps.base[slot]) +
-                                                      size_t(total - n) * rb);
-    uint4* dst = reinterpret_cast<uint4*>(p.ws + p.L.tail + size_t(slot) * kTailRows * rb);
-    const size_t nvec = size_t(n) * rb / 16;
-    for (size_t i = tid; i < nvec; i += blockDim.x) dst[i] = src[i];
-  }
-
-  // ---- per-sequence tensor maps: copy the template, point it at the sequence's first
-  //      row and clip its row extent to the sequence length.  A sequence whose last tile
-  //      would reach past the tensor's last row also gets a tail map over the tail copy,
-  //      pointed at that tile's first row and clipped to the tile's rows.
-  CUtensorMap* out_maps = reinterpret_cast<CUtensorMap*>(p.ws + p.L.maps);
-  for (int idx = tid; idx < p.B * kNumMapSlots; idx += blockDim.x) {
-    const int b = idx / kNumMapSlots, slot = idx % kNumMapSlots;
-    if (!maps.used[slot]) continue;
-    const bool is_q_side = (slot == kMapQ || slot == kMapDO);
-    const int64_t row0 = is_q_side ? p.q_off[b] : p.kv_off[b];
-    const int64_t len = (is_q_side ? p.q_off[b + 1] : p.kv_off[b + 1]) - row0;
-    const uint4* src = reinterpret_cast<const uint4*>(&maps.tmpl[slot]);
-    CUtensorMap* dst = out_maps + idx;
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d4[i] = src[i];
-    tmap_replace_address(dst, static_cast<const uint8_t*>(maps.base[slot]) + row0 * int64_t(rb));
-    tmap_replace_dim1(dst, uint32_t(len > 0 ? len : 1));
-    if (len <= 0) continue;
-    const int64_t total = is_q_side ? p.total_q : p.total_kv;
-    const int64_t g0 = row0 + (len - 1) / kBM * kBM;  // first row of the sequence's last tile
-    if (g0 + kBM > total) {
-      const int64_t n = total < kBM ? total : kBM;  // rows in the tail copy; it starts at row total - n
-      CUtensorMap* tdst = out_maps + size_t(p.B) * kNumMapSlots + size_t(slot) * kTailMaps + size_t(g0 + kBM - total);
-      uint4* t4 = reinterpret_cast<uint4*>(tdst);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) t4[i] = src[i];
-      tmap_replace_address(tdst, p.ws + p.L.tail + size_t(slot) * kTailRows * rb + size_t(g0 - (total - n)) * rb);
-      tmap_replace_dim1(tdst, uint32_t(row0 + len - g0));
-    }
-  }
-  tmap_release();
-
   // ---- work lists
   if (!p.backward) {
     emit_list(p, kListFwd, reinterpret_cast<WorkItem*>(p.ws + p.L.fwd), p.L.cap_fwd, &hdr->n_fwd, hist, base);
-  } else {
+  } else if (blockIdx.x == 0) {
     write_qpad(p);
     emit_list(p, kListDkv, reinterpret_cast<WorkItem*>(p.ws + p.L.dkv), p.L.cap_dkv, &hdr->n_dkv, hist,
               base);
+  } else if (blockIdx.x == 1) {
     emit_list(p, kListDq, reinterpret_cast<WorkItem*>(p.ws + p.L.dq), p.L.cap_dq, &hdr->n_dq, hist, base);
+  } else {
     emit_list(p, kListFused, reinterpret_cast<WorkItem*>(p.ws + p.L.fused), p.L.cap_fused, &hdr->n_fused, hist,
               base);
   }
@@ -310,7 +322,10 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   p.L = L;
   p.bias = pr.bias_table;
   p.nb = pr.num_buckets;
-  plan_kernel<<<1, 1024, 0, stream>>>(maps, p);
+  // one CTA per list; helpers for the maps (one thread each), tail copies and bias table
+  const long long map_ctas = (static_cast<long long>(pr.B) * kNumMapSlots + 1023) / 1024;
+  const int helpers = int(map_ctas < 1 ? 1 : (map_ctas > 32 ? 32 : map_ctas)) + 4;
+  plan_kernel<<<(backward ? 3 : 1) + helpers, 1024, 0, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
