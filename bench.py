@@ -473,14 +473,20 @@ def run_jfa(args, rank, world, device):
     return res
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources; DRAM counters taken from other sources are stale."""
+KERNEL_SOURCE = {"forward": "jfa_fwd.cu", "bwd_preprocess": "jfa_bwd.cu", "bwd_dkdv": "jfa_bwd.cu",
+                 "bwd_dq": "jfa_bwd.cu", "bwd_fused": "jfa_bwd.cu", "plan": "jfa_plan.cu"}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the sources a kernel is compiled from (its translation unit and every shared
+    header); DRAM counters taken from other sources are stale."""
     import glob
     import hashlib
     csrc = os.path.join(ROOT, "jagged_attention_recsys_jfa_gb300", "csrc")
+    files = [os.path.join(csrc, KERNEL_SOURCE[kernel])]
+    files += sorted(glob.glob(os.path.join(csrc, "*.cuh")) + glob.glob(os.path.join(csrc, "*.h")))
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
-                    glob.glob(os.path.join(csrc, "*.h"))):
+    for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
@@ -489,12 +495,12 @@ def kernel_source_hash():
 
 def load_traffic(kernel, workload):
     """DRAM bytes (read + write) per launch from the committed ncu summary, if one matches
-    this workload and was taken on the kernel sources as they are now (else None)."""
+    this workload and was taken on the kernel's sources as they are now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        if t.get("source_sha") != kernel_source_hash():
+        if t.get("source_sha", {}).get(kernel) != kernel_source_hash(kernel):
             return None
         return t.get(workload, {}).get(kernel)
     except Exception:

@@ -46,8 +46,8 @@ struct BwdParams {
   const WorkItem* items;
   const int* n_items;
   int* status;
-  const float* lse2;    // [H][qpad_cap]  lse * log2(e), padded per sequence to 128 rows
-  const float* delta;   // [H][qpad_cap]  D, same layout
+  const float* lse2;    // [H][qpad_cap]  -lse * log2(e), padded per sequence to 128 rows
+  const float* delta;   // [H][qpad_cap]  -D, same layout
   const int64_t* qpad;  // [B+1] sequence offsets in the padded vectors
   int64_t qpad_cap;
   __nv_bfloat16* g0;   // dK (dK/dV and fused passes) or dQ (dQ pass)
@@ -67,9 +67,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // ---------------------------------------------------------------- preprocess
 // For every query tile of the dQ work list and of the fused list (whose sequences have
-// one query tile): D_i = sum_c dO_ic O_ic and lse_i * log2(e)
-// (+inf where lse = -inf, so exp2(s - lse) = 0 for a row that sees no key) into the
-// 128-row-padded per-query vectors, zeros on padding rows.  One warp per row, the lanes
+// one query tile): -D_i = -sum_c dO_ic O_ic and -lse_i * log2(e)
+// (-inf where lse = -inf, so exp2(s - lse) = 0 for a row that sees no key) into the
+// 128-row-padded per-query vectors, zeros on padding rows.  Both are stored negated so the
+// consumers add them with packed fp32x2 instructions.  One warp per row, the lanes
 // across the head dimension (coalesced 2*d-byte rows).
 struct PreParams {
   const int64_t* q_off;
@@ -128,13 +129,13 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
 #pragma unroll
         for (int k = 0; k < kLoads; ++k) {
           const int i = t * kBM + warp * 16 + k * kRowsPerLoad + sub;
-          float l2 = 0.f;
+          float nl2 = 0.f;
           if (i < Lq) {
             const float l = __ldg(p.lse + int64_t(it.h) * p.total_q + qo + i);
-            l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;
+            nl2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
           }
-          p.delta[pad0 + i] = i < Lq ? acc[k] : 0.f;
-          p.lse2[pad0 + i] = l2;
+          p.delta[pad0 + i] = i < Lq ? -acc[k] : 0.f;
+          p.lse2[pad0 + i] = nl2;
         }
       }
     }
@@ -533,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         ring_n += 2;
         const float* vec = sVec + (qtile_n % C::kVecSlots) * 256;
         ++qtile_n;
-        const float* lse2 = vec + 64 * w;
-        const float* dvec = vec + 128 + 64 * w;
+        const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(vec + 64 * w);  // -lse2 pairs
+        const uint64_t* ndvec = reinterpret_cast<const uint64_t*>(vec + 128 + 64 * w);  // -D pairs
         if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
@@ -552,22 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
               x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
           }
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 l = reinterpret_cast<const float4*>(lse2)[c4];
-            x[4 * c4] -= l.x;
-            x[4 * c4 + 1] -= l.y;
-            x[4 * c4 + 2] -= l.z;
-            x[4 * c4 + 3] -= l.w;
-          }
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
         } else {
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 l = reinterpret_cast<const float4*>(lse2)[c4];
-            x[4 * c4] = fmaf(x[4 * c4], sl2, -l.x);
-            x[4 * c4 + 1] = fmaf(x[4 * c4 + 1], sl2, -l.y);
-            x[4 * c4 + 2] = fmaf(x[4 * c4 + 2], sl2, -l.z);
-            x[4 * c4 + 3] = fmaf(x[4 * c4 + 3], sl2, -l.w);
-          }
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
         }
         if (causal) {
           const int lim = j - diag - i0;  // columns c < lim are hidden
@@ -591,13 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         float dp[64];
         ld_cols64(tP, dp);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {  // dS^T
-          const float4 dd = reinterpret_cast<const float4*>(dvec)[c4];
-          dp[4 * c4] = x[4 * c4] * (dp[4 * c4] - dd.x);
-          dp[4 * c4 + 1] = x[4 * c4 + 1] * (dp[4 * c4 + 1] - dd.y);
-          dp[4 * c4 + 2] = x[4 * c4 + 2] * (dp[4 * c4 + 2] - dd.z);
-          dp[4 * c4 + 3] = x[4 * c4 + 3] * (dp[4 * c4 + 3] - dd.w);
-        }
+        for (int c2 = 0; c2 < 32; ++c2)  // dS^T = P^T o (dP^T - D)
+          f2_unpack(f2_mul(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_add(f2_pack(dp[2 * c2], dp[2 * c2 + 1]), ndvec[c2])),
+                    dp[2 * c2], dp[2 * c2 + 1]);
         st_bf16_64(tP, dp);
         tmem_st_wait();
         tc_fence_before();
@@ -915,9 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         store_acc_row(0, D / 2, 0.f, dq_row, valid, true);
         continue;
       }
-      // padded per-query vectors: 0 past the sequence end, +inf lse2 for rows that see no key
-      const float lse2 = __ldg(p.lse2 + vec0 + i);
-      const float dd = __ldg(p.delta + vec0 + i);
+      // padded per-query vectors (stored negated): 0 past the sequence end, -inf for rows
+      // that see no key
+      const float nl2 = __ldg(p.lse2 + vec0 + i);
+      const uint64_t k_nl2 = f2_pack(nl2, nl2);
+      const float nd = __ldg(p.delta + vec0 + i);
+      const uint64_t k_nd = f2_pack(nd, nd);
       const int diag = Lk - Lq;
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       for (int jt = 0; jt < nkv && ok; ++jt) {
@@ -935,15 +926,20 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
           const int idx0 = j0 - i + p.center;
           if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 + c)) - lse2;
+            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 + c));
           } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 + c, 0), p.num_buckets - 1))) - lse2;
+              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 + c, 0), p.num_buckets - 1)));
           }
-        } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, -lse2);
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_nl2), x[2 * c2], x[2 * c2 + 1]);
+        } else {
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, k_nl2), x[2 * c2], x[2 * c2 + 1]);
         }
         if (causal) {
           const int lim = i + diag - j0;  // columns c > lim are hidden
@@ -970,7 +966,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         float dp[64];
         ld_cols64(tP, dp);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) dp[c] = x[c] * (dp[c] - dd);  // dS
+        for (int c2 = 0; c2 < 32; ++c2)  // dS = P o (dP - D)
+          f2_unpack(f2_mul(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_add(f2_pack(dp[2 * c2], dp[2 * c2 + 1]), k_nd)),
+                    dp[2 * c2], dp[2 * c2 + 1]);
         st_bf16_64(tP, dp);
         tmem_st_wait();
         tc_fence_before();
@@ -1251,8 +1249,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
     const float sl2 = p.scale_log2;
-    const float* lse2v = sVec + 64 * w;
-    const float* dvec = sVec + kBM + 64 * w;
+    const uint64_t* nlse2v = reinterpret_cast<const uint64_t*>(sVec + 64 * w);  // -lse2 pairs
+    const uint64_t* ndvec = reinterpret_cast<const uint64_t*>(sVec + kBM + 64 * w);  // -D pairs
     uint32_t g = 0, item_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
@@ -1291,10 +1289,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
         for (int c = 0; c < 64; ++c)
           x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] -= lse2v[c];
+        for (int c2 = 0; c2 < 32; ++c2)
+          f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2v[c2]), x[2 * c2], x[2 * c2 + 1]);
       } else {
+        const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, -lse2v[c]);
+        for (int c2 = 0; c2 < 32; ++c2)
+          f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, nlse2v[c2]), x[2 * c2], x[2 * c2 + 1]);
       }
       {
         // hidden: padded keys (whole row), padded queries, and i < j - diag when causal
@@ -1326,9 +1327,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
           for (int ch = 0; ch < 4; ++ch) {
             float d8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int c = 32 * hf + 8 * ch + e;
-              d8[e] = x[c] * (__uint_as_float(r[8 * ch + e]) - dvec[c]);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int c = 32 * hf + 8 * ch + 2 * e2;
+              const uint64_t dpp = f2_pack(__uint_as_float(r[8 * ch + 2 * e2]), __uint_as_float(r[8 * ch + 2 * e2 + 1]));
+              f2_unpack(f2_mul(f2_pack(x[c], x[c + 1]), f2_add(dpp, ndvec[c >> 1])), d8[2 * e2], d8[2 * e2 + 1]);
             }
             uint4 v;
             v.x = pack_bf16x2(d8[0], d8[1]);
