@@ -189,11 +189,13 @@ __device__ __forceinline__ void st_bf16_64(uint32_t taddr, const float* v) {
   tmem_st32(taddr, pk);
 }
 
-// Write `ncols` (a multiple of 32) accumulator columns of this thread's TMEM lane, times
-// `mul`, as bf16 to global (or zeros when `zero`).
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float mul, __nv_bfloat16* dst,
-                                              bool valid, bool zero) {
-  for (int cc = 0; cc < ncols / 32; ++cc) {
+// Write NC (32 or 64) accumulator columns of this thread's TMEM lane, times `mul`, as bf16
+// to global (or zeros when `zero`), one thread per row.
+template <int NC>
+__device__ __forceinline__ void store_acc_row_own(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid,
+                                                  bool zero) {
+#pragma unroll
+  for (int cc = 0; cc < NC / 32; ++cc) {
     uint32_t r[32];
     if (!zero) {
       tmem_ld32(taddr + cc * 32, r);
@@ -208,6 +210,32 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
       st_global_v8(dst + cc * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
     }
   }
+}
+// Write NC (32 or 64) accumulator columns of this thread's TMEM lane, times `mul`, as bf16
+// to global (or zeros when `zero`).  All 32 lanes of the warp call it together: the rows'
+// stores are shared across lanes so that each store instruction writes whole row segments.
+template <int NC>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid, bool zero) {
+  uint4 c[NC / 8];  // the row's NC bf16 values as 16-byte chunks
+#pragma unroll
+  for (int cc = 0; cc < NC / 32; ++cc) {
+    uint32_t r[32];
+    if (!zero) {
+      tmem_ld32(taddr + cc * 32, r);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int e = 8 * q + 2 * t;
+        w4[t] = zero ? 0u : pack_bf16x2(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul);
+      }
+      c[4 * cc + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+  }
+  st_rows_coalesced<NC * 2>(c, valid ? static_cast<void*>(dst) : nullptr);
 }
 
 // ================================================================== dK / dV pass
@@ -520,8 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       __nv_bfloat16* dk_row = p.g0 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
       __nv_bfloat16* dv_row = p.g1 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
       if (count == 0) {
-        store_acc_row(0, D / 2, 0.f, dk_row, valid, true);
-        store_acc_row(0, D / 2, 0.f, dv_row, valid, true);
+        store_acc_row<D / 2>(0, 0.f, dk_row, valid, true);
+        store_acc_row<D / 2>(0, 0.f, dv_row, valid, true);
         continue;
       }
       const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
@@ -595,13 +623,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
       if (!ok) break;
       if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
-      store_acc_row(tmem + lane_addr + C::kColA1 + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
+      store_acc_row<D / 2>(tmem + lane_addr + C::kColA1 + w * (D / 2), 1.f, dv_row, valid, false);
       tc_fence_before();
       mbar_arrive(&dv_empty);
       if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
-      store_acc_row(tmem + lane_addr + C::kColA0 + w * (D / 2), D / 2, p.scale, dk_row, valid, false);
+      store_acc_row<D / 2>(tmem + lane_addr + C::kColA0 + w * (D / 2), p.scale, dk_row, valid, false);
       tc_fence_before();
       mbar_arrive(&dk_empty);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
@@ -900,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       const bool valid = i < Lq;
       __nv_bfloat16* dq_row = p.g0 + ((qo + i) * p.H + it.h) * int64_t(D) + w * (D / 2);
       if (nkv == 0) {
-        store_acc_row(0, D / 2, 0.f, dq_row, valid, true);
+        store_acc_row<D / 2>(0, 0.f, dq_row, valid, true);
         continue;
       }
       // padded per-query vectors (stored negated): 0 past the sequence end, -inf for rows
@@ -979,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
-      store_acc_row(tmem + lane_addr + C::kColDQ + w * (D / 2), D / 2, p.scale, dq_row, valid, false);
+      store_acc_row<D / 2>(tmem + lane_addr + C::kColDQ + w * (D / 2), p.scale, dq_row, valid, false);
       tc_fence_before();
       mbar_arrive(&acc_empty);
      }
@@ -1272,8 +1300,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       __nv_bfloat16* dk_row = p.g0 + ((it.ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
       __nv_bfloat16* dv_row = p.g1 + ((it.ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
       if (!visible(kt, Lq, Lk)) {
-        store_acc_row(0, D / 2, 0.f, dk_row, valid, true);
-        store_acc_row(0, D / 2, 0.f, dv_row, valid, true);
+        store_acc_row_own<D / 2>(0, 0.f, dk_row, valid, true);
+        store_acc_row_own<D / 2>(0, 0.f, dv_row, valid, true);
         continue;
       }
       // ---- P^T = exp2(S^T * scale * log2e (+ bias) - lse2), 0 on padding and hidden pairs
@@ -1349,13 +1377,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       // ---- dV_j and dK_j rows
       if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
-      store_acc_row(tmem + lane_addr + C::kColFdV + w * (D / 2), D / 2, 1.f, dv_row, valid, false);
+      store_acc_row_own<D / 2>(tmem + lane_addr + C::kColFdV + w * (D / 2), 1.f, dv_row, valid, false);
       tc_fence_before();
       mbar_arrive(&dv_empty);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
-      store_acc_row(tmem + lane_addr + C::kColP + w * (D / 2), D / 2, p.scale, dk_row, valid, false);
+      store_acc_row_own<D / 2>(tmem + lane_addr + C::kColP + w * (D / 2), p.scale, dk_row, valid, false);
       tc_fence_before();
       mbar_arrive(&dk_empty);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
@@ -1370,12 +1398,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       if (live) {
         if (!mbar_wait(&dq_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
-        store_acc_row(tmem + lane_addr + C::kColFdQ + w * (D / 2), D / 2, p.scale, dq_row, qvalid, false);
+        store_acc_row_own<D / 2>(tmem + lane_addr + C::kColFdQ + w * (D / 2), p.scale, dq_row, qvalid, false);
         tc_fence_before();
         mbar_arrive(&dq_empty);
         ++item_n;
       } else {
-        store_acc_row(0, D / 2, 0.f, dq_row, qvalid, true);
+        store_acc_row_own<D / 2>(0, 0.f, dq_row, qvalid, true);
       }
      }
      if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);

@@ -303,6 +303,45 @@ __device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1
                : "memory");
 }
 
+// Stores one NB-byte row segment per lane (NB = 64 or 128; dst 16-byte aligned, nullptr
+// skips the row) so that every store instruction writes whole segments rather than one
+// 32-byte piece per row: within each group of NB/16 lanes the 16-byte chunks are transposed
+// with xor-shuffles (afterwards lane base+i holds chunk i of the group's rows base..base+G-1),
+// then the group writes one row segment per instruction.  All 32 lanes call it together.
+template <int NB>
+__device__ __forceinline__ void st_rows_coalesced(uint4 (&c)[NB / 16], void* dst) {
+  constexpr int G = NB / 16;
+  const int lane = threadIdx.x & 31;
+  const int i = lane & (G - 1);
+#pragma unroll
+  for (int s = 1; s < G; s <<= 1) {
+    const bool hi = (i & s) != 0;
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      if ((k & s) == 0) {
+        const uint4 send = hi ? c[k] : c[k | s];
+        uint4 got;
+        got.x = __shfl_xor_sync(0xffffffffu, send.x, s);
+        got.y = __shfl_xor_sync(0xffffffffu, send.y, s);
+        got.z = __shfl_xor_sync(0xffffffffu, send.z, s);
+        got.w = __shfl_xor_sync(0xffffffffu, send.w, s);
+        if (hi) c[k] = got;
+        else c[k | s] = got;
+      }
+    }
+  }
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+  const int base = lane & ~(G - 1);
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const unsigned long long d = __shfl_sync(0xffffffffu, mine, base + k);
+    if (d != 0ull)
+      asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(d + 16ull * i), "r"(c[k].x), "r"(c[k].y),
+                   "r"(c[k].z), "r"(c[k].w)
+                   : "memory");
+  }
+}
+
 // bf16 pair (packed in a 32-bit word, element 0 in the low half) -> two floats, exactly.
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
