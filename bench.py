@@ -7,7 +7,8 @@ Metric: valid-token TFLOPS (bf16), forward+backward, counting only the (query, k
 pairs the attention visits: fwd 4*d*H*P, bwd 10*d*H*P flops, P = sum_b Lq_b*Lk_b
 (causal: the visible pairs).  Inputs are resident in HBM for `value`; `e2e` times
 the same step through the public call with pinned host buffers copied in and the
-results copied out every step.
+results copied out every step (consecutive steps overlapped: the next step's inputs
+stream in while this one computes and its results stream out).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl jfa|reference]
 
@@ -362,31 +363,66 @@ def run_jfa(args, rank, world, device):
     value = total_flops / t_max_s / 1e12
     launches = sum(c for _, c in per_kernel.values())
 
-    # ---- end to end through the public call with host buffers
+    # ---- end to end through the public call with host buffers.  Every step copies its
+    # inputs in from pinned host memory and its results (out, lse, dq, dk, dv) back out.
+    # Consecutive steps overlap the way a training loop would run them: the next step's
+    # inputs stream in on one copy stream while this step computes, and its results stream
+    # out on another; device inputs and outputs are double-buffered so no copy touches a
+    # buffer a kernel still uses.
     pin = lambda t: t.cpu().pin_memory()
     h_in = {n: pin(getattr(batch, n)) for n in ("q", "k", "v", "dout", "q_offsets", "kv_offsets")}
-    h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-             for n, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-    d_in = {n: torch.empty_like(getattr(batch, n)) for n in h_in}
+    out_names = ("out", "lse", "dq", "dk", "dv")
+    res = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    h_out = [{n: torch.empty(res[n].shape, dtype=res[n].dtype, pin_memory=True) for n in out_names}
+             for _ in range(2)]
+    d_in = [{n: torch.empty_like(getattr(batch, n)) for n in h_in} for _ in range(2)]
+    d_out = [{n: torch.empty_like(res[n]) for n in out_names} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def e2e_step():
-        for n in h_in:
-            d_in[n].copy_(h_in[n], non_blocking=True)
-        fwd(d_in["q"], d_in["k"], d_in["v"], d_in["q_offsets"], d_in["kv_offsets"])
-        bwd(d_in["q"], d_in["k"], d_in["v"], d_in["dout"], d_in["q_offsets"], d_in["kv_offsets"])
-        for n, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            h_out[n].copy_(t, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    def e2e_step(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(ev_done[b])  # the step that last used these inputs has computed
+            for n in h_in:
+                d_in[b][n].copy_(h_in[n], non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        if used[b]:
+            s_comp.wait_event(ev_free[b])  # its results have been copied out
+        x, o = d_in[b], d_out[b]
+        jfa.jfa_forward(x["q"], x["k"], x["v"], x["q_offsets"], x["kv_offsets"], batch.bias, center, cfg.scale,
+                        cfg.causal, out=o["out"], lse=o["lse"], workspace=ws_f)
+        jfa.jfa_backward(x["dout"], x["q"], x["k"], x["v"], o["out"], o["lse"], x["q_offsets"], x["kv_offsets"],
+                         batch.bias, center, cfg.scale, cfg.causal, dq=o["dq"], dk=o["dk"], dv=o["dv"],
+                         workspace=ws_b)
+        ev_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            for n in out_names:
+                h_out[b][n].copy_(o[n], non_blocking=True)
+            ev_free[b].record(s_out)
+        used[b] = True
 
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
+    for i in range(max(2, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    # the copied-out results are the resident run's (the kernels are deterministic)
+    if not (torch.equal(h_out[0]["out"], out.cpu()) and torch.equal(h_out[0]["dq"], dq.cpu())):
+        raise RuntimeError("end-to-end results differ from the resident run")
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
+    for i in range(args.steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
     t_e2e = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=device)
     if world > 1:
         torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
