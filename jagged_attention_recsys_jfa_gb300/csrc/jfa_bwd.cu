@@ -29,6 +29,10 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kRegsLoad = 104, kRegsCompute = 200;
 static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds the launch allocation");
+// dK/dV pass (512 threads): role warps, compute warpgroups, epilogue warpgroup
+constexpr uint32_t kRegsLoadDkdv = 96, kRegsComputeDkdv = 168, kRegsEpiDkdv = 72;
+static_assert(reg_split_fits_dkdv(kRegsLoadDkdv, kRegsComputeDkdv, kRegsEpiDkdv),
+              "register split exceeds the launch allocation");
 // the fused short-query pass: more issue state in warpgroup 0, lighter compute warps
 constexpr uint32_t kRegsLoadFused = 136, kRegsComputeFused = 184;
 static_assert(reg_split_fits(kRegsLoadFused, kRegsComputeFused), "register split exceeds the launch allocation");
@@ -238,13 +242,40 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, __nv_bf
   st_rows_coalesced<NC * 2>(c, valid ? static_cast<void*>(dst) : nullptr);
 }
 
+// Writes the D accumulator columns of this thread's TMEM lane, times `mul`, as bf16 to the
+// row at `dst`, 32 columns at a time (coalesced across the warp), and arrives on `empty`
+// once the last columns are in registers: the accumulator may be overwritten from then on.
+// All 32 lanes of the warp call it together.
+template <int D>
+__device__ __forceinline__ void drain_acc_rows(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid,
+                                               uint64_t* empty) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c0, r);
+    tmem_ld_wait();
+    if (c0 + 32 == D) {
+      tc_fence_before();
+      mbar_arrive(empty);
+    }
+    uint4 c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      c[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * mul, __uint_as_float(r[8 * q + 1]) * mul),
+                        pack_bf16x2(__uint_as_float(r[8 * q + 2]) * mul, __uint_as_float(r[8 * q + 3]) * mul),
+                        pack_bf16x2(__uint_as_float(r[8 * q + 4]) * mul, __uint_as_float(r[8 * q + 5]) * mul),
+                        pack_bf16x2(__uint_as_float(r[8 * q + 6]) * mul, __uint_as_float(r[8 * q + 7]) * mul));
+    st_rows_coalesced<64>(c, valid ? static_cast<void*>(dst + c0) : nullptr);
+  }
+}
+
 // ================================================================== dK / dV pass
 // Ring of single tiles, filled in the order dO_i, Q_i for the query tiles i of each key
 // tile: dO_i is released after dV(i) and Q_i after dK(i), i.e. in fill order.  Each Q_i
 // brings its tile's lse2 and D vectors (vector slot = query tile count mod kVecSlots; a
 // slot is refilled only after dK of its previous tile completed).
 template <int D, bool kBias>
-__global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingDkdv;
   extern __shared__ uint8_t smem_raw[];
@@ -273,15 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     mbar_init(&p_full, 256);
     mbar_init(&ds_full, 256);
     mbar_init(&dv_full, 1);
-    mbar_init(&dv_empty, 256);
+    mbar_init(&dv_empty, 128);
     mbar_init(&dk_full, 1);
-    mbar_init(&dk_empty, 256);
+    mbar_init(&dk_empty, 128);
     mbar_init(&mma_done, 1);
     for (int i = 0; i < R; ++i) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    meta_init(meta);
+    meta_init(meta, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -301,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
   };
 
   if (warp < kFirstComputeWarp) {
-   setmaxnreg_dec<kRegsLoad>();
+   setmaxnreg_dec<kRegsLoadDkdv>();
    if (warp == 2) {
     // ------------------------------------------------------------ K/V loader
     // Its own warp, so a key tile's K/V load starts as soon as the previous tile's last
@@ -521,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
-  } else {
-    setmaxnreg_inc<kRegsCompute>();
+  } else if (warp < kFirstEpilogueWarp) {
+    setmaxnreg_inc<kRegsComputeDkdv>();
     // ------------------------------------------------------------ compute warpgroups
     const int w = (warp - kFirstComputeWarp) >> 2;  // column half owned: queries [64w, 64w+64)
     const int quarter = warp & 3;
@@ -531,27 +562,19 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
     const float sl2 = p.scale_log2;
-    uint32_t ring_n = 0, tile_n = 0, acc_n = 0, qtile_n = 0, tn = 0;
+    uint32_t ring_n = 0, tile_n = 0, qtile_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     uint32_t item_k = 0;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
      if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
      const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
-     const int64_t ko = it.ko;
      const int Lq = it.Lq, Lk = it.Lk;
      for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
       int first, count;
       q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
       const int j = kt * kBN + row;  // local key index
-      const bool valid = j < Lk;
-      __nv_bfloat16* dk_row = p.g0 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
-      __nv_bfloat16* dv_row = p.g1 + ((ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
-      if (count == 0) {
-        store_acc_row<D / 2>(0, 0.f, dk_row, valid, true);
-        store_acc_row<D / 2>(0, 0.f, dv_row, valid, true);
-        continue;
-      }
+      if (count == 0) continue;  // rows of zeros: written by the epilogue warpgroup
       const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       for (int i = 0; i < count && ok; ++i) {
@@ -621,18 +644,49 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const BwdParams p) {
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       }
       if (!ok) break;
+     }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  } else {
+    setmaxnreg_dec<kRegsEpiDkdv>();
+    // ------------------------------------------------------------ epilogue warpgroup
+    // Writes each key tile's dV and dK rows (this thread's TMEM lane = one key row, all D
+    // columns, 32 at a time) while the compute warpgroups go on with the next key tile;
+    // an accumulator is released as soon as its last columns are in registers.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    uint32_t acc_n = 0;
+    bool ok = true;
+    uint32_t item_k = 0;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     const int64_t ko = it.ko;
+     const int Lq = it.Lq, Lk = it.Lk;
+     for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
+      int first, count;
+      q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+      const int j = kt * kBN + row;  // local key index
+      const bool valid = j < Lk;
+      __nv_bfloat16* dk_row = p.g0 + ((ko + j) * p.H + it.h) * int64_t(D);
+      __nv_bfloat16* dv_row = p.g1 + ((ko + j) * p.H + it.h) * int64_t(D);
+      if (count == 0) {  // no query sees these keys
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          store_acc_row<32>(0, 0.f, dk_row + c0, valid, true);
+          store_acc_row<32>(0, 0.f, dv_row + c0, valid, true);
+        }
+        continue;
+      }
       if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
-      store_acc_row<D / 2>(tmem + lane_addr + C::kColA1 + w * (D / 2), 1.f, dv_row, valid, false);
-      tc_fence_before();
-      mbar_arrive(&dv_empty);
+      drain_acc_rows<D>(tmem + lane_addr + C::kColA1, 1.f, dv_row, valid, &dv_empty);
       if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
-      store_acc_row<D / 2>(tmem + lane_addr + C::kColA0 + w * (D / 2), p.scale, dk_row, valid, false);
-      tc_fence_before();
-      mbar_arrive(&dk_empty);
-      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
+      drain_acc_rows<D>(tmem + lane_addr + C::kColA0, p.scale, dk_row, valid, &dk_empty);
      }
      if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
     }
@@ -1488,6 +1542,16 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   return cudaGetLastError();
 }
 
+template <typename K>
+cudaError_t launch_dkdv_k(K kern, int smem, int grid, const BwdParams& bp, cudaStream_t stream) {
+  cudaError_t e = check_launch_registers(kern, kLaunchRegsDkdv);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreadsDkdv, smem, stream>>>(bp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dk, void* dv,
                             int num_sms, cudaStream_t stream) {
   BwdParams bp = make_params(pr, lse, ws, L, kPassDkdv);
@@ -1495,10 +1559,10 @@ cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const
   bp.g1 = static_cast<__nv_bfloat16*>(dv);
   const bool bias = pr.bias_table != nullptr;
   if (pr.d == 128)
-    return bias ? launch_big(dkdv_kernel<128, true>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream)
-                : launch_big(dkdv_kernel<128, false>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream);
-  return bias ? launch_big(dkdv_kernel<64, true>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream)
-              : launch_big(dkdv_kernel<64, false>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream);
+    return bias ? launch_dkdv_k(dkdv_kernel<128, true>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream)
+                : launch_dkdv_k(dkdv_kernel<128, false>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream);
+  return bias ? launch_dkdv_k(dkdv_kernel<64, true>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream)
+              : launch_dkdv_k(dkdv_kernel<64, false>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream);
 }
 
 cudaError_t launch_bwd_fused(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,

@@ -26,6 +26,16 @@ constexpr uint32_t kLaunchRegs = 168;
 __host__ __device__ constexpr bool reg_split_fits(uint32_t load, uint32_t compute) {
   return load % 8 == 0 && compute % 8 == 0 && 128 * load + 256 * compute <= kLaunchRegs * kThreads;
 }
+// The dK/dV pass adds a fourth warpgroup (warps 12..15) that writes the dK / dV rows out
+// while the compute warpgroups start the next key tile: 512 threads, 128 registers each
+// at launch, split role / compute / epilogue with setmaxnreg.
+constexpr int kThreadsDkdv = 512;
+constexpr int kFirstEpilogueWarp = 12;
+constexpr uint32_t kLaunchRegsDkdv = 128;
+__host__ __device__ constexpr bool reg_split_fits_dkdv(uint32_t load, uint32_t compute, uint32_t epi) {
+  return load % 8 == 0 && compute % 8 == 0 && epi % 8 == 0 &&
+         128 * load + 256 * compute + 128 * epi <= kLaunchRegsDkdv * kThreadsDkdv;
+}
 
 // One unit of work for a persistent CTA: the consecutive units [u0, u1) of sequence b,
 // head h, where a unit is

@@ -31,13 +31,13 @@ struct PlanMaps {
 // Checked once per kernel before its first launch: a build that lowered the kernel's
 // register count is refused (cudaErrorInvalidConfiguration) instead of launched.
 template <typename K>
-cudaError_t check_launch_registers(K kern) {
+cudaError_t check_launch_registers(K kern, uint32_t launch_regs = kLaunchRegs) {
   static int verdict = -1;  // -1 unknown, 0 ok, 1 refused
   if (verdict < 0) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    verdict = fa.numRegs >= int(kLaunchRegs) ? 0 : 1;
+    verdict = fa.numRegs >= int(launch_regs) ? 0 : 1;
   }
   return verdict == 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }

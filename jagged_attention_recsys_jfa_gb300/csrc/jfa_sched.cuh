@@ -28,10 +28,10 @@ struct MetaRing {
 };
 
 // One thread, before the CTA-wide barrier that publishes mbarrier initialisation.
-__device__ __forceinline__ void meta_init(MetaRing& r) {
+__device__ __forceinline__ void meta_init(MetaRing& r, int consumers = kMetaConsumers) {
   for (int i = 0; i < kMetaSlots; ++i) {
     mbar_init(&r.full[i], 1);
-    mbar_init(&r.empty[i], kMetaConsumers);
+    mbar_init(&r.empty[i], consumers);
   }
 }
 
