@@ -597,7 +597,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
           const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
           if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 - c));
+            for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias, two columns per op
+              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
+                               f2_pack(__ldg(brow + idx0 - 2 * c2), __ldg(brow + idx0 - 2 * c2 - 1))),
+                        x[2 * c2], x[2 * c2 + 1]);
           } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
@@ -1008,7 +1011,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
           const int idx0 = j0 - i + p.center;
           if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 + c));
+            for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias, two columns per op
+              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
+                               f2_pack(__ldg(brow + idx0 + 2 * c2), __ldg(brow + idx0 + 2 * c2 + 1))),
+                        x[2 * c2], x[2 * c2 + 1]);
           } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c)

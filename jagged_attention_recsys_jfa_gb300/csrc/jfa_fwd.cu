@@ -437,7 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           const int idx0 = kv0 - i + p.center;
           if (idx0 >= 0 && idx0 + kBN - 1 < p.num_buckets && n_real == kBN) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = fmaf(x[c], sl2, __ldg(brow + idx0 + c));
+            for (int c2 = 0; c2 < 64; ++c2)  // packed: x*scale + bias, two columns per op
+              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
+                               f2_pack(__ldg(brow + idx0 + 2 * c2), __ldg(brow + idx0 + 2 * c2 + 1))),
+                        x[2 * c2], x[2 * c2 + 1]);
           } else {
 #pragma unroll
             for (int c = 0; c < 128; ++c) {
