@@ -5,11 +5,14 @@ benchmark's CPU-baseline leg.  The library never routes through it.
 """
 from .jfa_oracle import (  # noqa: F401
     causal_visible,
+    jagged_bias_grad,
     jagged_backward,
     jagged_forward,
     padded_dense_forward,
     relpos_bias,
     sequence_backward,
+    sequence_bias_grad,
+    sequence_score_grad,
     sequence_forward,
     sequence_reference,
     softmax_rows,

@@ -13,7 +13,9 @@ What it computes (plain definitions, no tiling, no fusion):
   sequences packed as values plus int64 offsets ("Jagged Flash Attention (JFA)",
   Definition), with asymmetric query/key lengths and an additive per-head bias.
 * The backward of the same function (the Definition lists a backward pass among
-  JFA's features; the gradient formulas are the standard ones of FlashAttention-2).
+  JFA's features; the gradient formulas are the standard ones of FlashAttention-2),
+  and the gradient of the relative-position bias table (the Definition's custom
+  biases as a trained parameter: the chain rule through s_ij = ... + table[bucket]).
 * Two independent formulations used to pin the first one: brute-force padded
   dense attention with a -inf mask (the masking that "Four generations" item 1
   replaces), and a step-by-step float64 emulation of the tiled online softmax
@@ -112,22 +114,43 @@ def sequence_forward(q, k, v, scale, bias=None, visible=None):
     return p @ v, lse
 
 
-def sequence_backward(do, q, k, v, scale, bias=None, visible=None):
-    """Gradients of sum(dO * O) w.r.t. q, k, v (bias held constant).
+def sequence_score_grad(do, q, k, v, scale, bias=None, visible=None):
+    """Gradient of sum(dO * O) w.r.t. the scores s_ij, and P.
 
-    dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij (= rowsum(dO * O));
-    dS = P * (dP - D);  dQ = scale * dS K;  dK = scale * dS^T Q.
+    dP = dO V^T;  D_i = sum_j P_ij dP_ij (= rowsum(dO * O));  dS = P * (dP - D).
+    Hidden pairs have P = 0 and so dS = 0.
     """
     s = sequence_scores(q, k, scale, bias, visible)
     p, _ = softmax_rows(s)
     o = p @ v
-    dv = p.T @ do
     dp = do @ v.T
     D = (do * o).sum(axis=1)
-    ds = p * (dp - D[:, None])
+    return p * (dp - D[:, None]), p
+
+
+def sequence_backward(do, q, k, v, scale, bias=None, visible=None):
+    """Gradients of sum(dO * O) w.r.t. q, k, v (bias held constant).
+
+    dV = P^T dO;  dS as in `sequence_score_grad`;  dQ = scale * dS K;  dK = scale * dS^T Q.
+    """
+    ds, p = sequence_score_grad(do, q, k, v, scale, bias, visible)
+    dv = p.T @ do
     dq = scale * (ds @ k)
     dk = scale * (ds.T @ q)
     return dq, dk, dv
+
+
+def sequence_bias_grad(ds, num_buckets, center):
+    """Gradient of the loss w.r.t. one head's relative-position table from this
+    sequence's dS: s_ij depends on table[clamp(j - i + center, 0, n - 1)] with slope 1,
+    so each table entry collects the dS of every (i, j) whose bucket it is."""
+    Lq, Lk = ds.shape
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lk)[None, :]
+    idx = np.clip(j - i + center, 0, num_buckets - 1)
+    g = np.zeros(num_buckets)
+    np.add.at(g, idx.ravel(), ds.ravel())
+    return g
 
 
 # ---------------------------------------------------------------------------
@@ -199,6 +222,28 @@ def jagged_backward(dout, q, k, v, q_offsets, kv_offsets, scale, causal=False,
             dk[k0:k1, h, :] = g[1]
             dv[k0:k1, h, :] = g[2]
     return dq, dk, dv
+
+
+def jagged_bias_grad(dout, q, k, v, q_offsets, kv_offsets, scale, causal, bias_table, bias_center,
+                     heads=None):
+    """Gradient of sum(dout * out) w.r.t. the relative-position bias table: float64
+    [H, num_buckets], summed over every sequence (the table is shared by the batch).
+    `heads` optionally restricts it to a subset of heads (other rows NaN)."""
+    do, q, k, v = to_f64(dout), to_f64(q), to_f64(k), to_f64(v)
+    Tq, H, d = q.shape
+    qo = check_offsets(q_offsets, Tq)
+    ko = check_offsets(kv_offsets, k.shape[0])
+    bt = to_f64(bias_table)
+    n = bt.shape[1]
+    g = np.full((H, n), np.nan)
+    for h in (range(H) if heads is None else heads):
+        g[h] = 0.0
+        for b in range(qo.size - 1):
+            (q0, q1, _, _), qb, kb, vb, bias, vis = _seq_inputs(
+                b, h, q, k, v, qo, ko, scale, causal, bt, bias_center)
+            ds, _ = sequence_score_grad(do[q0:q1, h, :], qb, kb, vb, scale, bias, vis)
+            g[h] += sequence_bias_grad(ds, n, bias_center)
+    return g
 
 
 def sequence_reference(b, h, q, k, v, q_offsets, kv_offsets, scale, causal=False,

@@ -165,6 +165,58 @@ def test_backward_finite_differences(lq, lk, causal, bias):
         assert rel <= 1e-7, (which, rel)
 
 
+@pytest.mark.parametrize("lq,lk,causal,nb,center", [
+    ([2, 5], [3, 4], False, 12, 6),   # every relative position has its own bucket
+    ([4, 3], [2, 3], True, 12, 6),
+    ([2, 5], [3, 4], False, 5, 2),    # |j - i| > 2 clamps onto the edge buckets
+    ([4, 3, 0], [6, 3, 2], True, 4, 1),
+])
+def test_bias_grad_finite_differences(lq, lk, causal, nb, center):
+    """The table gradient against central differences of sum(dout * out) in float64."""
+    rng = np.random.default_rng(8)
+    q, k, v, do, qo, ko, bt = rand_batch(rng, lq, lk, H=2, d=4, bias_buckets=nb)
+    kw = dict(scale=0.7, causal=causal, bias_table=bt, bias_center=center)
+    g = orc.jagged_bias_grad(do, q, k, v, qo, ko, 0.7, causal, bt, center)
+    eps = 1e-6
+    num = np.zeros_like(g)
+    for idx in np.ndindex(*bt.shape):
+        plus, minus = bt.copy(), bt.copy()
+        plus[idx] += eps
+        minus[idx] -= eps
+        num[idx] = (_objective(q, k, v, do, qo, ko, dict(kw, bias_table=plus))
+                    - _objective(q, k, v, do, qo, ko, dict(kw, bias_table=minus))) / (2 * eps)
+    rel = np.linalg.norm(num - g) / max(np.linalg.norm(g), 1e-30)
+    assert rel <= 1e-7, rel
+
+
+def test_bias_grad_two_keys_closed_form():
+    """One query, two keys: softmax over two scores has dP_0 - dP_1 as its only
+    direction, so the two buckets get +-P_0 P_1 (dO.v_0 - dO.v_1)."""
+    rng = np.random.default_rng(9)
+    q, k, v, do, qo, ko, bt = rand_batch(rng, [1], [2], H=1, d=5, bias_buckets=7)
+    scale, center = 0.9, 3
+    g = orc.jagged_bias_grad(do, q, k, v, qo, ko, scale, False, bt, center)
+    s0 = scale * q[0, 0] @ k[0, 0] + bt[0, center]
+    s1 = scale * q[0, 0] @ k[1, 0] + bt[0, center + 1]
+    p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    want = p0 * (1.0 - p0) * (do[0, 0] @ v[0, 0] - do[0, 0] @ v[1, 0])
+    expect = np.zeros(7)
+    expect[center], expect[center + 1] = want, -want
+    np.testing.assert_allclose(g[0], expect, rtol=1e-12, atol=1e-15)
+
+
+def test_bias_grad_sums_to_zero_per_head():
+    """Adding one constant to a whole table row leaves every output unchanged (softmax
+    shift invariance), so each head's gradient entries sum to zero."""
+    rng = np.random.default_rng(10)
+    q, k, v, do, qo, ko, bt = rand_batch(rng, [9, 1, 0, 17], [12, 4, 3, 17], H=3, d=6, bias_buckets=20)
+    for causal in (False, True):
+        g = orc.jagged_bias_grad(do, q, k, v, qo, ko, 0.5, causal, bt, 10)
+        for h in range(3):
+            assert abs(g[h].sum()) <= 1e-12 * max(np.abs(g[h]).sum(), 1.0), (causal, h, g[h].sum())
+            assert np.abs(g[h]).sum() > 1e-3
+
+
 # --------------------------------------------------------------------------- invariants
 def test_rows_sum_to_one_and_D_identity():
     rng = np.random.default_rng(5)
@@ -363,6 +415,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
         for delta in (-2, 1):
             test_one_hot_bias_selects_relative_position(delta)
         test_backward_finite_differences([2, 5], [3, 4], False, True)
+        test_bias_grad_finite_differences([2, 5], [3, 4], False, 5, 2)
         test_causal_bottom_right_closed_forms()
         test_matches_torch_sdpa_fwd_bwd(True, 3, 7)
 
@@ -372,6 +425,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
     orig_vis = orc.causal_visible
     orig_bwd = orc.sequence_backward
     orig_scores = orc.sequence_scores
+    orig_bgrad = orc.sequence_bias_grad
 
     mutants = {
         "bias index i - j": lambda: monkeypatch.setattr(
@@ -385,6 +439,11 @@ def test_planted_mistakes_are_caught(monkeypatch):
         "bias scaled too": lambda: monkeypatch.setattr(
             orc, "sequence_scores",
             lambda q, k, s, b=None, vis=None: orig_scores(q, k, s, None if b is None else s * b, vis)),
+        "bias grad bucket i - j": lambda: monkeypatch.setattr(
+            orc, "sequence_bias_grad",
+            lambda ds, n, c: orig_bgrad(ds.T, n, c) if ds.size else orig_bgrad(ds, n, c)),
+        "bias grad without clamp merge": lambda: monkeypatch.setattr(
+            orc, "sequence_bias_grad", lambda ds, n, c: _bias_grad_drop_clamped(ds, n, c)),
         "dropped D term": lambda: monkeypatch.setattr(
             orc, "sequence_backward",
             lambda do, q, k, v, s, b=None, vis=None: _bwd_without_D(orig_scores, do, q, k, v, s, b, vis)),
@@ -401,3 +460,14 @@ def _bwd_without_D(scores, do, q, k, v, s, b, vis):
     p, _ = orc.softmax_rows(scores(q, k, s, b, vis))
     ds = p * (do @ v.T)
     return s * ds @ k, s * ds.T @ q, p.T @ do
+
+
+def _bias_grad_drop_clamped(ds, n, c):
+    """Planted mistake: pairs whose relative position falls outside the table are dropped
+    instead of landing on the edge buckets."""
+    Lq, Lk = ds.shape
+    rel = np.arange(Lk)[None, :] - np.arange(Lq)[:, None] + c
+    keep = (rel >= 0) & (rel < n)
+    g = np.zeros(n)
+    np.add.at(g, rel[keep], ds[keep])
+    return g
