@@ -66,12 +66,19 @@ typedef enum {
  * (JFA)", Definition).  kind 0 = none.  kind 1 = per-head relative-position table:
  *   beta_h(i, j) = table[h * num_buckets + clamp(j - i + center, 0, num_buckets - 1)]
  * with i, j local 0-based positions; added after scaling.  `table` is a device
- * fp32 [H][num_buckets] array; num_buckets in [1, 8192]. */
+ * fp32 [H][num_buckets] array; num_buckets in [1, 8192].
+ * `grad` (kind 1, jfa_backward only; NULL = not wanted): a device fp32 [H][num_buckets]
+ * array, 4-byte aligned, not overlapping any other argument, that jfa_backward
+ * overwrites with the gradient of sum(dout * out) w.r.t. `table`: entry (h, n) is the sum
+ * of dS_ij = P_ij (dP_ij - D_i) over every sequence's visible pairs (i, j) whose bucket is
+ * n.  It is accumulated with fp32 additions in L2 whose order is not fixed, so repeated
+ * calls can differ in the last bits.  jfa_forward ignores it. */
 typedef struct {
   int kind;
   const float* table;
   int num_buckets;
   int center;
+  float* grad;
 } jfa_bias;
 
 /* Bytes of workspace jfa_forward (is_backward = 0) or jfa_backward (is_backward = 1)
@@ -89,8 +96,9 @@ jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_
  * features, "Jagged Flash Attention (JFA)", Definition; split scheme of "Four generations"
  * item 2: dK/dV computed per key/value block, dQ in a separate pass that owns each
  * dQ tile, no atomics).  out and lse must be the forward's results for the same
- * inputs.  The bias is a constant (no bias gradient).  dq, dk, dv are bf16 with the
- * shapes of q, k, v and are fully overwritten (rows of keys no query sees get 0). */
+ * inputs.  dq, dk, dv are bf16 with the shapes of q, k, v and are fully overwritten
+ * (rows of keys no query sees get 0).  With a relative-position bias whose `grad` is
+ * non-NULL, the table's gradient is written there too (see jfa_bias). */
 jfa_status jfa_backward(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, const int64_t* q_offsets, const int64_t* kv_offsets, int B, int H,
                         int d, int64_t total_q, int64_t total_kv, const jfa_bias* bias, float scale,

@@ -132,6 +132,7 @@ jfa_status check_common(int B, int H, int d, int64_t total_q, int64_t total_kv, 
     if (bias->kind != 1) return JFA_ERR_UNSUPPORTED;
     if (!bias->table || bias->num_buckets < 1 || bias->num_buckets > kMaxBuckets) return JFA_ERR_INVALID_ARG;
     if (!aligned16(bias->table)) return JFA_ERR_INVALID_ARG;
+    if (bias->grad && (reinterpret_cast<uintptr_t>(bias->grad) & 3u) != 0) return JFA_ERR_INVALID_ARG;
   }
   return JFA_OK;
 }
@@ -152,6 +153,7 @@ Problem make_problem(int B, int H, int d, int64_t total_q, int64_t total_kv, con
   p.bias_table = has_bias ? bias->table : nullptr;
   p.num_buckets = has_bias ? bias->num_buckets : 0;
   p.center = has_bias ? bias->center : 0;
+  p.bias_grad = has_bias ? bias->grad : nullptr;
   std::lock_guard<std::mutex> g(g_trace_mu);
   for (int k = 0; k < JFA_NUM_KERNEL_KINDS; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
   return p;

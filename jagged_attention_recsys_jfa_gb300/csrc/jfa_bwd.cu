@@ -45,6 +45,7 @@ struct BwdParams {
   float scale, scale_log2;
   int causal;
   const float* bias2;  // [H][num_buckets] bias * log2(e), or nullptr
+  float* bias_grad;    // [H][num_buckets] gradient of the bias table (cleared by the planner), or nullptr
   int num_buckets, center;
   const CUtensorMap* maps;
   const WorkItem* items;
@@ -191,6 +192,43 @@ __device__ __forceinline__ void st_bf16_64(uint32_t taddr, const float* v) {
 #pragma unroll
   for (int t = 0; t < 32; ++t) pk[t] = pack_bf16x2(v[2 * t], v[2 * t + 1]);
   tmem_st32(taddr, pk);
+}
+
+// ---------------------------------------------------------------- bias-table gradient
+// Table entry (h, n) collects dS_ij over the pairs of bucket n = clamp(j - i + center, 0,
+// nb - 1).  A warp holds dS^T for its 32 key rows j = j0 + lane against 64 query columns
+// i = i0 + c: entry (lane, c) lies on relative position j - i = (j0 - i0 - 63) + b with
+// b = lane - c + 63 in [0, 95).  The warp sums along these diagonals in registers: in
+// round k (0..31) each lane takes columns k and k + 32 of lane (lane + k) mod 32 with one
+// shuffle each.  Every value a lane receives this way lies on the same diagonal --
+// b = lane + 63 for column k, lane + 31 for column k + 32 -- except those whose source
+// wrapped around the warp (lane + k >= 32), which lie 32 lower.  So each lane ends with
+// three sums, b = lane + 63, lane + 31 and lane - 1, and adds them to the table with one
+// coalesced fp32 reduction each (rel0 = j0 - i0 - 63 + center is the unclamped bucket of
+// b = 0).  No shared memory, two shuffles and two packed adds per round.
+__device__ __forceinline__ void dbias_flush(float s_hi, float s_mid, float s_lo, float* grad_row, int nb, int rel0,
+                                            int lane) {
+  const int top = nb - 1;
+  if (s_hi != 0.f) red_add_global(grad_row + min(max(rel0 + lane + 63, 0), top), s_hi);
+  if (s_mid != 0.f) red_add_global(grad_row + min(max(rel0 + lane + 31, 0), top), s_mid);
+  if (s_lo != 0.f) red_add_global(grad_row + min(max(rel0 + lane - 1, 0), top), s_lo);  // lane 0: always 0
+}
+
+__device__ __forceinline__ void dbias_warp_tile(const float* ds, float* grad_row, int nb, int rel0, int lane) {
+  uint64_t straight = 0, wrapped = 0;  // packed (column k, column k + 32) sums
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int src = (lane + k) & 31;
+    const uint64_t v = f2_pack(__shfl_sync(0xffffffffu, ds[k], src), __shfl_sync(0xffffffffu, ds[k + 32], src));
+    if (lane + k < 32)
+      straight = f2_add(straight, v);
+    else
+      wrapped = f2_add(wrapped, v);
+  }
+  float s0, s1, w0, w1;
+  f2_unpack(straight, s0, s1);
+  f2_unpack(wrapped, w0, w1);
+  dbias_flush(s0, w0 + s1, w1, grad_row, nb, rel0, lane);
 }
 
 // Write NC (32 or 64) accumulator columns of this thread's TMEM lane, times `mul`, as bf16
@@ -645,6 +683,18 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         tc_fence_before();
         mbar_arrive(&ds_full);
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
+        if (kBias && p.bias_grad) {
+          // dS^T of a padded key row is not zero (k = 0 but lse2 of the query is not), and
+          // padded query columns only give 0 while their P^T stays finite: count neither
+          const int ncols = j < Lk ? Lq - i0 : 0;
+          if (ncols < 64) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c >= ncols) dp[c] = 0.f;
+          }
+          dbias_warp_tile(dp, p.bias_grad + size_t(it.h) * p.num_buckets, p.num_buckets,
+                          kt * kBN + quarter * 32 - i0 - 63 + p.center, lane);
+        }
       }
       if (!ok) break;
      }
@@ -1404,6 +1454,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       if (!mbar_wait(&dpt_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      // bias gradient: diagonal sums of this warp's dS^T (as in dbias_warp_tile, one column
+      // half at a time); hidden and padded pairs have P^T = 0, so dS^T = 0 there
+      float db_straight[2] = {0.f, 0.f}, db_wrapped[2] = {0.f, 0.f};
       {
         uint8_t* drow = sDS + w * 16384 + row * 128;
 #pragma unroll
@@ -1420,6 +1473,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
               const uint64_t dpp = f2_pack(__uint_as_float(r[8 * ch + 2 * e2]), __uint_as_float(r[8 * ch + 2 * e2 + 1]));
               f2_unpack(f2_mul(f2_pack(x[c], x[c + 1]), f2_add(dpp, ndvec[c >> 1])), d8[2 * e2], d8[2 * e2 + 1]);
             }
+            if (kBias && p.bias_grad) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int kk = 8 * ch + e;  // round: column 32 * hf + kk of lane (lane + kk) mod 32
+                const float v = __shfl_sync(0xffffffffu, d8[e], (lane + kk) & 31);
+                if (lane + kk < 32)
+                  db_straight[hf] += v;
+                else
+                  db_wrapped[hf] += v;
+              }
+            }
             uint4 v;
             v.x = pack_bf16x2(d8[0], d8[1]);
             v.y = pack_bf16x2(d8[2], d8[3]);
@@ -1434,6 +1498,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       tc_fence_before();
       mbar_arrive(&ds_full);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
+      if (kBias && p.bias_grad)
+        dbias_flush(db_straight[0], db_wrapped[0] + db_straight[1], db_wrapped[1],
+                    p.bias_grad + size_t(it.h) * p.num_buckets, p.num_buckets,
+                    kt * kBN + quarter * 32 - i0 - 63 + p.center, lane);
       // ---- dV_j and dK_j rows
       if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
@@ -1492,6 +1560,8 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.scale_log2 = pr.scale * kLog2e;
   bp.causal = pr.causal;
   bp.bias2 = pr.bias_table ? reinterpret_cast<const float*>(w + L.bias2) : nullptr;
+  // the dK/dV and fused passes together see every visible pair once: they add the bias gradient
+  bp.bias_grad = (pr.bias_table && pass != kPassDq) ? pr.bias_grad : nullptr;
   bp.num_buckets = pr.num_buckets;
   bp.center = pr.center;
   bp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);

@@ -16,6 +16,7 @@ struct Problem {
   int causal;
   const float* bias_table;  // nullptr = no bias
   int num_buckets, center;
+  float* bias_grad;         // [H][num_buckets] fp32 gradient of the bias table (backward), or nullptr
   TraceBuf trace[JFA_NUM_KERNEL_KINDS];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
 };
 

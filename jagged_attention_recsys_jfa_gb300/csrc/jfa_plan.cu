@@ -21,6 +21,7 @@ struct PlanParams {
   uint8_t* ws;
   WsLayout L;
   const float* bias;  // [H][nb] or nullptr
+  float* bias_grad;   // [H][nb] gradient table to clear before the backward passes add into it, or nullptr
   int nb;
 };
 
@@ -198,6 +199,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
       float* b2 = reinterpret_cast<float*>(p.ws + p.L.bias2);
       for (size_t i = gt; i < size_t(p.H) * p.nb; i += gstride) b2[i] = p.bias[i] * 1.4426950408889634f;
     }
+    if (p.bias_grad)
+      for (size_t i = gt; i < size_t(p.H) * p.nb; i += gstride) p.bias_grad[i] = 0.f;
     // ---- tail copies: the last min(128, total) rows of each tensor, which the boxes that
     //      would otherwise read past the tensor's last row load from instead
     const size_t rb = p.L.row_bytes;
@@ -321,6 +324,7 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   p.ws = static_cast<uint8_t*>(ws);
   p.L = L;
   p.bias = pr.bias_table;
+  p.bias_grad = backward ? pr.bias_grad : nullptr;
   p.nb = pr.num_buckets;
   // one CTA per list; helpers for the maps (one thread each), tail copies and bias table
   const long long map_ctas = (static_cast<long long>(pr.B) * kNumMapSlots + 1023) / 1024;

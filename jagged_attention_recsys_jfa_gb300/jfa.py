@@ -41,7 +41,7 @@ class JfaError(RuntimeError):
 
 class _Bias(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("num_buckets", ctypes.c_int),
-                ("center", ctypes.c_int)]
+                ("center", ctypes.c_int), ("grad", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -125,13 +125,21 @@ def _check_offsets(name, off):
         raise ValueError(f"{name} must be a contiguous int64 CUDA tensor [B+1] with B >= 1")
 
 
-def _bias_struct(bias, center, H):
+def _bias_struct(bias, center, H, grad=None):
     if bias is None:
+        if grad is not None:
+            raise ValueError("bias_grad needs a bias table")
         return None, None
     if not bias.is_cuda or bias.dtype != torch.float32 or bias.dim() != 2 or bias.shape[0] != H:
         raise ValueError("bias must be a float32 CUDA tensor [H, num_buckets]")
     bias = bias.contiguous()
-    return _Bias(1, bias.data_ptr(), bias.shape[1], int(center)), bias
+    gptr = None
+    if grad is not None:
+        if (grad.device != bias.device or grad.dtype != torch.float32 or tuple(grad.shape) != tuple(bias.shape)
+                or not grad.is_contiguous()):
+            raise ValueError("bias_grad must be a contiguous float32 tensor shaped like the bias table, on its device")
+        gptr = grad.data_ptr()
+    return _Bias(1, bias.data_ptr(), bias.shape[1], int(center), gptr), bias
 
 
 def workspace_size(B, H, d, total_q, total_kv, backward) -> int:
@@ -188,8 +196,10 @@ def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=
 
 
 def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None,
-                 causal=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dq, dk, dv = jfa_backward(...): gradients of sum(dout * out) (bias held constant)."""
+                 causal=False, dq=None, dk=None, dv=None, workspace=None, stream=None, bias_grad=None):
+    """dq, dk, dv, workspace = jfa_backward(...): gradients of sum(dout * out).  With
+    `bias_grad` (a float32 tensor shaped like `bias`) the bias table's gradient is written
+    into it as well."""
     lib = load_library()
     _check_values("q", q)
     Tq, H, d = q.shape
@@ -201,7 +211,7 @@ def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias
     _check_offsets("kv_offsets", kv_offsets)
     B = q_offsets.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    bstruct, bias_keep = _bias_struct(bias, bias_center, H)
+    bstruct, bias_keep = _bias_struct(bias, bias_center, H, bias_grad)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -272,7 +282,7 @@ def decode_trace(buffer: torch.Tensor):
 class JaggedAttention(torch.autograd.Function):
     """Differentiable jagged attention: out = JaggedAttention.apply(q, k, v, q_offsets,
     kv_offsets, bias, bias_center, scale, causal).  lse is saved for the backward; the
-    bias table gets no gradient."""
+    bias table gets its gradient when it requires one."""
 
     @staticmethod
     def forward(ctx, q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False):
@@ -285,9 +295,10 @@ class JaggedAttention(torch.autograd.Function):
     def backward(ctx, dout):
         q, k, v, out, lse, q_offsets, kv_offsets, bias = ctx.saved_tensors
         bias_center, scale, causal = ctx.cfg
+        dbias = torch.empty_like(bias) if bias is not None and ctx.needs_input_grad[5] else None
         dq, dk, dv, _ = jfa_backward(dout.contiguous(), q, k, v, out, lse, q_offsets, kv_offsets, bias,
-                                     bias_center, scale, causal)
-        return dq, dk, dv, None, None, None, None, None, None
+                                     bias_center, scale, causal, bias_grad=dbias)
+        return dq, dk, dv, None, None, dbias, None, None, None
 
 
 def jagged_attention(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False):

@@ -71,6 +71,8 @@ def test_host_argument_checks_return_before_any_device_work():
     assert _fwd(lib, bias=ctypes.byref(bad_bias)) == 2
     big_bias = jfa.jfa._Bias(1, 16, 100000, 0)
     assert _fwd(lib, bias=ctypes.byref(big_bias)) == 1
+    odd_grad = jfa.jfa._Bias(1, 16, 16, 0, 18)     # gradient table not 4-byte aligned
+    assert _fwd(lib, bias=ctypes.byref(odd_grad)) == 1
 
 
 def test_status_strings():

@@ -1,0 +1,91 @@
+"""GPU parity of the relative-position bias table's gradient (the Definition's custom
+attention biases as a trained parameter): the CUDA path's dK/dV and fused short-query
+passes add dS into the table's buckets; the float64 oracle scatters its dS the same way.
+Tolerance: ||g - g*||_F / ||g*||_F <= 2e-2 over the whole [H, buckets] table, the bound
+the other gradients use (dS is formed in fp32 from the same bf16 inputs; its error is
+dominated by D = rowsum(dO * O) taken from the bf16 output)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.jfa_oracle as orc
+from jagged_attention_recsys_jfa_gb300 import jfa_backward, jfa_check_status, jfa_forward
+from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, JaggedConfig, make_batch
+from parity_utils import GRAD_RTOL, compare_grads, oracle_full, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(batch):
+    cfg = batch.cfg
+    out, lse, ws = jfa_forward(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, batch.bias,
+                               cfg.bias_center, cfg.scale, cfg.causal)
+    assert jfa_check_status(ws) == 0
+    g = torch.full_like(batch.bias, float("nan"))   # every entry must be written
+    dq, dk, dv, ws2 = jfa_backward(batch.dout, batch.q, batch.k, batch.v, out, lse, batch.q_offsets,
+                                   batch.kv_offsets, batch.bias, cfg.bias_center, cfg.scale, cfg.causal,
+                                   bias_grad=g)
+    assert jfa_check_status(ws2) == 0
+    torch.cuda.synchronize()
+    return {"dq": dq, "dk": dk, "dv": dv, "dbias": g}
+
+
+def _oracle_dbias(batch, heads=None):
+    cfg = batch.cfg
+    return orc.jagged_bias_grad(batch.dout, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets,
+                                cfg.scale, cfg.causal, batch.bias, cfg.bias_center, heads=heads)
+
+
+CASES = {
+    # (heads, d, q lengths, kv lengths or None, causal, buckets, center)
+    # split dK/dV pass only (every sequence has several query tiles), causal, d = 64
+    "split_causal_d64": (4, 64, [1100, 300, 129, 700], None, True, 4096, 2048),
+    # fused short-query pass only (Lq <= 128), long keys, d = 128
+    "fused_cross_d128": (2, 128, [33, 1, 100, 128, 64], [500, 2, 129, 900, 1], False, 4096, 2048),
+    # both passes in one batch, empty sequences, unequal lengths, causal
+    "mixed_causal_d128": (2, 128, [0, 5, 140, 7, 400, 90], [3, 0, 140, 9, 260, 300], True, 4096, 2048),
+    # a small table: most pairs clamp onto the two edge buckets, in both passes
+    "clamped_d64": (3, 64, [300, 40, 129, 1], [280, 700, 129, 5], False, 64, 20),
+    "clamped_causal_d128": (2, 128, [513, 77], [513, 200], True, 33, 16),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_bias_grad_matches_oracle(name):
+    H, d, lq, lk, causal, nb, center = CASES[name]
+    cfg = JaggedConfig(name, len(lq), H, d, ("uniform", 1, 1), causal=causal, bias_buckets=nb, bias_center=center)
+    batch = make_batch(cfg, device="cuda", q_lengths=lq, kv_lengths=lk)
+    res = _run(batch)
+    ref = _oracle_dbias(batch)
+    assert torch.isfinite(res["dbias"]).all(), "bias gradient has unwritten or non-finite entries"
+    e = rel_frob(res["dbias"], ref)
+    assert e <= GRAD_RTOL, f"{name}: dbias relative Frobenius error {e:.3g} > {GRAD_RTOL}"
+    # asking for the bias gradient leaves dq, dk, dv as they were
+    compare_grads(res, oracle_full(batch), name)
+
+
+def test_bias_grad_autograd():
+    from jagged_attention_recsys_jfa_gb300 import jagged_attention
+    cfg = dataclasses.replace(CONFIGS["biased_causal"], batch=5)
+    batch = make_batch(cfg, device="cuda")
+    bias = batch.bias.clone().requires_grad_(True)
+    out = jagged_attention(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, bias, cfg.bias_center,
+                           cfg.scale, cfg.causal)
+    out.backward(batch.dout)
+    e = rel_frob(bias.grad, _oracle_dbias(batch))
+    assert e <= GRAD_RTOL, f"autograd dbias relative error {e:.3g}"
+
+
+def test_bias_grad_full_size_one_head():
+    """The full biased_causal workload in the launch configuration the benchmark times;
+    the table row of one head depends on every sequence, so the oracle computes that
+    row over the whole batch."""
+    batch = make_batch(CONFIGS["biased_causal"], device="cuda")
+    res = _run(batch)
+    assert torch.isfinite(res["dbias"]).all()
+    h = int(np.random.default_rng(1).integers(batch.cfg.heads))
+    ref = _oracle_dbias(batch, heads=[h])
+    e = rel_frob(res["dbias"][h], ref[h])
+    assert e <= GRAD_RTOL, f"full size head {h}: dbias relative error {e:.3g}"
