@@ -148,9 +148,7 @@ def sequence_bias_grad(ds, num_buckets, center):
     i = np.arange(Lq)[:, None]
     j = np.arange(Lk)[None, :]
     idx = np.clip(j - i + center, 0, num_buckets - 1)
-    g = np.zeros(num_buckets)
-    np.add.at(g, idx.ravel(), ds.ravel())
-    return g
+    return np.bincount(idx.ravel(), weights=ds.ravel(), minlength=num_buckets).astype(np.float64)
 
 
 # ---------------------------------------------------------------------------
