@@ -8,7 +8,10 @@ pairs the attention visits: fwd 4*d*H*P, bwd 10*d*H*P flops, P = sum_b Lq_b*Lk_b
 (causal: the visible pairs).  Inputs are resident in HBM for `value`; `e2e` times
 the same step through the public call with pinned host buffers copied in and the
 results copied out every step (consecutive steps overlapped: the next step's inputs
-stream in while this one computes and its results stream out).
+stream in while this one computes and its results stream out).  Workloads with a
+relative-position bias also report `bias_grad`: the backward that writes the bias
+table's gradient as well, timed against the plain backward (the step itself holds the
+bias constant).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl jfa|reference]
 
@@ -391,6 +394,41 @@ def run_jfa(args, rank, world, device):
         raise RuntimeError(f"device status {st} in the graph replays")
     del graph
 
+    # ---- bias-table gradient (workloads with a relative-position bias): the same backward
+    # also writing the table's gradient, timed against the plain backward on the same inputs
+    bias_grad = None
+    if batch.bias is not None:
+        dbias = torch.empty_like(batch.bias)
+
+        def bwd_g():
+            jfa.jfa_backward(batch.dout, batch.q, batch.k, batch.v, out, lse, batch.q_offsets, batch.kv_offsets,
+                             batch.bias, center, cfg.scale, cfg.causal, dq=dq, dk=dk, dv=dv, workspace=ws_b,
+                             bias_grad=dbias)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / args.steps
+
+        t_plain, t_grad = timed(bwd), timed(bwd_g)
+        jfa.jfa_timing_read()
+        jfa.jfa_timing_enable(True)
+        timed(bwd_g)
+        jfa.jfa_timing_enable(False)
+        pk = jfa.jfa_timing_read()
+        if jfa.jfa_check_status(ws_b) != 0:
+            raise RuntimeError("device status after the bias-gradient backward")
+        bias_grad = {"bwd_ms": round(t_grad, 4), "bwd_ms_without": round(t_plain, 4),
+                     "overhead": round(t_grad / t_plain - 1, 4),
+                     "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in pk.items() if v[1]}}
+
     # ---- end to end through the public call with host buffers.  Every step copies its
     # inputs in from pinned host memory and its results (out, lse, dq, dk, dv) back out.
     # Consecutive steps overlap the way a training loop would run them: the next step's
@@ -533,7 +571,7 @@ def run_jfa(args, rank, world, device):
                          "unit": "TFLOPS"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches, "clocks": clk, "padded_sdpa": sdpa,
+        "gpu_launches": launches, "clocks": clk, "padded_sdpa": sdpa, "bias_grad": bias_grad,
         "peak_mem_extra_gb": round(peak_mem / 1e9, 3),
     }
     return res
