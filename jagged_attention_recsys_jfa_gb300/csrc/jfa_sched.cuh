@@ -1,5 +1,5 @@
 // Work-item metadata staged in shared memory.  One scheduler thread walks the CTA's
-// items (idx = blockIdx.x + k * gridDim.x) of the planner's longest-first list, loads
+// items (idx = blockIdx.x + k * gridDim.x) of the planner's work list, loads
 // each item and its sequence's offsets from global memory, and publishes them into a
 // small ring; every role of the CTA (loaders, MMA issuer, compute warps) takes item k
 // from the ring.  The scheduler runs up to kMetaSlots items ahead, so the dependent
