@@ -50,6 +50,7 @@ struct BwdParams {
   const CUtensorMap* maps;
   const WorkItem* items;
   const int* n_items;
+  int* claim;  // the list's claim counter (zeroed by the planner)
   int* status;
   const float* lse2;    // [H][qpad_cap]  -lse * log2(e), padded per sequence to 128 rows
   const float* delta;   // [H][qpad_cap]  -D, same layout
@@ -380,9 +381,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       int acq_b = -1;  // sequence whose maps this thread has acquired
       bool ok = true;
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
         if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
         const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+        if (wi.b < 0) break;  // end of this CTA's items
         const int Lq = wi.Lq, Lk = wi.Lk;
         const int64_t k0 = wi.ko;
         acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
@@ -408,9 +410,8 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
             int nb = -1, nh = 0, nt = 0;
             if (kt + 1 < wi.u1) {
               nb = wi.b, nh = wi.h, nt = kt + 1;
-            } else if (idx + int(gridDim.x) < n_items) {
-              const WorkItem wn = p.items[idx + gridDim.x];
-              nb = wn.b, nh = wn.h, nt = wn.u0;
+            } else if (const ItemMeta* wn = meta_peek_next(meta, item_k)) {
+              nb = wn->b, nh = wn->h, nt = wn->u0;
             }
             if (nb >= 0) {
               const int64_t nko = p.kv_off[nb];
@@ -449,9 +450,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         return true;
       };
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
         if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
         const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+        if (wi.b < 0) break;  // end of this CTA's items
         const int Lq = wi.Lq, Lk = wi.Lk;
         const int64_t q0 = wi.qo;
         acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
@@ -459,9 +461,9 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           int first, count;
           q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
-          if (kt + 1 == wi.u1 && idx + int(gridDim.x) < n_items) {
+          if (const ItemMeta* wnp = kt + 1 == wi.u1 ? meta_peek_next(meta, item_k) : nullptr) {
             // pull the first query tiles of this CTA's next item into L2 meanwhile
-            const WorkItem wn = p.items[idx + gridDim.x];
+            const ItemMeta& wn = *wnp;
             int nLq, nLk, nfirst, ncount;
             seq_len(wn.b, &nLq, &nLk);
             q_tiles_for_kv_tile(wn.u0, nLq, nLk, causal, &nfirst, &ncount);
@@ -523,9 +525,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
                   (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        const int Lq = wi.Lq, Lk = wi.Lk;
        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
         int first, count;
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     }
    } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else if (warp < kFirstEpilogueWarp) {
@@ -604,9 +607,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     uint32_t item_k = 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+    for (; ok; ++item_k) {
      if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
      const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     if (it.b < 0) break;  // end of this CTA's items
      const int Lq = it.Lq, Lk = it.Lk;
      for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
       int first, count;
@@ -713,9 +717,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     uint32_t acc_n = 0;
     bool ok = true;
     uint32_t item_k = 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+    for (; ok; ++item_k) {
      if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
      const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     if (it.b < 0) break;  // end of this CTA's items
      const int64_t ko = it.ko;
      const int Lq = it.Lq, Lk = it.Lk;
      for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
@@ -824,9 +829,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       int acq_b = -1;  // sequence whose maps this thread has acquired
       bool ok = true;
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        const int Lq = wi.Lq, Lk = wi.Lk;
        const int64_t q0 = wi.qo;
        acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
@@ -850,9 +856,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
           int nb = -1, nh = 0, nt = 0;
           if (qt + 1 < wi.u1) {
             nb = wi.b, nh = wi.h, nt = qt + 1;
-          } else if (idx + int(gridDim.x) < n_items) {
-            const WorkItem wn = p.items[idx + gridDim.x];
-            nb = wn.b, nh = wn.h, nt = wn.u0;
+          } else if (const ItemMeta* wn = meta_peek_next(meta, item_k)) {
+            nb = wn->b, nh = wn->h, nt = wn->u0;
           }
           if (nb >= 0) {
             const int64_t nqo = p.q_off[nb];
@@ -886,17 +891,18 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         return true;
       };
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        const int Lq = wi.Lq, Lk = wi.Lk;
        const int64_t k0 = wi.ko;
        acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
-        if (qt + 1 == wi.u1 && idx + int(gridDim.x) < n_items) {
+        if (const ItemMeta* wnp = qt + 1 == wi.u1 ? meta_peek_next(meta, item_k) : nullptr) {
           // pull the first key tiles of this CTA's next item into L2 meanwhile
-          const WorkItem wn = p.items[idx + gridDim.x];
+          const ItemMeta& wn = *wnp;
           const int64_t nko = p.kv_off[wn.b];
           const int nLk = int(p.kv_off[wn.b + 1] - nko);
           acquire_seq_maps(p.maps, wn.b, kMapK, kMapV, acq_b, true);
@@ -940,9 +946,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         }
       };
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        const int Lq = wi.Lq, Lk = wi.Lk;
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
@@ -1008,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     }
    } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else {
@@ -1023,9 +1030,10 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     uint32_t item_k = 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+    for (; ok; ++item_k) {
      if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
      const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     if (it.b < 0) break;  // end of this CTA's items
      const int64_t qo = it.qo;
      const int Lq = it.Lq, Lk = it.Lk;
      const int64_t vec0 = int64_t(it.h) * p.qpad_cap + it.qp;
@@ -1218,9 +1226,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       int acq_b = -1;
       bool ok = true;
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
         if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
         const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+        if (wi.b < 0) break;  // end of this CTA's items
         if (any_visible(wi.u0, wi.u1, wi.Lq, wi.Lk)) {
           acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
           const TileMap mq = tile_map(p.maps, p.B, kMapQ, wi.b, wi.qo, 0, p.total_q);
@@ -1252,9 +1261,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       int acq_b = -1;
       bool ok = true;
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
         if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
         const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+        if (wi.b < 0) break;  // end of this CTA's items
         for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
           if (!visible(kt, wi.Lq, wi.Lk)) continue;
           acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
@@ -1301,9 +1311,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
         }
       };
       uint32_t item_k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+      for (; ok; ++item_k) {
        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+       if (wi.b < 0) break;  // end of this CTA's items
        const int Lq = wi.Lq, Lk = wi.Lk;
        if (any_visible(wi.u0, wi.u1, Lq, Lk)) {
         if (!wait(&q_full, item_n & 1)) { ok = false; break; }
@@ -1374,7 +1385,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     }
    } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, p.qpad, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else {
@@ -1393,9 +1404,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     uint32_t item_k = 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++item_k) {
+    for (; ok; ++item_k) {
      if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
      const ItemMeta& it = meta.e[item_k % kMetaSlots];
+     if (it.b < 0) break;  // end of this CTA's items
      const int Lq = it.Lq, Lk = it.Lk;
      const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
@@ -1568,6 +1580,8 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.items = reinterpret_cast<const WorkItem*>(w + (pass == kPassDq ? L.dq : pass == kPassFused ? L.fused : L.dkv));
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);
   bp.n_items = pass == kPassDq ? &hdr->n_dq : pass == kPassFused ? &hdr->n_fused : &hdr->n_dkv;
+  WsHeader* mh = reinterpret_cast<WsHeader*>(w);
+  bp.claim = pass == kPassDq ? &mh->claim_dq : pass == kPassFused ? &mh->claim_fused : &mh->claim_dkv;
   bp.status = &reinterpret_cast<WsHeader*>(w)->status;
   (void)lse;
   bp.lse2 = reinterpret_cast<const float*>(w + L.lse2);

@@ -97,7 +97,9 @@ struct WsHeader {
   int n_dkv;       // number of dK/dV items
   int64_t total_qpad;  // sum_b round_up(Lq_b, 128): rows of the padded per-query vectors
   int n_fused;     // number of fused short-query backward items
-  int pad[57];
+  // next unclaimed item of each list (forward, dQ, dK/dV, fused), zeroed by the planner
+  int claim_fwd, claim_dq, claim_dkv, claim_fused;
+  int pad[53];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -51,6 +51,7 @@ struct FwdParams {
   const CUtensorMap* maps;  // [B][kNumMapSlots]
   const WorkItem* items;
   const int* n_items;
+  int* claim;  // the list's claim counter (zeroed by the planner)
   int* status;
   __nv_bfloat16* out;
   float* lse;
@@ -161,9 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       // descriptor prefetched) once, an item ahead, not before every load -- an acquire
       // makes the next copy through the map wait for a fresh descriptor fetch
       int acq_b = -1;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+      for (; ok; ++k) {
        if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
@@ -190,9 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           int nb = -1, nh = 0, nu = 0;
           if (u + 1 < wi.u1) {
             nb = wi.b, nh = wi.h, nu = u + 1;
-          } else if (idx + int(gridDim.x) < n_items) {
-            const WorkItem wn = p.items[idx + gridDim.x];
-            nb = wn.b, nh = wn.h, nu = wn.u0;
+          } else if (const ItemMeta* wn = meta_peek_next(meta, k)) {
+            nb = wn->b, nh = wn->h, nu = wn->u0;
           }
           if (nb >= 0) {
             const int64_t nqo = p.q_off[nb];
@@ -220,9 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       bool ok = true;
       uint32_t k = 0;
       int acq_b = -1;  // sequence whose K / V maps this thread has acquired (see the Q loader)
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+      for (; ok; ++k) {
        if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
@@ -232,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           acq_b = it.b;
         }
         // last unit of this item: pull the first key tiles of this CTA's next item into L2
-        if (u + 1 == wi.u1 && idx + int(gridDim.x) < n_items) {
-          const WorkItem wn = p.items[idx + gridDim.x];
+        if (const ItemMeta* wnp = u + 1 == wi.u1 ? meta_peek_next(meta, k) : nullptr) {
+          const ItemMeta& wn = *wnp;
           const int64_t nko = p.kv_off[wn.b];
           const int nLk = int(p.kv_off[wn.b + 1] - nko);
           if (wn.b != acq_b) {
@@ -288,9 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0}, tn = 0;
       bool ok = true;
       uint32_t k = 0;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+      for (; ok; ++k) {
        if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
+       if (wi.b < 0) break;  // end of this CTA's items
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.q_off, p.kv_off, nullptr, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, nullptr, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
   }
   } else {
@@ -383,9 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     const bool leader = (warp & 3) == 0 && lane == 0;  // records this warpgroup's trace
     bool ok = true;
     uint32_t k = 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+    for (; ok; ++k) {
      if (!meta_wait_warp(meta, k, abort_flag)) { ok = false; break; }
      const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
+     if (wi.b < 0) break;  // end of this CTA's items
      for (int u = wi.u0; u < wi.u1 && ok; ++u) {
       const ItemInfo it = decode(p, wi, u);
       const int t = s ? it.t1 : it.t0;
@@ -595,6 +599,7 @@ cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void*
   fp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
   fp.items = reinterpret_cast<const WorkItem*>(w + L.fwd);
   fp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_fwd;
+  fp.claim = &reinterpret_cast<WsHeader*>(w)->claim_fwd;
   fp.status = &reinterpret_cast<WsHeader*>(w)->status;
   fp.out = static_cast<__nv_bfloat16*>(out);
   fp.lse = lse;

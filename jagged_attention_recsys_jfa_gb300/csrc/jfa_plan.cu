@@ -2,10 +2,10 @@
 // (sequence, tensor) whose row extent is that sequence's length -- so tile loads
 // past a sequence end arrive as zeros, which the subtraction scheme of "Jagged
 // Flash Attention (JFA)", "Four generations" item 1, relies on -- and writes the
-// persistent kernels' work lists sorted longest first (counting sort on cost) and
-// laid out so that each CTA's static-stride walk takes the rounds in alternating
-// directions, the scheduling that keeps SMs busy when short sequences finish early
-// (same page, "Why standard FlashAttention falls short" and item 3).
+// persistent kernels' work lists sorted longest first (counting sort on cost), which
+// the kernels' CTAs claim one at a time from a counter, the scheduling that keeps SMs busy
+// when short sequences finish early (same page, "Why standard FlashAttention falls short"
+// and item 3).
 #include "jfa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -114,18 +114,6 @@ __device__ void for_each_range(int kind, int Lq, int Lk, bool causal, long long 
   if (n > 0) f(start, n, acc);
 }
 
-// List position of the item of sorted (longest-first) rank r, for n items walked by G
-// persistent CTAs with a static stride (CTA c takes positions c, c + G, c + 2G, ...): odd
-// rounds run backwards, so the CTA that took one round's largest item takes the next
-// round's smallest, which keeps the per-CTA totals much closer than a plain stride (a
-// partial last round is reversed within itself).
-__device__ __forceinline__ int snake_position(int r, int n, int G) {
-  const int round = r / G, k = r - round * G;
-  if ((round & 1) == 0) return r;
-  const int m = min(G, n - round * G);  // items in this round
-  return round * G + (m - 1 - k);
-}
-
 __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_t cap, int* count_out,
                           int* hist, int* base) {
   __shared__ long long total_cost;
@@ -168,7 +156,7 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
     for_each_range(kind, Lq, Lk, causal, range_cap, [&](int u0, int u1, long long cost) {
       const int pos = atomicAdd(&base[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
-      for (int h = 0; h < p.H; ++h) items[snake_position(pos + h, total, p.grid)] = WorkItem{b, h, u0, u1};
+      for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u0, u1};
     });
   }
   if (tid == 0) *count_out = total;
@@ -277,6 +265,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     if (p.q_off[0] != 0 || p.kv_off[0] != 0 || p.q_off[p.B] != p.total_q || p.kv_off[p.B] != p.total_kv)
       bad = 1;
   }
+  if (blockIdx.x == 0 && tid == 0) hdr->claim_fwd = hdr->claim_dq = hdr->claim_dkv = hdr->claim_fused = 0;
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) {

@@ -1,9 +1,10 @@
-// Work-item metadata staged in shared memory.  One scheduler thread walks the CTA's
-// items (idx = blockIdx.x + k * gridDim.x) of the planner's work list, loads
-// each item and its sequence's offsets from global memory, and publishes them into a
-// small ring; every role of the CTA (loaders, MMA issuer, compute warps) takes item k
-// from the ring.  The scheduler runs up to kMetaSlots items ahead, so the dependent
-// global loads (item, then offsets) are off the critical path at unit boundaries.
+// Work-item metadata staged in shared memory.  One scheduler thread per CTA claims items
+// of the planner's longest-first list from a launch-wide counter, loads each item and
+// its sequence's offsets from global memory, and publishes them into a small ring; every
+// role of the CTA (loaders, MMA issuer, compute warps) takes item k from the ring.  Items
+// are claimed one ahead of the one in progress, so the list is dealt out greedily, largest
+// first, to whichever CTA frees up first, and the dependent global loads (item, then
+// offsets) are still off the critical path at unit boundaries.
 #pragma once
 #include "jfa_common.cuh"
 #include "sm100_ptx.cuh"
@@ -35,28 +36,50 @@ __device__ __forceinline__ void meta_init(MetaRing& r, int consumers = kMetaCons
   }
 }
 
-// Scheduler (one thread).  False when a bounded wait ran out (the CTA is aborting).
-__device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items, int n_items, const int64_t* q_off,
-                                             const int64_t* kv_off, const int64_t* qpad, volatile int* abort) {
-  uint32_t k = 0;
-  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++k) {
-    const WorkItem wi = items[idx];
+// Scheduler (one thread).  Claims item k (idx = atomicAdd(claim, 1)) once item k - 2 is
+// released by every role, i.e. while the CTA works on item k - 1, so a CTA never holds
+// more than one claimed item it has not started.  After the list runs out it publishes an
+// end marker (b = -1) that ends every role's loop.  Slot k % kMetaSlots was last used by
+// item k - 4, which every role released before item k - 2.  False when a bounded wait ran
+// out (the CTA is aborting).
+__device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items, int n_items, int* claim,
+                                             const int64_t* q_off, const int64_t* kv_off, const int64_t* qpad,
+                                             volatile int* abort) {
+  for (uint32_t k = 0;; ++k) {
+    if (k >= 2) {
+      const uint32_t kp = k - 2;
+      if (!mbar_wait(&r.empty[kp % kMetaSlots], (kp / kMetaSlots) & 1, abort, kWaitTimeoutNs)) return false;
+    }
+    const int idx = atomicAdd(claim, 1);
     ItemMeta m;
-    m.b = wi.b;
-    m.h = wi.h;
-    m.u0 = wi.u0;
-    m.u1 = wi.u1;
-    m.qo = q_off[wi.b];
-    m.ko = kv_off[wi.b];
-    m.Lq = int(q_off[wi.b + 1] - m.qo);
-    m.Lk = int(kv_off[wi.b + 1] - m.ko);
-    m.qp = qpad ? qpad[wi.b] : 0;
+    if (idx < n_items) {
+      const WorkItem wi = items[idx];
+      m.b = wi.b;
+      m.h = wi.h;
+      m.u0 = wi.u0;
+      m.u1 = wi.u1;
+      m.qo = q_off[wi.b];
+      m.ko = kv_off[wi.b];
+      m.Lq = int(q_off[wi.b + 1] - m.qo);
+      m.Lk = int(kv_off[wi.b + 1] - m.ko);
+      m.qp = qpad ? qpad[wi.b] : 0;
+    } else {
+      m = ItemMeta{-1, 0, 0, 0, 0, 0, 0, 0, 0};
+    }
     const uint32_t s = k % kMetaSlots;
-    if (!mbar_wait(&r.empty[s], ((k / kMetaSlots) & 1) ^ 1, abort, kWaitTimeoutNs)) return false;
     r.e[s] = m;
     mbar_arrive(&r.full[s]);  // release: the entry is visible to every thread that waits on it
+    if (idx >= n_items) return true;
   }
-  return true;
+}
+
+// The CTA's item after k if the scheduler has already published it (nullptr if not yet,
+// or if it is the end marker): a look ahead for L2 prefetches, never a wait.
+__device__ __forceinline__ const ItemMeta* meta_peek_next(MetaRing& r, uint32_t k) {
+  const uint32_t n = k + 1;
+  if (!mbar_test_wait(&r.full[n % kMetaSlots], (n / kMetaSlots) & 1)) return nullptr;
+  const ItemMeta* m = &r.e[n % kMetaSlots];
+  return m->b >= 0 ? m : nullptr;
 }
 
 // Entry k for a single-thread role, read in place for the item's duration and then

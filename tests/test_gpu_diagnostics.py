@@ -32,8 +32,11 @@ def test_bounded_wait_times_out_and_reports():
 
 @pytest.mark.parametrize("kind", ["forward", "bwd_dkdv", "bwd_dq", "bwd_fused"])
 def test_trace_records_ordered_events(kind):
-    # one sequence with several query tiles (split backward passes), two with one (fused)
-    batch = make_batch(CONFIGS["tiny"], device="cuda", q_lengths=[300, 40, 7], kv_lengths=[300, 260, 9])
+    # sequences with several query tiles (split backward passes) and with one (fused).  The
+    # first CTA records; CTAs claim items as they free up and each claims its first two at
+    # once, so every list holds more than two items per SM to be sure the first CTA works
+    lq = [300, 40] * 200
+    batch = make_batch(CONFIGS["tiny"], device="cuda", q_lengths=lq, kv_lengths=[300, 260] * 200)
     buf = torch.zeros(5 * 1024, dtype=torch.int64, device="cuda")
     jfa_trace_configure(buf, kind)
     try:
