@@ -72,21 +72,29 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- preprocess
-// For every query tile of the dQ work list and of the fused list (whose sequences have
-// one query tile): -D_i = -sum_c dO_ic O_ic and -lse_i * log2(e)
-// (-inf where lse = -inf, so exp2(s - lse) = 0 for a row that sees no key) into the
-// 128-row-padded per-query vectors, zeros on padding rows.  Both are stored negated so the
-// consumers add them with packed fp32x2 instructions.  One warp per row, the lanes
-// across the head dimension (coalesced 2*d-byte rows).
+// For every query row of the 128-row-padded per-query vectors (every sequence's rows,
+// each sequence rounded up to whole tiles): -D_i = -sum_c dO_ic O_ic and -lse_i * log2(e)
+// (-inf where lse = -inf, so exp2(s - lse) = 0 for a row that sees no key), for every
+// head; zeros on padding rows.  Both are stored negated so the consumers add them with
+// packed fp32x2 instructions.  Two kernels, chosen by the width of a token row (H*d):
+// - preprocess_kernel (H*d >= 1024): one warp per padded row.  It finds the row's sequence
+//   by binary search in the padded offsets, reads the token's whole dO and O rows (H*d
+//   contiguous bf16 each, 16-byte chunks across the lanes, all loads and the row's lse
+//   values in flight before any reduction), and reduces each head's products within its
+//   group of d/8 lanes.  Consecutive warps take consecutive rows, so the reads stream.
+// - preprocess_items_kernel (narrower rows): one block per item of the dQ and fused lists,
+//   one warp per 16 rows of one head, which keeps enough loads in flight when a token row
+//   is only a few hundred bytes.
 struct PreParams {
   const int64_t* q_off;
-  int H;
+  int B, H;
   int64_t total_q;
-  const WorkItem* items;    // dQ list: units are query tiles
+  const WorkItem* items;      // dQ list: units are query tiles
   const int* n_items;
-  const WorkItem* items2;   // fused list: the sequence's one query tile
+  const WorkItem* items2;     // fused list: the sequence's one query tile
   const int* n_items2;
-  const int64_t* qpad;
+  const int64_t* qpad;        // [B+1] padded row offsets
+  const int64_t* total_qpad;  // qpad[B], written by the planner
   int64_t qpad_cap;
   const __nv_bfloat16* dout;
   const __nv_bfloat16* out;
@@ -96,7 +104,7 @@ struct PreParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
+__global__ void __launch_bounds__(256) preprocess_items_kernel(const PreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n1 = *p.n_items, n2 = *p.n_items2;
   for (int idx = blockIdx.x; idx < n1 + n2; idx += gridDim.x) {
@@ -142,6 +150,70 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreParams p) {
           }
           p.delta[pad0 + i] = i < Lq ? -acc[k] : 0.f;
           p.lse2[pad0 + i] = nl2;
+        }
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 4) preprocess_kernel(const PreParams p) {
+  constexpr int kLanesPerHead = D / 8;  // 16-byte chunks per head row
+  constexpr int kLoads = 4;             // chunks per lane in flight (rows of up to 128 chunks per pass)
+  const int lane = threadIdx.x & 31;
+  const int64_t total = *p.total_qpad;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int nchunks = p.H * kLanesPerHead;
+  for (int64_t pr = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; pr < total; pr += nwarps) {
+    int lo = 0, hi = p.B;  // the last b with qpad[b] <= pr (qpad[0] = 0 <= pr < qpad[B])
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.qpad + mid) <= pr) lo = mid; else hi = mid;
+    }
+    const int64_t qo = __ldg(p.q_off + lo);
+    const int64_t i = pr - __ldg(p.qpad + lo);
+    if (i >= __ldg(p.q_off + lo + 1) - qo) {  // padding row
+      for (int h = lane; h < p.H; h += 32) {
+        p.delta[int64_t(h) * p.qpad_cap + pr] = 0.f;
+        p.lse2[int64_t(h) * p.qpad_cap + pr] = 0.f;
+      }
+      continue;
+    }
+    const int64_t row = qo + i;
+    const uint4* drow = reinterpret_cast<const uint4*>(p.dout + row * p.H * int64_t(D));
+    const uint4* orow = reinterpret_cast<const uint4*>(p.out + row * p.H * int64_t(D));
+    for (int c0 = 0; c0 < nchunks; c0 += 32 * kLoads) {
+      // this pass covers heads [h0, h0 + 32 * kLoads / kLanesPerHead): lane t fetches head
+      // h0 + t's lse with the row loads, handed to the storing lanes by shuffle
+      const int h0 = c0 / kLanesPerHead;
+      const float l_own = h0 + lane < p.H ? __ldg(p.lse + int64_t(h0 + lane) * p.total_q + row) : 0.f;
+      uint4 a[kLoads], c[kLoads];
+#pragma unroll
+      for (int k = 0; k < kLoads; ++k) {
+        const int ch = c0 + 32 * k + lane;
+        if (ch < nchunks) {
+          a[k] = __ldg(drow + ch);
+          c[k] = __ldg(orow + ch);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kLoads; ++k) {
+        const int ch0 = c0 + 32 * k;  // warp-uniform
+        if (ch0 >= nchunks) break;
+        const int ch = ch0 + lane;
+        float acc = 0.f;
+        if (ch < nchunks)
+          acc = fmaf(bf16lo(a[k].x), bf16lo(c[k].x), bf16hi(a[k].x) * bf16hi(c[k].x)) +
+                fmaf(bf16lo(a[k].y), bf16lo(c[k].y), bf16hi(a[k].y) * bf16hi(c[k].y)) +
+                fmaf(bf16lo(a[k].z), bf16lo(c[k].z), bf16hi(a[k].z) * bf16hi(c[k].z)) +
+                fmaf(bf16lo(a[k].w), bf16lo(c[k].w), bf16hi(a[k].w) * bf16hi(c[k].w));
+#pragma unroll
+        for (int o = kLanesPerHead / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const int h = ch / kLanesPerHead;
+        const float l = __shfl_sync(0xffffffffu, l_own, (h - h0) & 31);
+        if (ch < nchunks && lane % kLanesPerHead == 0) {
+          p.delta[int64_t(h) * p.qpad_cap + pr] = -acc;
+          p.lse2[int64_t(h) * p.qpad_cap + pr] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
         }
       }
     }
@@ -1612,6 +1684,7 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   uint8_t* w = static_cast<uint8_t*>(ws);
   PreParams pp;
   pp.q_off = pr.q_off;
+  pp.B = pr.B;
   pp.H = pr.H;
   pp.total_q = pr.total_q;
   pp.items = reinterpret_cast<const WorkItem*>(w + L.dq);
@@ -1619,16 +1692,23 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   pp.items2 = reinterpret_cast<const WorkItem*>(w + L.fused);
   pp.n_items2 = &reinterpret_cast<const WsHeader*>(w)->n_fused;
   pp.qpad = reinterpret_cast<const int64_t*>(w + L.qpad);
+  pp.total_qpad = &reinterpret_cast<const WsHeader*>(w)->total_qpad;
   pp.qpad_cap = L.qpad_cap;
   pp.dout = static_cast<const __nv_bfloat16*>(dout);
   pp.out = static_cast<const __nv_bfloat16*>(out);
   pp.lse = lse;
   pp.lse2 = reinterpret_cast<float*>(w + L.lse2);
   pp.delta = reinterpret_cast<float*>(w + L.delta);
-  if (pr.d == 128)
-    preprocess_kernel<128><<<8 * num_sms, 256, 0, stream>>>(pp);
-  else
-    preprocess_kernel<64><<<8 * num_sms, 256, 0, stream>>>(pp);
+  // row-parallel for wide token rows (every block resident at once, 4 per SM at <= 64
+  // registers); per item otherwise
+  const bool wide = int64_t(pr.H) * pr.d >= 1024;
+  if (pr.d == 128) {
+    if (wide) preprocess_kernel<128><<<4 * num_sms, 256, 0, stream>>>(pp);
+    else preprocess_items_kernel<128><<<8 * num_sms, 256, 0, stream>>>(pp);
+  } else {
+    if (wide) preprocess_kernel<64><<<4 * num_sms, 256, 0, stream>>>(pp);
+    else preprocess_items_kernel<64><<<8 * num_sms, 256, 0, stream>>>(pp);
+  }
   return cudaGetLastError();
 }
 

@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     if (tid == 0) {
       atomicCAS(&hdr->status, 0, int(JFA_ERR_BAD_OFFSETS));
       hdr->n_fwd = hdr->n_dq = hdr->n_dkv = hdr->n_fused = 0;
+      hdr->total_qpad = 0;  // the preprocess walks no rows
     }
     return;
   }

@@ -58,6 +58,8 @@ EDGE = {
     "tail_two_crossing": (dict(heads=2, head_dim=128), [200, 1], [130, 70], False, False),
     "tail_trailing_empty": (dict(heads=2, head_dim=128), [90, 0, 0], [260, 0, 0], False, False),
     "tail_crossing_causal_bias_d64": (dict(heads=3, head_dim=64), [129, 3, 0], [131, 0, 2], True, True),
+    # token rows wider than one 128-chunk pass of the row-parallel preprocess (12 heads)
+    "many_heads_d128": (dict(heads=12, head_dim=128), [300, 5, 129], [260, 9, 129], False, False),
     # one long sequence with many tiles
     "long_single_d128": (dict(heads=1, head_dim=128), [1500], None, False, False),
     "long_single_causal_d64": (dict(heads=2, head_dim=64), [1100], None, True, True),
