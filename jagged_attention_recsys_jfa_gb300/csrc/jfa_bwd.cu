@@ -105,6 +105,8 @@ struct PreParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_items_kernel(const PreParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n1 = *p.n_items, n2 = *p.n_items2;
   for (int idx = blockIdx.x; idx < n1 + n2; idx += gridDim.x) {
@@ -158,6 +160,8 @@ __global__ void __launch_bounds__(256) preprocess_items_kernel(const PreParams p
 
 template <int D>
 __global__ void __launch_bounds__(256, 4) preprocess_kernel(const PreParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   constexpr int kLanesPerHead = D / 8;  // 16-byte chunks per head row
   constexpr int kLoads = 4;             // chunks per lane in flight (rows of up to 128 chunks per pass)
   const int lane = threadIdx.x & 31;
@@ -430,6 +434,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
+  grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -879,6 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
+  grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1270,6 +1276,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
+  grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1673,8 +1680,7 @@ cudaError_t launch_big(K kern, int smem, int grid, const BwdParams& bp, cudaStre
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(bp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, bp);
 }
 
 }  // namespace
@@ -1702,14 +1708,11 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   // row-parallel for wide token rows (every block resident at once, 4 per SM at <= 64
   // registers); per item otherwise
   const bool wide = int64_t(pr.H) * pr.d >= 1024;
-  if (pr.d == 128) {
-    if (wide) preprocess_kernel<128><<<4 * num_sms, 256, 0, stream>>>(pp);
-    else preprocess_items_kernel<128><<<8 * num_sms, 256, 0, stream>>>(pp);
-  } else {
-    if (wide) preprocess_kernel<64><<<4 * num_sms, 256, 0, stream>>>(pp);
-    else preprocess_items_kernel<64><<<8 * num_sms, 256, 0, stream>>>(pp);
-  }
-  return cudaGetLastError();
+  if (pr.d == 128)
+    return wide ? launch_pdl(preprocess_kernel<128>, dim3(4 * num_sms), dim3(256), 0, stream, pp)
+                : launch_pdl(preprocess_items_kernel<128>, dim3(8 * num_sms), dim3(256), 0, stream, pp);
+  return wide ? launch_pdl(preprocess_kernel<64>, dim3(4 * num_sms), dim3(256), 0, stream, pp)
+              : launch_pdl(preprocess_items_kernel<64>, dim3(8 * num_sms), dim3(256), 0, stream, pp);
 }
 
 template <typename K>
@@ -1718,8 +1721,7 @@ cudaError_t launch_dkdv_k(K kern, int smem, int grid, const BwdParams& bp, cudaS
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreadsDkdv, smem, stream>>>(bp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreadsDkdv), smem, stream, bp);
 }
 
 cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dk, void* dv,

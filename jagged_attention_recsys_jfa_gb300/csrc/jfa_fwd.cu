@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
+  grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -575,8 +576,7 @@ cudaError_t launch_fwd_t(const FwdParams& fp, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(fp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, fp);
 }
 
 }  // namespace

@@ -43,6 +43,26 @@ cudaError_t check_launch_registers(K kern, uint32_t launch_regs = kLaunchRegs) {
   return verdict == 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
+// Launch with programmatic stream serialization: the kernel's CTAs may be scheduled while the
+// previous kernel on the stream finishes (they take SMs as its CTAs exit), and every kernel
+// of this library executes griddepcontrol.wait before its first access to memory that
+// earlier work wrote, so the results are those of plain stream order.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Launch the planner: validates offsets, writes per-sequence tensor maps and the
 // longest-first work lists for the forward (backward = false) or the two backward passes.
 cudaError_t launch_plan(const Problem& p, const PlanMaps& maps, void* ws, const WsLayout& L, bool backward,

@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   __shared__ int base[kCostBuckets];
   const int tid = threadIdx.x;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+  grid_dependency_wait();    // the offsets and the workspace may come from earlier work
+  grid_launch_dependents();  // the next kernel may start its prologue; it waits for this one
 
   const int list_ctas = p.backward ? 3 : 1;
   if (int(blockIdx.x) >= list_ctas) {
@@ -332,8 +334,7 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   // one CTA per list; helpers for the maps (one thread each), tail copies and bias table
   const long long map_ctas = (static_cast<long long>(pr.B) * kNumMapSlots + 1023) / 1024;
   const int helpers = int(map_ctas < 1 ? 1 : (map_ctas > 32 ? 32 : map_ctas)) + 4;
-  plan_kernel<<<(backward ? 3 : 1) + helpers, 1024, 0, stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3((backward ? 3 : 1) + helpers), dim3(1024), 0, stream, maps, p);
 }
 
 }  // namespace jfa

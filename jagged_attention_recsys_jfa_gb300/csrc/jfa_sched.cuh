@@ -69,7 +69,10 @@ __device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items,
     const uint32_t s = k % kMetaSlots;
     r.e[s] = m;
     mbar_arrive(&r.full[s]);  // release: the entry is visible to every thread that waits on it
-    if (idx >= n_items) return true;
+    if (idx >= n_items) {
+      grid_launch_dependents();  // nothing left to claim: the next kernel may take freed SMs
+      return true;
+    }
   }
 }
 

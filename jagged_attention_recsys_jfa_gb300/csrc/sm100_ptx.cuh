@@ -13,6 +13,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may start while the previous kernel on its stream is still finishing; it must wait here
+// before it reads or writes anything earlier work produced.  launch_dependents lets the next
+// kernel launch once every CTA of this one has issued it (or exited).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Fire-and-forget fp32 addition into global memory (performed at L2, no value returned).
 __device__ __forceinline__ void red_add_global(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
