@@ -11,7 +11,8 @@ key/value lengths that differ, an additive bias; Results: jaggedness around one
 half).  Production length distributions are not public; the uniform and log-normal
 mixes below stand in for them.
 
-Draw order (one generator per call): lengths -> q -> k -> v -> bias -> dout.
+Draw order (one generator per call): lengths -> q -> k -> v -> bias -> dout -> general
+bias (the last only for workloads that have one, so the others are unchanged by it).
 Values are float32 normal samples rounded to bfloat16 (round to nearest even);
 the oracle promotes exactly these bf16 values to float64.
 """
@@ -43,6 +44,7 @@ class JaggedConfig:
     bias_buckets: int = 0          # 0 = no bias; else per-head relative-position table size
     bias_center: int = 0           # bucket = clamp(j - i + center, 0, buckets - 1)
     bias_std: float = 0.5
+    general_bias: bool = False     # a general jagged bias: one Lq x Lk bf16 matrix per sequence and head
     seed: int = 0
 
     @property
@@ -79,6 +81,13 @@ def _draw_lengths(spec: tuple, n: int, g: torch.Generator) -> torch.Tensor:
     raise ValueError(f"unknown length spec {spec!r}")
 
 
+def jagged_bias_offsets(q_lengths: torch.Tensor, kv_lengths: torch.Tensor) -> torch.Tensor:
+    """Block offsets of a general jagged bias: sequence b's Lq_b x Lk_b block takes
+    Lq_b * round_up(Lk_b, 8) elements (rows padded to a multiple of 8), blocks packed."""
+    sizes = q_lengths.to(torch.int64) * ((kv_lengths.to(torch.int64) + 7) // 8 * 8)
+    return offsets_from_lengths(sizes)
+
+
 def offsets_from_lengths(lengths: torch.Tensor) -> torch.Tensor:
     """int64 [B+1] exclusive prefix sum: off[0] = 0, off[b+1] = off[b] + len[b]."""
     off = torch.zeros(lengths.numel() + 1, dtype=torch.int64)
@@ -98,6 +107,8 @@ class JaggedBatch:
     v: torch.Tensor              # bf16 [Tk, H, d]
     bias: Optional[torch.Tensor]  # fp32 [H, buckets] or None
     dout: torch.Tensor           # bf16 [Tq, H, d]
+    jbias: Optional[torch.Tensor] = None          # bf16 [H, plane]: general jagged bias, or None
+    jbias_offsets: Optional[torch.Tensor] = None  # int64 [B+1] block offsets, on `device`
 
     @property
     def total_q(self) -> int:
@@ -149,5 +160,12 @@ def make_batch(cfg: JaggedConfig, device="cpu", seed: Optional[int] = None,
         bias = torch.randn((H, cfg.bias_buckets), generator=gv, device=device,
                            dtype=torch.float32) * cfg.bias_std
     dout = normal_bf16(Tq)
+    jbias = jboff = None
+    if cfg.general_bias:
+        jboff = jagged_bias_offsets(lq, lk)
+        plane = int(jboff[-1])
+        jbias = (torch.randn((H, plane), generator=gv, device=device, dtype=torch.float32)
+                 * cfg.bias_std).to(torch.bfloat16)
+        jboff = jboff.to(device)
     return JaggedBatch(cfg, lq, lk, offsets_from_lengths(lq).to(device),
-                       offsets_from_lengths(lk).to(device), q, k, v, bias, dout)
+                       offsets_from_lengths(lk).to(device), q, k, v, bias, dout, jbias, jboff)

@@ -8,6 +8,7 @@ from .jfa_oracle import (  # noqa: F401
     jagged_bias_grad,
     jagged_backward,
     jagged_forward,
+    jagged_bias_block,
     padded_dense_forward,
     relpos_bias,
     sequence_backward,

@@ -28,7 +28,9 @@ Readings where the pages are silent (each also listed in the design notes):
 * layout: jagged values are token-major [T, H, d]; lse is [H, T];
 * scores: s_ij = scale * q_i . k_j + beta_h(i, j); bias is added after scaling;
 * bias: per-head relative-position table, beta_h(i, j) = table[h, clamp(j - i +
-  center, 0, buckets - 1)] with i, j local 0-based positions;
+  center, 0, buckets - 1)] with i, j local 0-based positions; or a general jagged
+  bias, one Lq x Lk matrix per sequence and head, stored row-major with rows padded
+  to a multiple of 8 elements from a per-sequence block offset;
 * causal with unequal lengths: bottom-right alignment, key j visible to query i
   iff j <= i + (Lk - Lq);
 * a query row that sees no key (empty key sequence, or causal with Lq > Lk):
@@ -72,6 +74,14 @@ def relpos_bias(table_row, Lq, Lk, center):
     j = np.arange(Lk)[None, :]
     idx = np.clip(j - i + center, 0, n - 1)
     return table_row[idx]
+
+
+def jagged_bias_block(values_h, off_b, Lq, Lk):
+    """One sequence's block of a general jagged bias (one head's plane `values_h`): the
+    Lq x Lk matrix stored row-major from element `off_b` with its rows padded to a
+    multiple of 8 elements."""
+    pitch = (Lk + 7) // 8 * 8
+    return values_h[off_b:off_b + Lq * pitch].reshape(Lq, pitch)[:, :Lk]
 
 
 def causal_visible(Lq, Lk):
@@ -155,7 +165,7 @@ def sequence_bias_grad(ds, num_buckets, center):
 # jagged front ends
 # ---------------------------------------------------------------------------
 
-def _seq_inputs(b, h, q, k, v, qo, ko, scale, causal, bias_table, bias_center):
+def _seq_inputs(b, h, q, k, v, qo, ko, scale, causal, bias_table, bias_center, jagged_bias=None):
     q0, q1 = int(qo[b]), int(qo[b + 1])
     k0, k1 = int(ko[b]), int(ko[b + 1])
     qb, kb, vb = q[q0:q1, h, :], k[k0:k1, h, :], v[k0:k1, h, :]
@@ -163,8 +173,18 @@ def _seq_inputs(b, h, q, k, v, qo, ko, scale, causal, bias_table, bias_center):
     bias = None
     if bias_table is not None:
         bias = relpos_bias(bias_table[h], Lq, Lk, bias_center)
+    elif jagged_bias is not None:
+        values, boff = jagged_bias
+        bias = jagged_bias_block(values[h], int(boff[b]), Lq, Lk)
     vis = causal_visible(Lq, Lk) if causal else None
     return (q0, q1, k0, k1), qb, kb, vb, bias, vis
+
+
+def _jagged_bias_f64(jagged_bias):
+    if jagged_bias is None:
+        return None
+    values, boff = jagged_bias
+    return to_f64(values), to_i64(boff)
 
 
 def check_offsets(off, total):
@@ -175,25 +195,29 @@ def check_offsets(off, total):
 
 
 def jagged_forward(q, k, v, q_offsets, kv_offsets, scale, causal=False,
-                   bias_table=None, bias_center=0, heads=None):
+                   bias_table=None, bias_center=0, heads=None, jagged_bias=None):
     """Jagged attention forward.
 
     q: [Tq, H, d]; k, v: [Tk, H, d]; offsets int64 [B+1].
     Returns out float64 [Tq, H, d] and lse float64 [H, Tq].
     `heads` optionally restricts the computation to a subset of heads (the other
     heads' entries are left as NaN) -- used to sample large workloads.
+    `jagged_bias` = (values [H, plane], block offsets [B+1]): a general additive bias,
+    one block per sequence (see `jagged_bias_block`), instead of the relative-position
+    table.
     """
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     Tq, H, d = q.shape
     qo = check_offsets(q_offsets, Tq)
     ko = check_offsets(kv_offsets, k.shape[0])
     bt = to_f64(bias_table)
+    jb = _jagged_bias_f64(jagged_bias)
     out = np.full((Tq, H, d), np.nan)
     lse = np.full((H, Tq), np.nan)
     for b in range(qo.size - 1):
         for h in (range(H) if heads is None else heads):
             (q0, q1, _, _), qb, kb, vb, bias, vis = _seq_inputs(
-                b, h, q, k, v, qo, ko, scale, causal, bt, bias_center)
+                b, h, q, k, v, qo, ko, scale, causal, bt, bias_center, jb)
             o, l = sequence_forward(qb, kb, vb, scale, bias, vis)
             out[q0:q1, h, :] = o
             lse[h, q0:q1] = l
@@ -201,20 +225,21 @@ def jagged_forward(q, k, v, q_offsets, kv_offsets, scale, causal=False,
 
 
 def jagged_backward(dout, q, k, v, q_offsets, kv_offsets, scale, causal=False,
-                    bias_table=None, bias_center=0):
+                    bias_table=None, bias_center=0, jagged_bias=None):
     """Jagged attention backward: (dq, dk, dv), float64, shapes of q, k, v."""
     do, q, k, v = to_f64(dout), to_f64(q), to_f64(k), to_f64(v)
     Tq, H, d = q.shape
     qo = check_offsets(q_offsets, Tq)
     ko = check_offsets(kv_offsets, k.shape[0])
     bt = to_f64(bias_table)
+    jb = _jagged_bias_f64(jagged_bias)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     for b in range(qo.size - 1):
         for h in range(H):
             (q0, q1, k0, k1), qb, kb, vb, bias, vis = _seq_inputs(
-                b, h, q, k, v, qo, ko, scale, causal, bt, bias_center)
+                b, h, q, k, v, qo, ko, scale, causal, bt, bias_center, jb)
             g = sequence_backward(do[q0:q1, h, :], qb, kb, vb, scale, bias, vis)
             dq[q0:q1, h, :] = g[0]
             dk[k0:k1, h, :] = g[1]
@@ -245,7 +270,7 @@ def jagged_bias_grad(dout, q, k, v, q_offsets, kv_offsets, scale, causal, bias_t
 
 
 def sequence_reference(b, h, q, k, v, q_offsets, kv_offsets, scale, causal=False,
-                       bias_table=None, bias_center=0, dout=None):
+                       bias_table=None, bias_center=0, dout=None, jagged_bias=None):
     """Oracle results for one (sequence, head): (o, lse) and, if dout is given,
     also (dq, dk, dv).  Inputs may be full jagged tensors on any device; only the
     rows of sequence b are copied to the host."""
@@ -257,6 +282,11 @@ def sequence_reference(b, h, q, k, v, q_offsets, kv_offsets, scale, causal=False
     bias = None
     if bias_table is not None:
         bias = relpos_bias(to_f64(bias_table[h]), q1 - q0, k1 - k0, bias_center)
+    elif jagged_bias is not None:
+        values, boff = jagged_bias
+        off_b = int(to_i64(boff[b:b + 1])[0])
+        pitch = (k1 - k0 + 7) // 8 * 8
+        bias = jagged_bias_block(to_f64(values[h, off_b:off_b + (q1 - q0) * pitch]), 0, q1 - q0, k1 - k0)
     vis = causal_visible(q1 - q0, k1 - k0) if causal else None
     o, lse = sequence_forward(qb, kb, vb, scale, bias, vis)
     if dout is None:
@@ -270,7 +300,7 @@ def sequence_reference(b, h, q, k, v, q_offsets, kv_offsets, scale, causal=False
 # ---------------------------------------------------------------------------
 
 def padded_dense_forward(q, k, v, q_offsets, kv_offsets, scale, causal=False,
-                         bias_table=None, bias_center=0):
+                         bias_table=None, bias_center=0, jagged_bias=None):
     """Pad every sequence to the batch maximum, build the full [B, H, Lq, Lk]
     score tensor, put -inf on every padded or causally hidden entry, softmax, and
     unpad.  Shares only numpy with the per-sequence path above."""
@@ -296,6 +326,15 @@ def padded_dense_forward(q, k, v, q_offsets, kv_offsets, scale, causal=False,
         bt = to_f64(bias_table)
         idx = np.clip(jj[0] - ii[0] + bias_center, 0, bt.shape[1] - 1)   # [Mq, Mk]
         S = S + bt[:, idx][None]
+    if jagged_bias is not None:
+        # general bias: sequence b's block starts at element boff[b] of each head's plane,
+        # rows of round_up(Lk_b, 8) elements; read element by element
+        vals, boff = to_f64(jagged_bias[0]), to_i64(jagged_bias[1])
+        for b in range(B):
+            pitch = -(-int(Lk[b]) // 8) * 8
+            for i in range(int(Lq[b])):
+                for j in range(int(Lk[b])):
+                    S[b, :, i, j] += vals[:, int(boff[b]) + i * pitch + j]
     mask = (ii < Lq[:, None, None]) & (jj < Lk[:, None, None])          # [B, Mq, Mk]
     if causal:
         mask &= jj <= ii + (Lk - Lq)[:, None, None]

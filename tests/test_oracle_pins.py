@@ -217,6 +217,71 @@ def test_bias_grad_sums_to_zero_per_head():
             assert np.abs(g[h]).sum() > 1e-3
 
 
+def _pack_jagged_bias(blocks, lq, lk, H):
+    """Lay per-sequence [H, Lq, Lk] bias blocks out in the packed format (rows padded to a
+    multiple of 8, blocks back to back), element by element."""
+    pitch = [(int(b) + 7) // 8 * 8 for b in lk]
+    off = np.concatenate([[0], np.cumsum([int(a) * p for a, p in zip(lq, pitch)])]).astype(np.int64)
+    vals = np.full((H, int(off[-1])), np.nan)   # padding columns must never be read
+    for b, blk in enumerate(blocks):
+        for h in range(H):
+            for i in range(int(lq[b])):
+                for j in range(int(lk[b])):
+                    vals[h, off[b] + i * pitch[b] + j] = blk[h, i, j]
+    return vals, off
+
+
+@pytest.mark.parametrize("lq,lk,causal", [
+    ([3, 1, 5], [3, 1, 5], False),
+    ([4, 2, 6], [7, 1, 3], True),
+    ([0, 5, 2, 9], [4, 0, 2, 11], False),
+    ([0, 5, 2, 9], [4, 0, 2, 11], True),
+])
+def test_jagged_bias_matches_padded_dense(lq, lk, causal):
+    """The general bias read through the oracle's block layout against the padded dense
+    formulation, which reads the packed values element by element."""
+    rng = np.random.default_rng(11)
+    q, k, v, _, qo, ko, _ = rand_batch(rng, lq, lk)
+    H = q.shape[1]
+    vals, off = _pack_jagged_bias([rng.standard_normal((H, a, b)) for a, b in zip(lq, lk)], lq, lk, H)
+    jb = (np.nan_to_num(vals, nan=1e300), off)   # a padding read would show up as a huge score
+    kw = dict(scale=0.37, causal=causal, jagged_bias=jb)
+    o1, l1 = orc.jagged_forward(q, k, v, qo, ko, **kw)
+    o2, l2 = orc.padded_dense_forward(q, k, v, qo, ko, **kw)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    fin = np.isfinite(l2)
+    assert np.array_equal(fin, np.isfinite(l1))
+    np.testing.assert_allclose(l1[fin], l2[fin], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_jagged_bias_equal_to_relpos_table(causal):
+    """A general bias whose blocks hold the relative-position lookup gives the relative-
+    position results exactly (forward and backward)."""
+    rng = np.random.default_rng(12)
+    lq, lk = [6, 2, 9], [5, 4, 9]
+    q, k, v, do, qo, ko, bt = rand_batch(rng, lq, lk, bias_buckets=9)
+    center = 4
+    H = q.shape[1]
+    blocks = []
+    for a, b in zip(lq, lk):
+        blk = np.zeros((H, a, b))
+        for i in range(a):
+            for j in range(b):
+                blk[:, i, j] = bt[:, min(max(j - i + center, 0), 8)]
+        blocks.append(blk)
+    jb = _pack_jagged_bias(blocks, lq, lk, H)
+    jb = (np.nan_to_num(jb[0], nan=1e300), jb[1])
+    r1 = orc.jagged_forward(q, k, v, qo, ko, 0.5, causal, bias_table=bt, bias_center=center)
+    r2 = orc.jagged_forward(q, k, v, qo, ko, 0.5, causal, jagged_bias=jb)
+    for a, b in zip(r1, r2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+    g1 = orc.jagged_backward(do, q, k, v, qo, ko, 0.5, causal, bias_table=bt, bias_center=center)
+    g2 = orc.jagged_backward(do, q, k, v, qo, ko, 0.5, causal, jagged_bias=jb)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
 # --------------------------------------------------------------------------- invariants
 def test_rows_sum_to_one_and_D_identity():
     rng = np.random.default_rng(5)
