@@ -98,11 +98,14 @@ def workload_bytes(batch):
     Tql, Tkl, Tqs, Tks = float(lq[long_].sum()), float(lk[long_].sum()), float(lq[short].sum()), float(lk[short].sum())
     vecl = 8.0 * H * float(((lq[long_] + 127) // 128 * 128).sum())
     vecs = vec - vecl
-    return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq,
+    # a general jagged bias is read once by each pass that covers its sequence (bf16 blocks)
+    jb = 2.0 * H * lq * ((lk + 7) // 8 * 8) if batch.cfg.general_bias else 0.0 * lq
+    jbl, jbs = float(np.sum(jb[long_])), float(np.sum(jb[short]))
+    return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq + jbl + jbs,
             "bwd_preprocess": 2 * Tq * row + 4.0 * H * Tq + vec,
-            "bwd_dkdv": (2 * Tql + 2 * Tkl) * row + vecl + 2 * Tkl * row,
-            "bwd_dq": (2 * Tql + 2 * Tkl) * row + vecl + Tql * row,
-            "bwd_fused": (2 * Tqs + 2 * Tks) * row + vecs + (Tqs + 2 * Tks) * row}
+            "bwd_dkdv": (2 * Tql + 2 * Tkl) * row + vecl + 2 * Tkl * row + jbl,
+            "bwd_dq": (2 * Tql + 2 * Tkl) * row + vecl + Tql * row + jbl,
+            "bwd_fused": (2 * Tqs + 2 * Tks) * row + vecs + (Tqs + 2 * Tks) * row + jbs}
 
 
 def load_peaks():
@@ -120,7 +123,8 @@ def config_dict(cfg, name):
          "lengths": list(cfg.lengths), "causal": cfg.causal,
          "kv_lengths": list(cfg.kv_lengths) if cfg.kv_lengths else "same as query",
          "bias": f"relpos table [H,{cfg.bias_buckets}] fp32, bucket j-i+{cfg.bias_center}" if cfg.bias_buckets
-         else None, "seed": cfg.seed, "l2": "inputs larger than L2, no flush"}
+         else ("general jagged bias, bf16 Lq x Lk block per sequence and head" if cfg.general_bias else None),
+         "seed": cfg.seed, "l2": "inputs larger than L2, no flush"}
     return d
 
 
@@ -202,7 +206,8 @@ def oracle_sample(batch, budget_s, rng_seed=0):
     for b in order:
         h = int(rng.integers(cfg.heads))
         orc.sequence_reference(int(b), h, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets,
-                               cfg.scale, cfg.causal, batch.bias, center, dout=batch.dout)
+                               cfg.scale, cfg.causal, batch.bias, center, dout=batch.dout,
+                               jagged_bias=(batch.jbias, batch.jbias_offsets) if batch.jbias is not None else None)
         P = valid_pairs([lq[b]], [lk[b]], cfg.causal)
         done_flops += 14.0 * dH * P
         pairs += 1
@@ -250,6 +255,18 @@ def padded_sdpa(batch, steps):
         if cfg.causal:
             bias = bias.masked_fill(j > i, float("-inf"))
         mask = bias.to(torch.bfloat16)
+    if cfg.general_bias:
+        # the blocks copied into the padded score shape; padding and hidden pairs -inf
+        jbo = batch.jbias_offsets.cpu().tolist()
+        mask = torch.full((B, H, Lq, Lk), float("-inf"), dtype=torch.bfloat16, device=dev)
+        for b in range(B):
+            lqb, lkb = qo[b + 1] - qo[b], ko[b + 1] - ko[b]
+            pitch = (lkb + 7) // 8 * 8
+            blk = batch.jbias[:, jbo[b]:jbo[b] + lqb * pitch].reshape(H, lqb, pitch)[:, :, :lkb]
+            if cfg.causal:
+                vis = torch.ones(lqb, lkb, dtype=torch.bool, device=dev).tril(diagonal=lkb - lqb)
+                blk = blk.masked_fill(~vis, float("-inf"))
+            mask[b, :, :lqb, :lkb] = blk
     backends = [SDPBackend.FLASH_ATTENTION, SDPBackend.EFFICIENT_ATTENTION, SDPBackend.MATH] if mask is None \
         else [SDPBackend.EFFICIENT_ATTENTION, SDPBackend.CUDNN_ATTENTION, SDPBackend.MATH]
     for be in backends:
@@ -299,13 +316,15 @@ def run_jfa(args, rank, world, device):
     ws_f = jfa.new_workspace(B, H, d, Tq, Tk, False, device)
     ws_b = jfa.new_workspace(B, H, d, Tq, Tk, True, device)
 
+    jb = (batch.jbias, batch.jbias_offsets) if batch.jbias is not None else None
+
     def fwd(q=batch.q, k=batch.k, v=batch.v, qo=batch.q_offsets, ko=batch.kv_offsets):
         jfa.jfa_forward(q, k, v, qo, ko, batch.bias, center, cfg.scale, cfg.causal, out=out, lse=lse,
-                        workspace=ws_f)
+                        workspace=ws_f, jagged_bias=jb)
 
     def bwd(q=batch.q, k=batch.k, v=batch.v, do=batch.dout, qo=batch.q_offsets, ko=batch.kv_offsets):
         jfa.jfa_backward(do, q, k, v, out, lse, qo, ko, batch.bias, center, cfg.scale, cfg.causal,
-                         dq=dq, dk=dk, dv=dv, workspace=ws_b)
+                         dq=dq, dk=dk, dv=dv, workspace=ws_b, jagged_bias=jb)
 
     for _ in range(args.warmup):
         fwd()
@@ -443,7 +462,9 @@ def run_jfa(args, rank, world, device):
     # out on another; device inputs and outputs are double-buffered so no copy touches a
     # buffer a kernel still uses.
     pin = lambda t: t.cpu().pin_memory()
-    h_in = {n: pin(getattr(batch, n)) for n in ("q", "k", "v", "dout", "q_offsets", "kv_offsets")}
+    in_names = ("q", "k", "v", "dout", "q_offsets", "kv_offsets") + (
+        ("jbias", "jbias_offsets") if batch.jbias is not None else ())  # a general bias is per-batch input
+    h_in = {n: pin(getattr(batch, n)) for n in in_names}
     out_names = ("out", "lse", "dq", "dk", "dv")
     res = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
     h_out = [{n: torch.empty(res[n].shape, dtype=res[n].dtype, pin_memory=True) for n in out_names}
@@ -471,11 +492,12 @@ def run_jfa(args, rank, world, device):
         if used[b]:
             s_comp.wait_event(ev_free[b])  # its results have been copied out
         x, o = d_in[b], d_out[b]
+        xjb = (x["jbias"], x["jbias_offsets"]) if "jbias" in x else None
         jfa.jfa_forward(x["q"], x["k"], x["v"], x["q_offsets"], x["kv_offsets"], batch.bias, center, cfg.scale,
-                        cfg.causal, out=o["out"], lse=o["lse"], workspace=ws_f)
+                        cfg.causal, out=o["out"], lse=o["lse"], workspace=ws_f, jagged_bias=xjb)
         jfa.jfa_backward(x["dout"], x["q"], x["k"], x["v"], o["out"], o["lse"], x["q_offsets"], x["kv_offsets"],
                          batch.bias, center, cfg.scale, cfg.causal, dq=o["dq"], dk=o["dk"], dv=o["dv"],
-                         workspace=ws_b)
+                         workspace=ws_b, jagged_bias=xjb)
         ev_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[b])

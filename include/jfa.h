@@ -55,15 +55,16 @@ typedef struct CUstream_st* jfa_stream_t; /* a cudaStream_t; NULL = legacy defau
 typedef enum {
   JFA_OK = 0,
   JFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
-  JFA_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128}, unsupported bias kind */
+  JFA_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128}, unsupported bias kind or bias gradient */
   JFA_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
   JFA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
-  JFA_ERR_BAD_OFFSETS = 5, /* device: offsets not 0-based, not monotone, or last != total */
+  JFA_ERR_BAD_OFFSETS = 5, /* device: offsets not 0-based, not monotone, or last != total (also kind-2 bias block offsets) */
   JFA_ERR_TIMEOUT = 6      /* device: a bounded pipeline wait ran out; outputs unspecified */
 } jfa_status;
 
 /* Additive attention bias (the user-defined biases of "Jagged Flash Attention
- * (JFA)", Definition).  kind 0 = none.  kind 1 = per-head relative-position table:
+ * (JFA)", Definition).  kind 0 = none.  kind 2 = general jagged bias (below).
+ * kind 1 = per-head relative-position table:
  *   beta_h(i, j) = table[h * num_buckets + clamp(j - i + center, 0, num_buckets - 1)]
  * with i, j local 0-based positions; added after scaling.  `table` is a device
  * fp32 [H][num_buckets] array; num_buckets in [1, 8192].
@@ -72,13 +73,25 @@ typedef enum {
  * overwrites with the gradient of sum(dout * out) w.r.t. `table`: entry (h, n) is the sum
  * of dS_ij = P_ij (dP_ij - D_i) over every sequence's visible pairs (i, j) whose bucket is
  * n.  It is accumulated with fp32 additions in L2 whose order is not fixed, so repeated
- * calls can differ in the last bits.  jfa_forward ignores it. */
+ * calls can differ in the last bits.  jfa_forward ignores it.
+ * kind 2 = general jagged bias: beta_h(i, j) = values[h * plane + block_offsets[b] +
+ * i * round_up(Lk_b, 8) + j], i.e. one Lq_b x Lk_b matrix per sequence and head, stored
+ * row-major with each row padded to a multiple of 8 elements (the padding is never
+ * read), the blocks of one head packed into a plane of `plane` elements.  `values` is a
+ * device bf16 array [H][plane], 16-byte aligned; `block_offsets` a device int64 array
+ * [B+1] with block_offsets[0] = 0 and block_offsets[b+1] - block_offsets[b] =
+ * Lq_b * round_up(Lk_b, 8), block_offsets[B] = plane -- checked on the device (a mismatch
+ * is JFA_ERR_BAD_OFFSETS and no attention is computed).  Added after scaling, like kind 1.
+ * It gets no gradient (`grad` must be NULL). */
 typedef struct {
   int kind;
   const float* table;
   int num_buckets;
   int center;
   float* grad;
+  const void* values;            /* kind 2 */
+  const int64_t* block_offsets;  /* kind 2 */
+  int64_t plane;                 /* kind 2 */
 } jfa_bias;
 
 /* Bytes of workspace jfa_forward (is_backward = 0) or jfa_backward (is_backward = 1)

@@ -128,7 +128,12 @@ jfa_status check_common(int B, int H, int d, int64_t total_q, int64_t total_kv, 
   if (!q_off || !kv_off) return JFA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return JFA_ERR_UNSUPPORTED;
   if ((total_q + 1) * int64_t(H) * d > (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
-  if (bias && bias->kind != 0) {
+  if (bias && bias->kind == 2) {
+    if (bias->grad) return JFA_ERR_UNSUPPORTED;
+    if (!bias->values || !bias->block_offsets || bias->plane < 0 || !aligned16(bias->values) ||
+        (reinterpret_cast<uintptr_t>(bias->block_offsets) & 7u) != 0)
+      return JFA_ERR_INVALID_ARG;
+  } else if (bias && bias->kind != 0) {
     if (bias->kind != 1) return JFA_ERR_UNSUPPORTED;
     if (!bias->table || bias->num_buckets < 1 || bias->num_buckets > kMaxBuckets) return JFA_ERR_INVALID_ARG;
     if (!aligned16(bias->table)) return JFA_ERR_INVALID_ARG;
@@ -154,6 +159,10 @@ Problem make_problem(int B, int H, int d, int64_t total_q, int64_t total_kv, con
   p.num_buckets = has_bias ? bias->num_buckets : 0;
   p.center = has_bias ? bias->center : 0;
   p.bias_grad = has_bias ? bias->grad : nullptr;
+  const bool has_jbias = bias && bias->kind == 2;
+  p.jbias = has_jbias ? bias->values : nullptr;
+  p.jb_off = has_jbias ? bias->block_offsets : nullptr;
+  p.jb_plane = has_jbias ? bias->plane : 0;
   std::lock_guard<std::mutex> g(g_trace_mu);
   for (int k = 0; k < JFA_NUM_KERNEL_KINDS; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
   return p;

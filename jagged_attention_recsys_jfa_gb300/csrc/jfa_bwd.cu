@@ -47,6 +47,9 @@ struct BwdParams {
   const float* bias2;  // [H][num_buckets] bias * log2(e), or nullptr
   float* bias_grad;    // [H][num_buckets] gradient of the bias table (cleared by the planner), or nullptr
   int num_buckets, center;
+  const __nv_bfloat16* jbias;  // general jagged bias [H][jb_plane], or nullptr
+  const int64_t* jb_off;       // its block offsets [B+1]
+  int64_t jb_plane;
   const CUtensorMap* maps;
   const WorkItem* items;
   const int* n_items;
@@ -389,7 +392,7 @@ __device__ __forceinline__ void drain_acc_rows(uint32_t taddr, float mul, __nv_b
 // tile: dO_i is released after dV(i) and Q_i after dK(i), i.e. in fill order.  Each Q_i
 // brings its tile's lse2 and D vectors (vector slot = query tile count mod kVecSlots; a
 // slot is refilled only after dK of its previous tile completed).
-template <int D, bool kBias>
+template <int D, bool kBias, bool kJBias = false>
 __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingDkdv;
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     }
    } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, p.jb_off, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else if (warp < kFirstEpilogueWarp) {
@@ -712,7 +715,14 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         float x[64];
         ld_cols64(tS, x);
         const int i0 = qt * kBM + 64 * w;  // local query index of column 0 of this half
-        if (kBias) {
+        if (kJBias) {
+          const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+          jbias_add_col<64>(x, j < Lk ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i0) * pitch + j : nullptr,
+                            pitch, Lq - i0, sl2, kLog2e);
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
+        } else if (kBias) {
           const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
           if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
 #pragma unroll
@@ -838,7 +848,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
 // Ring of single tiles, filled V_j, K_j per key tile: V_j is released after dP(j), K_j
 // after dQ(j), i.e. in fill order.  S and dP of the next key tile are issued as soon as
 // the warpgroups hold S in registers, so the dP/dS buffer alternates by tile parity.
-template <int D, bool kBias>
+template <int D, bool kBias, bool kJBias = false>
 __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingDq;
@@ -1093,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     }
    } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, p.jb_off, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else {
@@ -1143,7 +1153,14 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
         const int j0 = jt * kBN + 64 * w;  // local key index of column 0 of this half
         const int n_real = Lk - j0;        // columns >= n_real are past the sequence end
-        if (kBias) {
+        if (kJBias) {
+          const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+          jbias_add_row<64>(x, valid ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + j0 : nullptr,
+                            min(64, n_real), sl2, kLog2e);
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_nl2), x[2 * c2], x[2 * c2 + 1]);
+        } else if (kBias) {
           const int idx0 = j0 - i + p.center;
           if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
 #pragma unroll
@@ -1229,7 +1246,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
 //   dQ += dS K_j (SS, dS^T read as an MN-major A)   (accumulated in TMEM, stored at the end)
 // so K and V are read once instead of once per pass, still without atomics.  Key tiles
 // the query tile cannot see (causal) get zero dK / dV rows and no MMAs.
-template <int D, bool kBias>
+template <int D, bool kBias, bool kJBias = false>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingFused;
@@ -1464,7 +1481,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     }
    } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, p.jb_off, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
   } else {
@@ -1512,7 +1529,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       float x[64];
       ld_cols64(tS, x);
       const int i0 = 64 * w;  // query of column 0 of this half
-      if (kBias) {
+      if (kJBias) {
+        const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+        jbias_add_col<64>(x, valid ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i0) * pitch + j : nullptr,
+                          pitch, Lq - i0, sl2, kLog2e);
+#pragma unroll
+        for (int c2 = 0; c2 < 32; ++c2)
+          f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2v[c2]), x[2 * c2], x[2 * c2 + 1]);
+      } else if (kBias) {
         const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -1655,6 +1679,9 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.bias_grad = (pr.bias_table && pass != kPassDq) ? pr.bias_grad : nullptr;
   bp.num_buckets = pr.num_buckets;
   bp.center = pr.center;
+  bp.jbias = static_cast<const __nv_bfloat16*>(pr.jbias);
+  bp.jb_off = pr.jb_off;
+  bp.jb_plane = pr.jb_plane;
   bp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
   bp.items = reinterpret_cast<const WorkItem*>(w + (pass == kPassDq ? L.dq : pass == kPassFused ? L.fused : L.dkv));
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);
@@ -1729,12 +1756,14 @@ cudaError_t launch_bwd_dkdv(const Problem& pr, const float* lse, void* ws, const
   BwdParams bp = make_params(pr, lse, ws, L, kPassDkdv);
   bp.g0 = static_cast<__nv_bfloat16*>(dk);
   bp.g1 = static_cast<__nv_bfloat16*>(dv);
-  const bool bias = pr.bias_table != nullptr;
+  const bool bias = pr.bias_table != nullptr, jb = pr.jbias != nullptr;
   if (pr.d == 128)
     return bias ? launch_dkdv_k(dkdv_kernel<128, true>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream)
-                : launch_dkdv_k(dkdv_kernel<128, false>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream);
+                : jb ? launch_dkdv_k(dkdv_kernel<128, false, true>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream)
+                     : launch_dkdv_k(dkdv_kernel<128, false>, BwdCfg<128>::kSmemDkdv, num_sms, bp, stream);
   return bias ? launch_dkdv_k(dkdv_kernel<64, true>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream)
-              : launch_dkdv_k(dkdv_kernel<64, false>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream);
+              : jb ? launch_dkdv_k(dkdv_kernel<64, false, true>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream)
+                   : launch_dkdv_k(dkdv_kernel<64, false>, BwdCfg<64>::kSmemDkdv, num_sms, bp, stream);
 }
 
 cudaError_t launch_bwd_fused(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,
@@ -1743,24 +1772,28 @@ cudaError_t launch_bwd_fused(const Problem& pr, const float* lse, void* ws, cons
   bp.g0 = static_cast<__nv_bfloat16*>(dk);
   bp.g1 = static_cast<__nv_bfloat16*>(dv);
   bp.g2 = static_cast<__nv_bfloat16*>(dq);
-  const bool bias = pr.bias_table != nullptr;
+  const bool bias = pr.bias_table != nullptr, jb = pr.jbias != nullptr;
   if (pr.d == 128)
     return bias ? launch_big(fused_kernel<128, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
-                : launch_big(fused_kernel<128, false>, BwdCfg<128>::kSmemFused, num_sms, bp, stream);
+                : jb ? launch_big(fused_kernel<128, false, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
+                     : launch_big(fused_kernel<128, false>, BwdCfg<128>::kSmemFused, num_sms, bp, stream);
   return bias ? launch_big(fused_kernel<64, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
-              : launch_big(fused_kernel<64, false>, BwdCfg<64>::kSmemFused, num_sms, bp, stream);
+              : jb ? launch_big(fused_kernel<64, false, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
+                   : launch_big(fused_kernel<64, false>, BwdCfg<64>::kSmemFused, num_sms, bp, stream);
 }
 
 cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, int num_sms,
                           cudaStream_t stream) {
   BwdParams bp = make_params(pr, lse, ws, L, kPassDq);
   bp.g0 = static_cast<__nv_bfloat16*>(dq);
-  const bool bias = pr.bias_table != nullptr;
+  const bool bias = pr.bias_table != nullptr, jb = pr.jbias != nullptr;
   if (pr.d == 128)
     return bias ? launch_big(dq_kernel<128, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
-                : launch_big(dq_kernel<128, false>, BwdCfg<128>::kSmemDq, num_sms, bp, stream);
+                : jb ? launch_big(dq_kernel<128, false, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
+                     : launch_big(dq_kernel<128, false>, BwdCfg<128>::kSmemDq, num_sms, bp, stream);
   return bias ? launch_big(dq_kernel<64, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
-              : launch_big(dq_kernel<64, false>, BwdCfg<64>::kSmemDq, num_sms, bp, stream);
+              : jb ? launch_big(dq_kernel<64, false, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
+                   : launch_big(dq_kernel<64, false>, BwdCfg<64>::kSmemDq, num_sms, bp, stream);
 }
 
 }  // namespace jfa

@@ -48,6 +48,9 @@ struct FwdParams {
   int causal;
   const float* bias2;    // [H][num_buckets] bias * log2(e), or nullptr
   int num_buckets, center;
+  const __nv_bfloat16* jbias;  // general jagged bias [H][jb_plane], or nullptr
+  const int64_t* jb_off;       // its block offsets [B+1]
+  int64_t jb_plane;
   const CUtensorMap* maps;  // [B][kNumMapSlots]
   const WorkItem* items;
   const int* n_items;
@@ -71,6 +74,7 @@ struct FwdCfg {
 struct ItemInfo {
   int b, h, t0, t1;
   int64_t qo, ko;
+  int64_t jb;  // general jagged bias: the sequence's block offset
   int Lq, Lk;
   int nkv0, nkv1, njt;
   bool has1;
@@ -84,6 +88,7 @@ __device__ __forceinline__ ItemInfo decode(const FwdParams& p, const ItemMeta& i
   r.t0 = 2 * u;
   r.t1 = r.t0 + 1;
   r.qo = it.qo;
+  r.jb = it.jb;
   r.ko = it.ko;
   r.Lq = it.Lq;
   r.Lk = it.Lk;
@@ -104,7 +109,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D, bool kBias>
+template <int D, bool kBias, bool kJBias = false>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, nullptr, abort_flag))
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, nullptr, p.jb_off, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
   }
   } else {
@@ -436,6 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         }
         const int kv0 = j * kBN;
         const bool last = (j == nkv - 1);
+        if (kJBias) {
+          // x = scale*log2e * (q.k) + bias*log2e from this row of the sequence's block
+          const int64_t pitch = (it.Lk + 7) / 8 * 8;
+          const __nv_bfloat16* src =
+              valid_row ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + kv0 : nullptr;
+          jbias_add_row<128>(x, src, min(kBN, it.Lk - kv0), sl2, kLog2e);
+        }
         if (kBias) {
           // x = scale*log2e * (q.k) + bias*log2e, bias only on real key columns
           const int n_real = min(kBN, it.Lk - kv0);
@@ -472,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           mx4[k] = m0;
         }
         const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_tile = kBias ? mx : mx * sl2;
+        const float m_tile = (kBias || kJBias) ? mx : mx * sl2;
         // raise the reference max only when it grows by more than 2^8
         const bool need = m_tile > m + kRescaleThreshold;
         const float m_new = need ? m_tile : m;
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
 #pragma unroll
           for (int t2 = 0; t2 < 64; ++t2) {
             const uint64_t xx = f2_pack(x[2 * t2], x[2 * t2 + 1]);
-            const uint64_t arg = kBias ? f2_add(xx, k_negm) : f2_fma(xx, k_scale, k_negm);
+            const uint64_t arg = (kBias || kJBias) ? f2_add(xx, k_negm) : f2_fma(xx, k_scale, k_negm);
             float a, b;
             f2_unpack(arg, a, b);
             const float pa = ex2_approx(a), pb = ex2_approx(b);
@@ -568,10 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int D, bool kBias>
+template <int D, bool kBias, bool kJBias = false>
 cudaError_t launch_fwd_t(const FwdParams& fp, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, kBias>;
+  auto kern = fwd_kernel<D, kBias, kJBias>;
   cudaError_t e = check_launch_registers(kern);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -596,6 +608,9 @@ cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void*
   fp.bias2 = pr.bias_table ? reinterpret_cast<const float*>(w + L.bias2) : nullptr;
   fp.num_buckets = pr.num_buckets;
   fp.center = pr.center;
+  fp.jbias = static_cast<const __nv_bfloat16*>(pr.jbias);
+  fp.jb_off = pr.jb_off;
+  fp.jb_plane = pr.jb_plane;
   fp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
   fp.items = reinterpret_cast<const WorkItem*>(w + L.fwd);
   fp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_fwd;
@@ -606,8 +621,12 @@ cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void*
   fp.trace = pr.trace[JFA_KERNEL_FORWARD];
   const int grid = num_sms;
   const bool bias = pr.bias_table != nullptr;
-  if (pr.d == 128) return bias ? launch_fwd_t<128, true>(fp, grid, stream) : launch_fwd_t<128, false>(fp, grid, stream);
-  return bias ? launch_fwd_t<64, true>(fp, grid, stream) : launch_fwd_t<64, false>(fp, grid, stream);
+  const bool jb = pr.jbias != nullptr;
+  if (pr.d == 128)
+    return bias ? launch_fwd_t<128, true>(fp, grid, stream)
+                : (jb ? launch_fwd_t<128, false, true>(fp, grid, stream) : launch_fwd_t<128, false>(fp, grid, stream));
+  return bias ? launch_fwd_t<64, true>(fp, grid, stream)
+              : (jb ? launch_fwd_t<64, false, true>(fp, grid, stream) : launch_fwd_t<64, false>(fp, grid, stream));
 }
 
 }  // namespace jfa

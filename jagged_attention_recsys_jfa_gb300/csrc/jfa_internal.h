@@ -17,6 +17,9 @@ struct Problem {
   const float* bias_table;  // nullptr = no bias
   int num_buckets, center;
   float* bias_grad;         // [H][num_buckets] fp32 gradient of the bias table (backward), or nullptr
+  const void* jbias;        // general jagged bias: bf16 [H][jb_plane], or nullptr
+  const int64_t* jb_off;    // its block offsets [B+1]
+  int64_t jb_plane;
   TraceBuf trace[JFA_NUM_KERNEL_KINDS];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
 };
 

@@ -24,6 +24,8 @@ struct PlanParams {
   const float* bias;  // [H][nb] or nullptr
   float* bias_grad;   // [H][nb] gradient table to clear before the backward passes add into it, or nullptr
   int nb;
+  const int64_t* jb_off;  // general jagged bias block offsets [B+1], or nullptr
+  int64_t jb_plane;
 };
 
 enum ListKind { kListFwd = 0, kListDq = 1, kListDkv = 2, kListFused = 3 };
@@ -262,10 +264,13 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     const int64_t lq = p.q_off[b + 1] - p.q_off[b];
     const int64_t lk = p.kv_off[b + 1] - p.kv_off[b];
     if (lq < 0 || lk < 0 || lq > (int64_t(1) << 30) || lk > (int64_t(1) << 30)) bad = 1;
+    // a general bias's blocks must hold exactly Lq x round_up(Lk, 8) elements each
+    if (p.jb_off && !bad && p.jb_off[b + 1] - p.jb_off[b] != lq * ((lk + 7) / 8 * 8)) bad = 1;
   }
   if (tid == 0) {
     if (p.q_off[0] != 0 || p.kv_off[0] != 0 || p.q_off[p.B] != p.total_q || p.kv_off[p.B] != p.total_kv)
       bad = 1;
+    if (p.jb_off && (p.jb_off[0] != 0 || p.jb_off[p.B] != p.jb_plane)) bad = 1;
   }
   if (blockIdx.x == 0 && tid == 0) hdr->claim_fwd = hdr->claim_dq = hdr->claim_dkv = hdr->claim_fused = 0;
   bad = __syncthreads_or(bad);
@@ -330,6 +335,8 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   p.L = L;
   p.bias = pr.bias_table;
   p.bias_grad = backward ? pr.bias_grad : nullptr;
+  p.jb_off = pr.jb_off;
+  p.jb_plane = pr.jb_plane;
   p.nb = pr.num_buckets;
   // one CTA per list; helpers for the maps (one thread each), tail copies and bias table
   const long long map_ctas = (static_cast<long long>(pr.B) * kNumMapSlots + 1023) / 1024;

@@ -21,6 +21,7 @@ struct ItemMeta {
   int64_t qo, ko;     // first query / key row of the sequence
   int Lq, Lk;         // its lengths
   int64_t qp;         // backward: first row of the sequence in the 128-row-padded vectors
+  int64_t jb;         // general jagged bias: the sequence's block offset in each head's plane
 };
 
 struct MetaRing {
@@ -44,7 +45,7 @@ __device__ __forceinline__ void meta_init(MetaRing& r, int consumers = kMetaCons
 // out (the CTA is aborting).
 __device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items, int n_items, int* claim,
                                              const int64_t* q_off, const int64_t* kv_off, const int64_t* qpad,
-                                             volatile int* abort) {
+                                             const int64_t* jb_off, volatile int* abort) {
   for (uint32_t k = 0;; ++k) {
     if (k >= 2) {
       const uint32_t kp = k - 2;
@@ -63,8 +64,9 @@ __device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items,
       m.Lq = int(q_off[wi.b + 1] - m.qo);
       m.Lk = int(kv_off[wi.b + 1] - m.ko);
       m.qp = qpad ? qpad[wi.b] : 0;
+      m.jb = jb_off ? jb_off[wi.b] : 0;
     } else {
-      m = ItemMeta{-1, 0, 0, 0, 0, 0, 0, 0, 0};
+      m = ItemMeta{-1, 0, 0, 0, 0, 0, 0, 0, 0, 0};
     }
     const uint32_t s = k % kMetaSlots;
     r.e[s] = m;

@@ -371,6 +371,43 @@ __device__ __forceinline__ void st_rows_coalesced(uint4 (&c)[NB / 16], void* dst
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// General jagged bias on one query row: x[c] = x[c] * sl2 + l2e * bias[c] for the N columns
+// c < n_real (keys of the sequence), x[c] * sl2 past them.  `src` is the row's first
+// column (bf16, 16-byte aligned; the row is padded to a multiple of 8 elements, so every
+// 8-column chunk that starts before n_real lies inside it), or nullptr for no bias.
+template <int N>
+__device__ __forceinline__ void jbias_add_row(float* x, const void* src, int n_real, float sl2, float l2e) {
+  const uint64_t k_sl2 = f2_pack(sl2, sl2), k_l2e = f2_pack(l2e, l2e);
+#pragma unroll
+  for (int c8 = 0; c8 < N / 8; ++c8) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (src != nullptr && 8 * c8 < n_real) w = __ldg(reinterpret_cast<const uint4*>(src) + c8);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 8 * c8 + 2 * e;
+      const float b0 = c < n_real ? bf16lo(wv[e]) : 0.f;
+      const float b1 = c + 1 < n_real ? bf16hi(wv[e]) : 0.f;
+      f2_unpack(f2_fma(f2_pack(b0, b1), k_l2e, f2_mul(f2_pack(x[c], x[c + 1]), k_sl2)), x[c], x[c + 1]);
+    }
+  }
+}
+
+// General jagged bias on one key row against N query rows: x[c] = x[c] * sl2 + l2e *
+// bias[i0 + c][j], read at col[c * pitch] (bf16), for the query rows c < n_q; the lanes of
+// a warp hold consecutive keys, so each load instruction reads consecutive elements of one
+// query row.  `col` nullptr (a key past the sequence end) adds no bias.
+template <int N>
+__device__ __forceinline__ void jbias_add_col(float* x, const void* col, int64_t pitch, int n_q, float sl2,
+                                              float l2e) {
+  const uint16_t* c16 = reinterpret_cast<const uint16_t*>(col);
+#pragma unroll
+  for (int c = 0; c < N; ++c) {
+    const float b = (col != nullptr && c < n_q) ? __uint_as_float(uint32_t(__ldg(c16 + c * pitch)) << 16) : 0.f;
+    x[c] = fmaf(b, l2e, x[c] * sl2);
+  }
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -63,6 +63,10 @@ CONFIGS = {
                                   causal=True, bias_buckets=4096, bias_center=2048),
     "longtail_causal": JaggedConfig("longtail_causal", 64, 8, 128,
                                     ("lognormal", 512.0, 1.2, 16, 16384), causal=True),
+    # the biased_causal shape with a general jagged bias (one Lq x Lk block per sequence
+    # and head) in place of the relative-position table
+    "jagged_bias_causal": JaggedConfig("jagged_bias_causal", 128, 4, 64, ("uniform", 1, 2048),
+                                       causal=True, general_bias=True),
 }
 
 

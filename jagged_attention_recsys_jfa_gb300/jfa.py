@@ -41,7 +41,8 @@ class JfaError(RuntimeError):
 
 class _Bias(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("num_buckets", ctypes.c_int),
-                ("center", ctypes.c_int), ("grad", ctypes.c_void_p)]
+                ("center", ctypes.c_int), ("grad", ctypes.c_void_p), ("values", ctypes.c_void_p),
+                ("block_offsets", ctypes.c_void_p), ("plane", ctypes.c_int64)]
 
 
 _LIB = None
@@ -125,7 +126,16 @@ def _check_offsets(name, off):
         raise ValueError(f"{name} must be a contiguous int64 CUDA tensor [B+1] with B >= 1")
 
 
-def _bias_struct(bias, center, H, grad=None):
+def _bias_struct(bias, center, H, grad=None, jagged_bias=None):
+    if jagged_bias is not None:
+        if bias is not None or grad is not None:
+            raise ValueError("a general jagged bias excludes the relative-position table and its gradient")
+        values, boff = jagged_bias
+        if (not values.is_cuda or values.dtype != torch.bfloat16 or values.dim() != 2 or values.shape[0] != H
+                or not values.is_contiguous()):
+            raise ValueError("jagged bias values must be a contiguous bf16 CUDA tensor [H, plane]")
+        _check_offsets("jagged bias block offsets", boff)
+        return _Bias(2, None, 0, 0, None, values.data_ptr(), boff.data_ptr(), values.shape[1]), (values, boff)
     if bias is None:
         if grad is not None:
             raise ValueError("bias_grad needs a bias table")
@@ -158,11 +168,13 @@ def _workspace(nbytes, device):
 
 
 def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,
-                out=None, lse=None, workspace=None, stream=None):
+                out=None, lse=None, workspace=None, stream=None, jagged_bias=None):
     """out, lse = jfa_forward(...): the C-ABI forward on PyTorch-allocated device memory.
 
     q: bf16 [Tq, H, d]; k, v: bf16 [Tk, H, d]; offsets: int64 [B+1] on the device.
     bias: optional fp32 [H, num_buckets] relative-position table (bucket j - i + bias_center).
+    jagged_bias: optional (values bf16 [H, plane], block offsets int64 [B+1]): a general
+    bias, one Lq x Lk block per sequence with rows padded to 8 elements (see jfa.h).
     Returns out bf16 [Tq, H, d] and lse fp32 [H, Tq].  The call is asynchronous on
     the current stream; device-side errors are reported by jfa_check_status(workspace).
     """
@@ -177,7 +189,7 @@ def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=
     if kv_offsets.numel() != B + 1:
         raise ValueError("q_offsets and kv_offsets must have the same length")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    bstruct, bias_keep = _bias_struct(bias, bias_center, H)
+    bstruct, bias_keep = _bias_struct(bias, bias_center, H, jagged_bias=jagged_bias)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -196,7 +208,8 @@ def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=
 
 
 def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None,
-                 causal=False, dq=None, dk=None, dv=None, workspace=None, stream=None, bias_grad=None):
+                 causal=False, dq=None, dk=None, dv=None, workspace=None, stream=None, bias_grad=None,
+                 jagged_bias=None):
     """dq, dk, dv, workspace = jfa_backward(...): gradients of sum(dout * out).  With
     `bias_grad` (a float32 tensor shaped like `bias`) the bias table's gradient is written
     into it as well."""
@@ -211,7 +224,7 @@ def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias
     _check_offsets("kv_offsets", kv_offsets)
     B = q_offsets.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    bstruct, bias_keep = _bias_struct(bias, bias_center, H, bias_grad)
+    bstruct, bias_keep = _bias_struct(bias, bias_center, H, bias_grad, jagged_bias)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -281,25 +294,32 @@ def decode_trace(buffer: torch.Tensor):
 
 class JaggedAttention(torch.autograd.Function):
     """Differentiable jagged attention: out = JaggedAttention.apply(q, k, v, q_offsets,
-    kv_offsets, bias, bias_center, scale, causal).  lse is saved for the backward; the
-    bias table gets its gradient when it requires one."""
+    kv_offsets, bias, bias_center, scale, causal, jagged_bias_values, jagged_bias_offsets).
+    lse is saved for the backward; the relative-position table gets its gradient when it
+    requires one; a general jagged bias gets none."""
 
     @staticmethod
-    def forward(ctx, q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False):
-        out, lse, _ = jfa_forward(q, k, v, q_offsets, kv_offsets, bias, bias_center, scale, causal)
-        ctx.save_for_backward(q, k, v, out, lse, q_offsets, kv_offsets, bias)
+    def forward(ctx, q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,
+                jb_values=None, jb_offsets=None):
+        jb = (jb_values, jb_offsets) if jb_values is not None else None
+        out, lse, _ = jfa_forward(q, k, v, q_offsets, kv_offsets, bias, bias_center, scale, causal, jagged_bias=jb)
+        ctx.save_for_backward(q, k, v, out, lse, q_offsets, kv_offsets, bias, jb_values, jb_offsets)
         ctx.cfg = (bias_center, scale, causal)
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        q, k, v, out, lse, q_offsets, kv_offsets, bias = ctx.saved_tensors
+        q, k, v, out, lse, q_offsets, kv_offsets, bias, jb_values, jb_offsets = ctx.saved_tensors
         bias_center, scale, causal = ctx.cfg
+        jb = (jb_values, jb_offsets) if jb_values is not None else None
         dbias = torch.empty_like(bias) if bias is not None and ctx.needs_input_grad[5] else None
         dq, dk, dv, _ = jfa_backward(dout.contiguous(), q, k, v, out, lse, q_offsets, kv_offsets, bias,
-                                     bias_center, scale, causal, bias_grad=dbias)
-        return dq, dk, dv, None, None, dbias, None, None, None
+                                     bias_center, scale, causal, bias_grad=dbias, jagged_bias=jb)
+        return dq, dk, dv, None, None, dbias, None, None, None, None, None
 
 
-def jagged_attention(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False):
-    return JaggedAttention.apply(q, k, v, q_offsets, kv_offsets, bias, bias_center, scale, causal)
+def jagged_attention(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,
+                     jagged_bias=None):
+    jb_values, jb_offsets = jagged_bias if jagged_bias is not None else (None, None)
+    return JaggedAttention.apply(q, k, v, q_offsets, kv_offsets, bias, bias_center, scale, causal, jb_values,
+                                 jb_offsets)

@@ -19,14 +19,15 @@ GRAD_RTOL = 2e-2
 def gpu_run(batch, backward=True):
     cfg = batch.cfg
     center = cfg.bias_center if batch.bias is not None else 0
+    jb = (batch.jbias, batch.jbias_offsets) if batch.jbias is not None else None
     out, lse, ws = jfa_forward(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, batch.bias, center,
-                               cfg.scale, cfg.causal)
+                               cfg.scale, cfg.causal, jagged_bias=jb)
     st = jfa_check_status(ws)
     assert st == 0, f"forward device status {st}"
     res = {"out": out, "lse": lse}
     if backward:
         dq, dk, dv, ws2 = jfa_backward(batch.dout, batch.q, batch.k, batch.v, out, lse, batch.q_offsets,
-                                       batch.kv_offsets, batch.bias, center, cfg.scale, cfg.causal)
+                                       batch.kv_offsets, batch.bias, center, cfg.scale, cfg.causal, jagged_bias=jb)
         st = jfa_check_status(ws2)
         assert st == 0, f"backward device status {st}"
         res.update(dq=dq, dk=dk, dv=dv)
@@ -37,7 +38,8 @@ def gpu_run(batch, backward=True):
 def oracle_full(batch, backward=True):
     cfg = batch.cfg
     kw = dict(scale=cfg.scale, causal=cfg.causal, bias_table=batch.bias,
-              bias_center=cfg.bias_center if batch.bias is not None else 0)
+              bias_center=cfg.bias_center if batch.bias is not None else 0,
+              jagged_bias=(batch.jbias, batch.jbias_offsets) if batch.jbias is not None else None)
     out, lse = orc.jagged_forward(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, **kw)
     res = {"out": out, "lse": lse}
     if backward:
