@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ MetaRing meta;
+  __shared__ uint4 jb_scratch[kJBias ? 8 * 128 : 1];  // general bias: 2 KB transpose scratch per compute warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -701,6 +702,13 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       for (int i = 0; i < count && ok; ++i) {
         const int qt = first + i;
+        uint4 jbw[8];  // general bias for this tile (row order), loaded before the waits
+        if (kJBias) {
+          const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+          const int qi0 = qt * kBM + 64 * w, kj0 = kt * kBN + quarter * 32;
+          jbias_load_cols_vec(jbw, p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(qi0) * pitch + kj0, pitch,
+                              Lq - qi0, Lk - kj0, lane);
+        }
         // Q_i's ring slot carries this tile's lse2 / D vectors: wait for it
         const uint32_t nq = ring_n + 1;
         if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
@@ -716,9 +724,9 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         ld_cols64(tS, x);
         const int i0 = qt * kBM + 64 * w;  // local query index of column 0 of this half
         if (kJBias) {
-          const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
-          jbias_add_col<64>(x, j < Lk ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i0) * pitch + j : nullptr,
-                            pitch, Lq - i0, sl2, kLog2e);
+          uint32_t jbk[32];
+          jbias_col_transpose(jbk, jbw, jb_scratch + (warp - kFirstComputeWarp) * 128, j < Lk, lane);
+          jbias_apply<64>(x, jbk, sl2, kLog2e);
 #pragma unroll
           for (int c2 = 0; c2 < 32; ++c2)
             f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
@@ -1143,6 +1151,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       const int diag = Lk - Lq;
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       for (int jt = 0; jt < nkv && ok; ++jt) {
+        uint32_t jbk[kJBias ? 32 : 1];  // general bias for this tile, loaded before the wait
+        if (kJBias) {
+          const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+          const int jj0 = jt * kBN + 64 * w;
+          jbias_load_row<64>(jbk, valid ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + jj0 : nullptr,
+                             min(64, Lk - jj0));
+        }
         if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
@@ -1154,9 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         const int j0 = jt * kBN + 64 * w;  // local key index of column 0 of this half
         const int n_real = Lk - j0;        // columns >= n_real are past the sequence end
         if (kJBias) {
-          const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
-          jbias_add_row<64>(x, valid ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + j0 : nullptr,
-                            min(64, n_real), sl2, kLog2e);
+          jbias_apply<64>(x, jbk, sl2, kLog2e);
 #pragma unroll
           for (int c2 = 0; c2 < 32; ++c2)
             f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_nl2), x[2 * c2], x[2 * c2 + 1]);
@@ -1264,6 +1277,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ MetaRing meta;
+  __shared__ uint4 jb_scratch[kJBias ? 8 * 128 : 1];  // general bias: 2 KB transpose scratch per compute warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -1522,6 +1536,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
         store_acc_row_own<D / 2>(0, 0.f, dv_row, valid, true);
         continue;
       }
+      uint4 jbw[8];  // general bias for this tile (row order), loaded before the wait
+      if (kJBias) {
+        const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+        const int kj0 = kt * kBN + quarter * 32;
+        jbias_load_cols_vec(jbw, p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(64 * w) * pitch + kj0, pitch,
+                            Lq - 64 * w, Lk - kj0, lane);
+      }
       // ---- P^T = exp2(S^T * scale * log2e (+ bias) - lse2), 0 on padding and hidden pairs
       if (!mbar_wait(&st_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
@@ -1530,9 +1551,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       ld_cols64(tS, x);
       const int i0 = 64 * w;  // query of column 0 of this half
       if (kJBias) {
-        const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
-        jbias_add_col<64>(x, valid ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i0) * pitch + j : nullptr,
-                          pitch, Lq - i0, sl2, kLog2e);
+        uint32_t jbk[32];
+        jbias_col_transpose(jbk, jbw, jb_scratch + (warp - kFirstComputeWarp) * 128, valid, lane);
+        jbias_apply<64>(x, jbk, sl2, kLog2e);
 #pragma unroll
         for (int c2 = 0; c2 < 32; ++c2)
           f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2v[c2]), x[2 * c2], x[2 * c2 + 1]);

@@ -418,6 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkv; ++j) {
+        uint32_t jbk[kJBias ? 64 : 1];  // general bias for this tile, loaded before the wait
+        if (kJBias) {
+          const int64_t pitch = (it.Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
+          const int kvj = j * kBN;
+          jbias_load_row<128>(jbk, valid_row ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + kvj
+                                             : nullptr,
+                              min(kBN, it.Lk - kvj));
+        }
         if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++s_n;
         tc_fence_after();
@@ -443,10 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         const bool last = (j == nkv - 1);
         if (kJBias) {
           // x = scale*log2e * (q.k) + bias*log2e from this row of the sequence's block
-          const int64_t pitch = (it.Lk + 7) / 8 * 8;
-          const __nv_bfloat16* src =
-              valid_row ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + kv0 : nullptr;
-          jbias_add_row<128>(x, src, min(kBN, it.Lk - kv0), sl2, kLog2e);
+          jbias_apply<128>(x, jbk, sl2, kLog2e);
         }
         if (kBias) {
           // x = scale*log2e * (q.k) + bias*log2e, bias only on real key columns

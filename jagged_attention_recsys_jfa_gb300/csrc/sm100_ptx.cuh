@@ -371,41 +371,94 @@ __device__ __forceinline__ void st_rows_coalesced(uint4 (&c)[NB / 16], void* dst
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-// General jagged bias on one query row: x[c] = x[c] * sl2 + l2e * bias[c] for the N columns
-// c < n_real (keys of the sequence), x[c] * sl2 past them.  `src` is the row's first
-// column (bf16, 16-byte aligned; the row is padded to a multiple of 8 elements, so every
-// 8-column chunk that starts before n_real lies inside it), or nullptr for no bias.
+// General jagged bias, split into loads and arithmetic so the loads can be issued before
+// the wait for the scores they apply to.  Values are kept as packed bf16 pairs (0 where no
+// bias applies).
+//
+// One query row: N columns from `src` (bf16, 16-byte aligned; the row is padded to a
+// multiple of 8 elements, so every 8-column chunk that starts before n_real lies inside
+// it); columns c >= n_real (keys past the sequence end) get 0.  src nullptr: all 0.
 template <int N>
-__device__ __forceinline__ void jbias_add_row(float* x, const void* src, int n_real, float sl2, float l2e) {
-  const uint64_t k_sl2 = f2_pack(sl2, sl2), k_l2e = f2_pack(l2e, l2e);
+__device__ __forceinline__ void jbias_load_row(uint32_t* pk, const void* src, int n_real) {
 #pragma unroll
   for (int c8 = 0; c8 < N / 8; ++c8) {
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if (src != nullptr && 8 * c8 < n_real) w = __ldg(reinterpret_cast<const uint4*>(src) + c8);
-    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    pk[4 * c8 + 0] = w.x;
+    pk[4 * c8 + 1] = w.y;
+    pk[4 * c8 + 2] = w.z;
+    pk[4 * c8 + 3] = w.w;
+  }
+  if (n_real < N) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = 8 * c8 + 2 * e;
-      const float b0 = c < n_real ? bf16lo(wv[e]) : 0.f;
-      const float b1 = c + 1 < n_real ? bf16hi(wv[e]) : 0.f;
-      f2_unpack(f2_fma(f2_pack(b0, b1), k_l2e, f2_mul(f2_pack(x[c], x[c + 1]), k_sl2)), x[c], x[c + 1]);
+    for (int c2 = 0; c2 < N / 2; ++c2) {
+      if (2 * c2 >= n_real) pk[c2] = 0u;
+      else if (2 * c2 + 1 >= n_real) pk[c2] &= 0xffffu;
     }
   }
 }
 
-// General jagged bias on one key row against N query rows: x[c] = x[c] * sl2 + l2e *
-// bias[i0 + c][j], read at col[c * pitch] (bf16), for the query rows c < n_q; the lanes of
-// a warp hold consecutive keys, so each load instruction reads consecutive elements of one
-// query row.  `col` nullptr (a key past the sequence end) adds no bias.
+// One key row j against N query rows: bias[i0 + c][j] at col[c * pitch] (bf16); the lanes
+// of a warp hold consecutive keys, so each load instruction reads consecutive elements of
+// one query row.  Query rows c >= n_q get 0; col nullptr (a key past the sequence end): all 0.
 template <int N>
-__device__ __forceinline__ void jbias_add_col(float* x, const void* col, int64_t pitch, int n_q, float sl2,
-                                              float l2e) {
+__device__ __forceinline__ void jbias_load_col(uint32_t* pk, const void* col, int64_t pitch, int n_q) {
   const uint16_t* c16 = reinterpret_cast<const uint16_t*>(col);
 #pragma unroll
-  for (int c = 0; c < N; ++c) {
-    const float b = (col != nullptr && c < n_q) ? __uint_as_float(uint32_t(__ldg(c16 + c * pitch)) << 16) : 0.f;
-    x[c] = fmaf(b, l2e, x[c] * sl2);
+  for (int c2 = 0; c2 < N / 2; ++c2) {
+    const uint32_t lo = (col != nullptr && 2 * c2 < n_q) ? uint32_t(__ldg(c16 + (2 * c2) * pitch)) : 0u;
+    const uint32_t hi = (col != nullptr && 2 * c2 + 1 < n_q) ? uint32_t(__ldg(c16 + (2 * c2 + 1) * pitch)) : 0u;
+    pk[c2] = lo | (hi << 16);
   }
+}
+
+// One warp's 32 consecutive key rows j0 + lane against 64 query rows, loaded with 16-byte
+// loads: in pass p (0, 1) chunk q = lane + 32 k (k < 4) is query row 32 p + q / 4, keys
+// j0 + 8 (q % 4) .. + 7 of the block (`rows` points at query row 0, key j0; rows `pitch`
+// elements apart).  Chunks of query rows >= n_q or starting at a key >= n_k are 0.  The
+// values are in row order; jbias_col_transpose hands each lane its key's column.
+__device__ __forceinline__ void jbias_load_cols_vec(uint4 (&w)[8], const void* rows, int64_t pitch, int n_q, int n_k,
+                                                    int lane) {
+  const uint16_t* r16 = reinterpret_cast<const uint16_t*>(rows);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const int q = lane + 32 * (t & 3), row = 32 * (t >> 2) + q / 4, part = q % 4;
+    w[t] = make_uint4(0u, 0u, 0u, 0u);
+    if (rows != nullptr && row < n_q && 8 * part < n_k)
+      w[t] = __ldg(reinterpret_cast<const uint4*>(r16 + row * pitch + 8 * part));
+  }
+}
+
+// The transpose through a 2 KB per-warp shared scratch (16-byte aligned): each pass writes
+// its 32 rows x 32 keys, then lane l reads key l of every row (consecutive 2-byte elements
+// of one row per instruction: no bank conflicts).  key_valid false (a key past the sequence
+// end, whose padding holds no bias) gives 0.  Packs two query rows per register.
+__device__ __forceinline__ void jbias_col_transpose(uint32_t* pk, const uint4 (&w)[8], uint4* scratch, bool key_valid,
+                                                    int lane) {
+  const uint16_t* s16 = reinterpret_cast<const uint16_t*>(scratch);
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) scratch[lane + 32 * k] = w[4 * pass + k];
+    __syncwarp();
+#pragma unroll
+    for (int r2 = 0; r2 < 16; ++r2) {
+      const uint32_t lo = key_valid ? uint32_t(s16[(2 * r2) * 32 + lane]) : 0u;
+      const uint32_t hi = key_valid ? uint32_t(s16[(2 * r2 + 1) * 32 + lane]) : 0u;
+      pk[16 * pass + r2] = lo | (hi << 16);
+    }
+    __syncwarp();
+  }
+}
+
+// x[c] = x[c] * sl2 + l2e * bias[c] for the N columns, bias from the packed pairs.
+template <int N>
+__device__ __forceinline__ void jbias_apply(float* x, const uint32_t* pk, float sl2, float l2e) {
+  const uint64_t k_sl2 = f2_pack(sl2, sl2), k_l2e = f2_pack(l2e, l2e);
+#pragma unroll
+  for (int c2 = 0; c2 < N / 2; ++c2)
+    f2_unpack(f2_fma(f2_pack(bf16lo(pk[c2]), bf16hi(pk[c2])), k_l2e, f2_mul(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2)),
+              x[2 * c2], x[2 * c2 + 1]);
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
