@@ -6,6 +6,7 @@ benchmark's CPU-baseline leg.  The library never routes through it.
 from .jfa_oracle import (  # noqa: F401
     causal_visible,
     jagged_bias_grad,
+    jagged_general_bias_grad,
     jagged_backward,
     jagged_forward,
     jagged_bias_block,

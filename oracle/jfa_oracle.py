@@ -269,6 +269,29 @@ def jagged_bias_grad(dout, q, k, v, q_offsets, kv_offsets, scale, causal, bias_t
     return g
 
 
+def jagged_general_bias_grad(dout, q, k, v, q_offsets, kv_offsets, scale, causal, jagged_bias):
+    """Gradient of sum(dout * out) w.r.t. a general jagged bias: s_ij depends on its own
+    bias element with slope 1, so the gradient of element (h, b, i, j) is dS_ij of that
+    sequence and head.  Returned in the bias's own layout [H, plane] (row padding 0)."""
+    do, q, k, v = to_f64(dout), to_f64(q), to_f64(k), to_f64(v)
+    Tq, H, d = q.shape
+    qo = check_offsets(q_offsets, Tq)
+    ko = check_offsets(kv_offsets, k.shape[0])
+    jb = _jagged_bias_f64(jagged_bias)
+    g = np.zeros_like(jb[0])
+    for b in range(qo.size - 1):
+        Lq, Lk = int(qo[b + 1] - qo[b]), int(ko[b + 1] - ko[b])
+        pitch = (Lk + 7) // 8 * 8
+        off = int(jb[1][b])
+        for h in range(H):
+            (q0, q1, _, _), qb, kb, vb, bias, vis = _seq_inputs(
+                b, h, q, k, v, qo, ko, scale, causal, None, 0, jb)
+            ds, _ = sequence_score_grad(do[q0:q1, h, :], qb, kb, vb, scale, bias, vis)
+            blk = g[h, off:off + Lq * pitch].reshape(Lq, pitch)
+            blk[:, :Lk] = ds
+    return g
+
+
 def sequence_reference(b, h, q, k, v, q_offsets, kv_offsets, scale, causal=False,
                        bias_table=None, bias_center=0, dout=None, jagged_bias=None):
     """Oracle results for one (sequence, head): (o, lse) and, if dout is given,

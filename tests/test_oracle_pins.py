@@ -282,6 +282,31 @@ def test_jagged_bias_equal_to_relpos_table(causal):
         np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_general_bias_grad_finite_differences(causal):
+    """The general bias's gradient against central differences of sum(dout * out) with
+    respect to every stored element (padding elements have gradient 0)."""
+    rng = np.random.default_rng(13)
+    lq, lk = [3, 0, 4], [5, 2, 4]
+    q, k, v, do, qo, ko, _ = rand_batch(rng, lq, lk, H=2, d=4)
+    H = q.shape[1]
+    vals, off = _pack_jagged_bias([rng.standard_normal((H, a, b)) for a, b in zip(lq, lk)], lq, lk, H)
+    vals = np.nan_to_num(vals, nan=0.0)
+    g = orc.jagged_general_bias_grad(do, q, k, v, qo, ko, 0.6, causal, (vals, off))
+    eps = 1e-6
+    num = np.zeros_like(vals)
+    kw = lambda vv: dict(scale=0.6, causal=causal, jagged_bias=(vv, off))
+    for idx in np.ndindex(*vals.shape):
+        plus, minus = vals.copy(), vals.copy()
+        plus[idx] += eps
+        minus[idx] -= eps
+        num[idx] = (_objective(q, k, v, do, qo, ko, kw(plus)) - _objective(q, k, v, do, qo, ko, kw(minus))) / (2 * eps)
+    rel = np.linalg.norm(num - g) / max(np.linalg.norm(g), 1e-30)
+    assert rel <= 1e-7, rel
+    if causal:   # hidden pairs do not move the output: sequence 0 (3 x 5), row 0 sees keys 0..2
+        assert np.abs(g[:, int(off[0]) + 3:int(off[0]) + 5]).max() == 0.0
+
+
 # --------------------------------------------------------------------------- invariants
 def test_rows_sum_to_one_and_D_identity():
     rng = np.random.default_rng(5)
