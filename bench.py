@@ -9,9 +9,9 @@ pairs the attention visits: fwd 4*d*H*P, bwd 10*d*H*P flops, P = sum_b Lq_b*Lk_b
 the same step through the public call with pinned host buffers copied in and the
 results copied out every step (consecutive steps overlapped: the next step's inputs
 stream in while this one computes and its results stream out).  Workloads with a
-relative-position bias also report `bias_grad`: the backward that writes the bias
-table's gradient as well, timed against the plain backward (the step itself holds the
-bias constant).
+bias (relative-position table or general jagged bias) also report `bias_grad`: the
+backward that writes the bias's gradient as well, timed against the plain backward (the
+step itself holds the bias constant).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl jfa|reference]
 
@@ -423,13 +423,14 @@ def run_jfa(args, rank, world, device):
     # ---- bias-table gradient (workloads with a relative-position bias): the same backward
     # also writing the table's gradient, timed against the plain backward on the same inputs
     bias_grad = None
-    if batch.bias is not None:
-        dbias = torch.empty_like(batch.bias)
+    if batch.bias is not None or batch.jbias is not None:
+        dbias = torch.empty_like(batch.bias) if batch.bias is not None else None
+        djb = torch.empty_like(batch.jbias) if batch.jbias is not None else None
 
         def bwd_g():
             jfa.jfa_backward(batch.dout, batch.q, batch.k, batch.v, out, lse, batch.q_offsets, batch.kv_offsets,
                              batch.bias, center, cfg.scale, cfg.causal, dq=dq, dk=dk, dv=dv, workspace=ws_b,
-                             bias_grad=dbias)
+                             bias_grad=dbias, jagged_bias=jb, jagged_bias_grad=djb)
 
         def timed(fn):
             for _ in range(3):
@@ -451,7 +452,8 @@ def run_jfa(args, rank, world, device):
         pk = jfa.jfa_timing_read()
         if jfa.jfa_check_status(ws_b) != 0:
             raise RuntimeError("device status after the bias-gradient backward")
-        bias_grad = {"bwd_ms": round(t_grad, 4), "bwd_ms_without": round(t_plain, 4),
+        bias_grad = {"kind": "relative-position table" if batch.bias is not None else "general jagged bias",
+                     "bwd_ms": round(t_grad, 4), "bwd_ms_without": round(t_plain, 4),
                      "overhead": round(t_grad / t_plain - 1, 4),
                      "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in pk.items() if v[1]}}
 

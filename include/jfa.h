@@ -82,7 +82,10 @@ typedef enum {
  * [B+1] with block_offsets[0] = 0 and block_offsets[b+1] - block_offsets[b] =
  * Lq_b * round_up(Lk_b, 8), block_offsets[B] = plane -- checked on the device (a mismatch
  * is JFA_ERR_BAD_OFFSETS and no attention is computed).  Added after scaling, like kind 1.
- * It gets no gradient (`grad` must be NULL). */
+ * `grad` must be NULL for kind 2; its gradient goes to `values_grad` instead (jfa_backward
+ * only; NULL = not wanted): a device bf16 array with the layout of `values`, 16-byte
+ * aligned, not overlapping any other argument, overwritten with dS_ij = P_ij (dP_ij - D_i)
+ * at each block element (0 for pairs the causal mask hides and for the row padding). */
 typedef struct {
   int kind;
   const float* table;
@@ -92,6 +95,7 @@ typedef struct {
   const void* values;            /* kind 2 */
   const int64_t* block_offsets;  /* kind 2 */
   int64_t plane;                 /* kind 2 */
+  void* values_grad;             /* kind 2, jfa_backward */
 } jfa_bias;
 
 /* Bytes of workspace jfa_forward (is_backward = 0) or jfa_backward (is_backward = 1)

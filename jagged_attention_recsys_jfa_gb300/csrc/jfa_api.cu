@@ -131,7 +131,8 @@ jfa_status check_common(int B, int H, int d, int64_t total_q, int64_t total_kv, 
   if (bias && bias->kind == 2) {
     if (bias->grad) return JFA_ERR_UNSUPPORTED;
     if (!bias->values || !bias->block_offsets || bias->plane < 0 || !aligned16(bias->values) ||
-        (reinterpret_cast<uintptr_t>(bias->block_offsets) & 7u) != 0)
+        (reinterpret_cast<uintptr_t>(bias->block_offsets) & 7u) != 0 ||
+        (bias->values_grad && !aligned16(bias->values_grad)))
       return JFA_ERR_INVALID_ARG;
   } else if (bias && bias->kind != 0) {
     if (bias->kind != 1) return JFA_ERR_UNSUPPORTED;
@@ -163,6 +164,7 @@ Problem make_problem(int B, int H, int d, int64_t total_q, int64_t total_kv, con
   p.jbias = has_jbias ? bias->values : nullptr;
   p.jb_off = has_jbias ? bias->block_offsets : nullptr;
   p.jb_plane = has_jbias ? bias->plane : 0;
+  p.jb_grad = has_jbias ? bias->values_grad : nullptr;
   std::lock_guard<std::mutex> g(g_trace_mu);
   for (int k = 0; k < JFA_NUM_KERNEL_KINDS; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
   return p;
@@ -270,6 +272,8 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
     maps.row_bytes[i] = uint32_t(H) * uint32_t(d) * 2;
     maps.used[i] = 1;
   }
+  if (pr.jb_grad)  // pairs no pass visits (hidden by the causal mask) and the row padding read as 0
+    JFA_CHECK_LAUNCH(cudaMemsetAsync(pr.jb_grad, 0, size_t(H) * size_t(pr.jb_plane) * 2, s), "bias gradient clear");
   {
     KernelTimer t(JFA_KERNEL_PLAN, s);
     JFA_CHECK_LAUNCH(launch_plan(pr, maps, workspace, L, true, nsm, s), "planner launch");

@@ -50,6 +50,7 @@ struct BwdParams {
   const __nv_bfloat16* jbias;  // general jagged bias [H][jb_plane], or nullptr
   const int64_t* jb_off;       // its block offsets [B+1]
   int64_t jb_plane;
+  __nv_bfloat16* jb_grad;      // its gradient (dK/dV and fused passes), or nullptr
   const CUtensorMap* maps;
   const WorkItem* items;
   const int* n_items;
@@ -782,6 +783,16 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         tc_fence_before();
         mbar_arrive(&ds_full);
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
+        if (kJBias && p.jb_grad) {  // the general bias's gradient is dS itself
+          const int64_t pitch = (Lk + 7) / 8 * 8;
+          const int kj0 = kt * kBN + quarter * 32;
+          uint32_t gk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2) gk[c2] = pack_bf16x2(dp[2 * c2], dp[2 * c2 + 1]);
+          jbias_store_cols(gk, jb_scratch + (warp - kFirstComputeWarp) * 128,
+                           p.jb_grad + size_t(it.h) * p.jb_plane + it.jb + int64_t(i0) * pitch + kj0, pitch, Lq - i0,
+                           Lk - kj0, j < Lk, lane);
+        }
         if (kBias && p.bias_grad) {
           // dS^T of a padded key row is not zero (k = 0 but lse2 of the query is not), and
           // padded query columns only give 0 while their P^T stays finite: count neither
@@ -1593,6 +1604,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       // bias gradient: diagonal sums of this warp's dS^T (as in dbias_warp_tile, one column
       // half at a time); hidden and padded pairs have P^T = 0, so dS^T = 0 there
       float db_straight[2] = {0.f, 0.f}, db_wrapped[2] = {0.f, 0.f};
+      uint32_t gk[32];  // general bias: this key's dS^T as packed bf16 pairs of query rows
       {
         uint8_t* drow = sDS + w * 16384 + row * 128;
 #pragma unroll
@@ -1627,6 +1639,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
             v.w = pack_bf16x2(d8[6], d8[7]);
             const int chunk = 4 * hf + ch;
             *reinterpret_cast<uint4*>(drow + ((chunk ^ (row & 7)) << 4)) = v;
+            if (kJBias) {  // query rows 8 chunk .. + 7 of this key, for the general bias's gradient
+              gk[4 * chunk + 0] = v.x;
+              gk[4 * chunk + 1] = v.y;
+              gk[4 * chunk + 2] = v.z;
+              gk[4 * chunk + 3] = v.w;
+            }
           }
         }
       }
@@ -1634,6 +1652,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
       tc_fence_before();
       mbar_arrive(&ds_full);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
+      if (kJBias && p.jb_grad) {  // the general bias's gradient is dS itself
+        const int64_t pitch = (Lk + 7) / 8 * 8;
+        const int kj0 = kt * kBN + quarter * 32;
+        jbias_store_cols(gk, jb_scratch + (warp - kFirstComputeWarp) * 128,
+                         p.jb_grad + size_t(it.h) * p.jb_plane + it.jb + int64_t(64 * w) * pitch + kj0, pitch,
+                         Lq - 64 * w, Lk - kj0, valid, lane);
+      }
       if (kBias && p.bias_grad)
         dbias_flush(db_straight[0], db_wrapped[0] + db_straight[1], db_wrapped[1],
                     p.bias_grad + size_t(it.h) * p.num_buckets, p.num_buckets,
@@ -1703,6 +1728,7 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.jbias = static_cast<const __nv_bfloat16*>(pr.jbias);
   bp.jb_off = pr.jb_off;
   bp.jb_plane = pr.jb_plane;
+  bp.jb_grad = pass != kPassDq ? static_cast<__nv_bfloat16*>(pr.jb_grad) : nullptr;
   bp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
   bp.items = reinterpret_cast<const WorkItem*>(w + (pass == kPassDq ? L.dq : pass == kPassFused ? L.fused : L.dkv));
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);

@@ -20,6 +20,7 @@ struct Problem {
   const void* jbias;        // general jagged bias: bf16 [H][jb_plane], or nullptr
   const int64_t* jb_off;    // its block offsets [B+1]
   int64_t jb_plane;
+  void* jb_grad;            // its gradient (backward), bf16 [H][jb_plane], or nullptr
   TraceBuf trace[JFA_NUM_KERNEL_KINDS];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
 };
 

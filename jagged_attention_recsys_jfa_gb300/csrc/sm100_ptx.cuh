@@ -451,6 +451,35 @@ __device__ __forceinline__ void jbias_col_transpose(uint32_t* pk, const uint4 (&
   }
 }
 
+// The reverse of the two helpers above, for the general bias's gradient: a warp's 32 key
+// rows (lane) x 64 query rows, as packed bf16 pairs of query rows (pk[r2] = rows 2 r2,
+// 2 r2 + 1 of this lane's key), written row-major to `rows` (query row 0, key j0; rows
+// `pitch` elements apart) through the per-warp scratch, as 16-byte chunks: query rows >= n_q
+// and chunks starting at a key >= n_k are not written; key_valid false writes 0 (the row
+// padding past the sequence's keys).
+__device__ __forceinline__ void jbias_store_cols(const uint32_t* pk, uint4* scratch, void* rows, int64_t pitch,
+                                                 int n_q, int n_k, bool key_valid, int lane) {
+  uint16_t* s16 = reinterpret_cast<uint16_t*>(scratch);
+  uint16_t* r16 = reinterpret_cast<uint16_t*>(rows);
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+    for (int r2 = 0; r2 < 16; ++r2) {
+      const uint32_t v = key_valid ? pk[16 * pass + r2] : 0u;
+      s16[(2 * r2) * 32 + lane] = uint16_t(v & 0xffffu);
+      s16[(2 * r2 + 1) * 32 + lane] = uint16_t(v >> 16);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = lane + 32 * k, row = q / 4, part = q % 4;
+      if (rows != nullptr && 32 * pass + row < n_q && 8 * part < n_k)
+        *reinterpret_cast<uint4*>(r16 + (32 * pass + row) * pitch + 8 * part) = scratch[q];
+    }
+    __syncwarp();
+  }
+}
+
 // x[c] = x[c] * sl2 + l2e * bias[c] for the N columns, bias from the packed pairs.
 template <int N>
 __device__ __forceinline__ void jbias_apply(float* x, const uint32_t* pk, float sl2, float l2e) {

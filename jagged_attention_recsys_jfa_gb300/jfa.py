@@ -42,7 +42,7 @@ class JfaError(RuntimeError):
 class _Bias(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("table", ctypes.c_void_p), ("num_buckets", ctypes.c_int),
                 ("center", ctypes.c_int), ("grad", ctypes.c_void_p), ("values", ctypes.c_void_p),
-                ("block_offsets", ctypes.c_void_p), ("plane", ctypes.c_int64)]
+                ("block_offsets", ctypes.c_void_p), ("plane", ctypes.c_int64), ("values_grad", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -126,7 +126,7 @@ def _check_offsets(name, off):
         raise ValueError(f"{name} must be a contiguous int64 CUDA tensor [B+1] with B >= 1")
 
 
-def _bias_struct(bias, center, H, grad=None, jagged_bias=None):
+def _bias_struct(bias, center, H, grad=None, jagged_bias=None, jagged_bias_grad=None):
     if jagged_bias is not None:
         if bias is not None or grad is not None:
             raise ValueError("a general jagged bias excludes the relative-position table and its gradient")
@@ -135,7 +135,16 @@ def _bias_struct(bias, center, H, grad=None, jagged_bias=None):
                 or not values.is_contiguous()):
             raise ValueError("jagged bias values must be a contiguous bf16 CUDA tensor [H, plane]")
         _check_offsets("jagged bias block offsets", boff)
-        return _Bias(2, None, 0, 0, None, values.data_ptr(), boff.data_ptr(), values.shape[1]), (values, boff)
+        gptr = None
+        if jagged_bias_grad is not None:
+            if (jagged_bias_grad.dtype != torch.bfloat16 or tuple(jagged_bias_grad.shape) != tuple(values.shape)
+                    or not jagged_bias_grad.is_contiguous() or jagged_bias_grad.device != values.device):
+                raise ValueError("jagged_bias_grad must be a contiguous bf16 tensor shaped like the bias values")
+            gptr = jagged_bias_grad.data_ptr()
+        return (_Bias(2, None, 0, 0, None, values.data_ptr(), boff.data_ptr(), values.shape[1], gptr),
+                (values, boff))
+    if jagged_bias_grad is not None:
+        raise ValueError("jagged_bias_grad needs a general jagged bias")
     if bias is None:
         if grad is not None:
             raise ValueError("bias_grad needs a bias table")
@@ -209,10 +218,11 @@ def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=
 
 def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None,
                  causal=False, dq=None, dk=None, dv=None, workspace=None, stream=None, bias_grad=None,
-                 jagged_bias=None):
+                 jagged_bias=None, jagged_bias_grad=None):
     """dq, dk, dv, workspace = jfa_backward(...): gradients of sum(dout * out).  With
     `bias_grad` (a float32 tensor shaped like `bias`) the bias table's gradient is written
-    into it as well."""
+    into it as well; with `jagged_bias_grad` (a bf16 tensor shaped like a general bias's
+    values) that bias's gradient (dS at every block element)."""
     lib = load_library()
     _check_values("q", q)
     Tq, H, d = q.shape
@@ -224,7 +234,7 @@ def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias
     _check_offsets("kv_offsets", kv_offsets)
     B = q_offsets.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    bstruct, bias_keep = _bias_struct(bias, bias_center, H, bias_grad, jagged_bias)
+    bstruct, bias_keep = _bias_struct(bias, bias_center, H, bias_grad, jagged_bias, jagged_bias_grad)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -295,8 +305,8 @@ def decode_trace(buffer: torch.Tensor):
 class JaggedAttention(torch.autograd.Function):
     """Differentiable jagged attention: out = JaggedAttention.apply(q, k, v, q_offsets,
     kv_offsets, bias, bias_center, scale, causal, jagged_bias_values, jagged_bias_offsets).
-    lse is saved for the backward; the relative-position table gets its gradient when it
-    requires one; a general jagged bias gets none."""
+    lse is saved for the backward; the relative-position table and a general jagged bias's
+    values get their gradients when they require them."""
 
     @staticmethod
     def forward(ctx, q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,
@@ -313,9 +323,11 @@ class JaggedAttention(torch.autograd.Function):
         bias_center, scale, causal = ctx.cfg
         jb = (jb_values, jb_offsets) if jb_values is not None else None
         dbias = torch.empty_like(bias) if bias is not None and ctx.needs_input_grad[5] else None
+        djb = torch.empty_like(jb_values) if jb_values is not None and ctx.needs_input_grad[9] else None
         dq, dk, dv, _ = jfa_backward(dout.contiguous(), q, k, v, out, lse, q_offsets, kv_offsets, bias,
-                                     bias_center, scale, causal, bias_grad=dbias, jagged_bias=jb)
-        return dq, dk, dv, None, None, dbias, None, None, None, None, None
+                                     bias_center, scale, causal, bias_grad=dbias, jagged_bias=jb,
+                                     jagged_bias_grad=djb)
+        return dq, dk, dv, None, None, dbias, None, None, None, djb, None
 
 
 def jagged_attention(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=None, causal=False,

@@ -87,3 +87,42 @@ def test_jagged_bias_full_size_sampled():
         for gname, g, r in (("dq", res["dq"][sl, h], dq), ("dk", res["dk"][sl, h], dk), ("dv", res["dv"][sl, h], dv)):
             e = rel_frob(g, r)
             assert e <= GRAD_RTOL, f"b={b} h={h} {gname} rel err {e:.3g}"
+
+
+@pytest.mark.parametrize("name", ["causal_d64", "cross_fused_d128", "mixed_causal_d128"])
+def test_jagged_bias_gradient(name):
+    """The general bias's gradient (dS of every block element, 0 where the causal mask hides
+    the pair and on the row padding) against the oracle, over the whole [H, plane] array."""
+    from jagged_attention_recsys_jfa_gb300 import jfa_backward
+    H, d, lq, lk, causal = CASES[name]
+    batch = make_batch(_cfg(name, H, d, len(lq), causal), device="cuda", q_lengths=lq, kv_lengths=lk)
+    cfg = batch.cfg
+    jb = (batch.jbias, batch.jbias_offsets)
+    out, lse, ws = jfa_forward(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, None, 0, cfg.scale,
+                               cfg.causal, jagged_bias=jb)
+    g = torch.full_like(batch.jbias, float("nan"))   # every element must be written
+    dq, dk, dv, ws2 = jfa_backward(batch.dout, batch.q, batch.k, batch.v, out, lse, batch.q_offsets,
+                                   batch.kv_offsets, None, 0, cfg.scale, cfg.causal, jagged_bias=jb,
+                                   jagged_bias_grad=g)
+    assert jfa_check_status(ws) == 0 and jfa_check_status(ws2) == 0
+    torch.cuda.synchronize()
+    assert torch.isfinite(g.float()).all(), "unwritten or non-finite gradient elements"
+    ref = orc.jagged_general_bias_grad(batch.dout, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets,
+                                       cfg.scale, cfg.causal, jb)
+    e = rel_frob(g, ref)
+    assert e <= GRAD_RTOL, f"{name}: general bias gradient relative error {e:.3g}"
+    # the other gradients are unchanged by asking for it
+    compare_grads({"dq": dq, "dk": dk, "dv": dv}, oracle_full(batch), name)
+
+
+def test_jagged_bias_gradient_autograd():
+    from jagged_attention_recsys_jfa_gb300 import jagged_attention
+    batch = make_batch(_cfg("ag2", 2, 128, 3, False), device="cuda", q_lengths=[200, 7, 129], kv_lengths=[150, 300, 9])
+    values = batch.jbias.clone().requires_grad_(True)
+    out = jagged_attention(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, None, 0, batch.cfg.scale,
+                           False, jagged_bias=(values, batch.jbias_offsets))
+    out.backward(batch.dout)
+    ref = orc.jagged_general_bias_grad(batch.dout, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets,
+                                       batch.cfg.scale, False, (batch.jbias, batch.jbias_offsets))
+    e = rel_frob(values.grad, ref)
+    assert e <= GRAD_RTOL, f"autograd general bias gradient relative error {e:.3g}"
