@@ -709,6 +709,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
           const int qi0 = qt * kBM + 64 * w, kj0 = kt * kBN + quarter * 32;
           jbias_load_cols_vec(jbw, p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(qi0) * pitch + kj0, pitch,
                               Lq - qi0, Lk - kj0, lane);
+          if (kj0 < Lk) {  // the next query tile's rows of these keys into L2 meanwhile
+            const int nq0 = qi0 + kBM;
+            const __nv_bfloat16* nb = p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(nq0) * pitch + kj0;
+            if (nq0 + lane < Lq) prefetch_l2(nb + int64_t(lane) * pitch);
+            if (nq0 + 32 + lane < Lq) prefetch_l2(nb + int64_t(32 + lane) * pitch);
+          }
         }
         // Q_i's ring slot carries this tile's lse2 / D vectors: wait for it
         const uint32_t nq = ring_n + 1;
@@ -1166,8 +1172,12 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         if (kJBias) {
           const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
           const int jj0 = jt * kBN + 64 * w;
-          jbias_load_row<64>(jbk, valid ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + jj0 : nullptr,
-                             min(64, Lk - jj0));
+          const __nv_bfloat16* brow_i = p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch;
+          jbias_load_row<64>(jbk, valid ? brow_i + jj0 : nullptr, min(64, Lk - jj0));
+          if (valid && jj0 + kBN < Lk) {  // the next key tile's row segment into L2 meanwhile
+            prefetch_l2(brow_i + jj0 + kBN);
+            prefetch_l2(brow_i + jj0 + kBN + 56);
+          }
         }
         if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();

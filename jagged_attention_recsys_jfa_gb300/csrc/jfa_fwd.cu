@@ -422,9 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         if (kJBias) {
           const int64_t pitch = (it.Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
           const int kvj = j * kBN;
-          jbias_load_row<128>(jbk, valid_row ? p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch + kvj
-                                             : nullptr,
-                              min(kBN, it.Lk - kvj));
+          const __nv_bfloat16* brow_j = p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(i) * pitch;
+          jbias_load_row<128>(jbk, valid_row ? brow_j + kvj : nullptr, min(kBN, it.Lk - kvj));
+          if (valid_row && kvj + kBN < it.Lk) {  // the next key tile's row segment into L2 meanwhile
+            prefetch_l2(brow_j + kvj + kBN);
+            prefetch_l2(brow_j + kvj + kBN + 64);
+          }
         }
         if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++s_n;
