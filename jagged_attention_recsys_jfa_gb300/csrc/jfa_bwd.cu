@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
 // after dQ(j), i.e. in fill order.  S and dP of the next key tile are issued as soon as
 // the warpgroups hold S in registers, so the dP/dS buffer alternates by tile parity.
 template <int D, bool kBias, bool kJBias = false>
-__global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingDq;
   extern __shared__ uint8_t smem_raw[];
@@ -906,13 +906,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     mbar_init(&ds_full[0], 256);
     mbar_init(&ds_full[1], 256);
     mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 256);
+    mbar_init(&acc_empty, 128);
     mbar_init(&mma_done, 1);
     for (int i = 0; i < R; ++i) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    meta_init(meta);
+    meta_init(meta, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -934,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
   };
 
   if (warp < kFirstComputeWarp) {
-   setmaxnreg_dec<kRegsLoad>();
+   setmaxnreg_dec<kRegsLoadDkdv>();
    if (warp == 2) {
     // ------------------------------------------------------------ Q / dO loader
     if (lane == 0) {
@@ -1131,15 +1131,15 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
     if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, p.jb_off, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
-  } else {
-    setmaxnreg_inc<kRegsCompute>();
+  } else if (warp < kFirstEpilogueWarp) {
+    setmaxnreg_inc<kRegsComputeDkdv>();
     const int w = (warp - kFirstComputeWarp) >> 2;  // key columns [64w, 64w+64)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const float sl2 = p.scale_log2;
-    uint32_t tile_n = 0, acc_n = 0, tn = 0;
+    uint32_t tile_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     uint32_t item_k = 0;
@@ -1154,11 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
       const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
       const int i = qt * kBM + row;
       const bool valid = i < Lq;
-      __nv_bfloat16* dq_row = p.g0 + ((qo + i) * p.H + it.h) * int64_t(D) + w * (D / 2);
-      if (nkv == 0) {
-        store_acc_row<D / 2>(0, 0.f, dq_row, valid, true);
-        continue;
-      }
+      if (nkv == 0) continue;  // rows of zeros: written by the epilogue warpgroup
       // padded per-query vectors (stored negated): 0 past the sequence end, -inf for rows
       // that see no key
       const float nl2 = __ldg(p.lse2 + vec0 + i);
@@ -1251,12 +1247,40 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const BwdParams p) {
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
       }
       if (!ok) break;
+     }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  } else {
+    setmaxnreg_dec<kRegsEpiDkdv>();
+    // ------------------------------------------------------------ epilogue warpgroup
+    // Writes each query tile's dQ rows (this thread's TMEM lane = one query row, all D
+    // columns, 32 at a time) while warpgroups 1 and 2 start the next query tile; the
+    // accumulator is released as soon as its last columns are in registers.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    uint32_t acc_n = 0;
+    bool ok = true;
+    uint32_t item_k = 0;
+    for (; ok; ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+     if (it.b < 0) break;  // end of this CTA's items
+     const int Lq = it.Lq, Lk = it.Lk;
+     for (int qt = it.u0; qt < it.u1 && ok; ++qt) {
+      const int i = qt * kBM + row;
+      const bool valid = i < Lq;
+      __nv_bfloat16* dq_row = p.g0 + ((it.qo + i) * p.H + it.h) * int64_t(D);
+      if (kv_tiles_for_q_tile(qt, Lq, Lk, causal) == 0) {  // the query tile sees no key
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) store_acc_row<32>(0, 0.f, dq_row + c0, valid, true);
+        continue;
+      }
       if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
-      store_acc_row<D / 2>(tmem + lane_addr + C::kColDQ + w * (D / 2), p.scale, dq_row, valid, false);
-      tc_fence_before();
-      mbar_arrive(&acc_empty);
+      drain_acc_rows<D>(tmem + lane_addr + C::kColDQ, p.scale, dq_row, valid, &acc_empty);
      }
      if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
     }
@@ -1845,12 +1869,12 @@ cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const W
   bp.g0 = static_cast<__nv_bfloat16*>(dq);
   const bool bias = pr.bias_table != nullptr, jb = pr.jbias != nullptr;
   if (pr.d == 128)
-    return bias ? launch_big(dq_kernel<128, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
-                : jb ? launch_big(dq_kernel<128, false, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
-                     : launch_big(dq_kernel<128, false>, BwdCfg<128>::kSmemDq, num_sms, bp, stream);
-  return bias ? launch_big(dq_kernel<64, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
-              : jb ? launch_big(dq_kernel<64, false, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
-                   : launch_big(dq_kernel<64, false>, BwdCfg<64>::kSmemDq, num_sms, bp, stream);
+    return bias ? launch_dkdv_k(dq_kernel<128, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
+                : jb ? launch_dkdv_k(dq_kernel<128, false, true>, BwdCfg<128>::kSmemDq, num_sms, bp, stream)
+                     : launch_dkdv_k(dq_kernel<128, false>, BwdCfg<128>::kSmemDq, num_sms, bp, stream);
+  return bias ? launch_dkdv_k(dq_kernel<64, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
+              : jb ? launch_dkdv_k(dq_kernel<64, false, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
+                   : launch_dkdv_k(dq_kernel<64, false>, BwdCfg<64>::kSmemDq, num_sms, bp, stream);
 }
 
 }  // namespace jfa
