@@ -73,6 +73,14 @@ def test_host_argument_checks_return_before_any_device_work():
     assert _fwd(lib, bias=ctypes.byref(big_bias)) == 1
     odd_grad = jfa.jfa._Bias(1, 16, 16, 0, 18)     # gradient table not 4-byte aligned
     assert _fwd(lib, bias=ctypes.byref(odd_grad)) == 1
+    # general jagged bias (kind 2): values 16-byte aligned, block offsets 8-byte aligned,
+    # no relative-position gradient, its own gradient 16-byte aligned
+    assert _fwd(lib, bias=ctypes.byref(jfa.jfa._Bias(2, None, 0, 0, None, 40, 64, 100))) == 1
+    assert _fwd(lib, bias=ctypes.byref(jfa.jfa._Bias(2, None, 0, 0, None, 32, 68, 100))) == 1
+    assert _fwd(lib, bias=ctypes.byref(jfa.jfa._Bias(2, None, 0, 0, None, None, 64, 100))) == 1
+    assert _fwd(lib, bias=ctypes.byref(jfa.jfa._Bias(2, None, 0, 0, 16, 32, 64, 100))) == 2
+    assert _fwd(lib, bias=ctypes.byref(jfa.jfa._Bias(2, None, 0, 0, None, 32, 64, 100, 24))) == 1
+    assert _fwd(lib, bias=ctypes.byref(jfa.jfa._Bias(2, None, 0, 0, None, 32, 64, -1))) == 1
 
 
 def test_status_strings():
@@ -88,3 +96,23 @@ def test_python_binding_rejects_cpu_tensors():
     off = torch.tensor([0, 4], dtype=torch.int64)
     with pytest.raises(ValueError):
         jfa.jfa_forward(q, q, q, off, off)
+
+
+def test_python_binding_checks_bias_arguments():
+    import torch
+    H = 2
+    table = torch.zeros(H, 16)
+    values = torch.zeros(H, 64, dtype=torch.bfloat16)
+    boff = torch.tensor([0, 64], dtype=torch.int64)
+    with pytest.raises(ValueError):   # the table must be a CUDA tensor
+        jfa.jfa._bias_struct(table, 0, H)
+    with pytest.raises(ValueError):   # a general bias excludes the table
+        jfa.jfa._bias_struct(table, 0, H, jagged_bias=(values, boff))
+    with pytest.raises(ValueError):   # and the table's gradient
+        jfa.jfa._bias_struct(None, 0, H, grad=table, jagged_bias=(values, boff))
+    with pytest.raises(ValueError):   # its values must be CUDA bf16 [H, plane]
+        jfa.jfa._bias_struct(None, 0, H, jagged_bias=(values, boff))
+    with pytest.raises(ValueError):   # a general-bias gradient needs a general bias
+        jfa.jfa._bias_struct(None, 0, H, jagged_bias_grad=values)
+    with pytest.raises(ValueError):   # a table gradient needs a table
+        jfa.jfa._bias_struct(None, 0, H, grad=table)
