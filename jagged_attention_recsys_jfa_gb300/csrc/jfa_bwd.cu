@@ -34,8 +34,9 @@ constexpr uint32_t kRegsLoadDkdv = 96, kRegsComputeDkdv = 168, kRegsEpiDkdv = 72
 static_assert(reg_split_fits_dkdv(kRegsLoadDkdv, kRegsComputeDkdv, kRegsEpiDkdv),
               "register split exceeds the launch allocation");
 // the fused short-query pass: more issue state in warpgroup 0, lighter compute warps
-constexpr uint32_t kRegsLoadFused = 136, kRegsComputeFused = 184;
-static_assert(reg_split_fits(kRegsLoadFused, kRegsComputeFused), "register split exceeds the launch allocation");
+constexpr uint32_t kRegsLoadFused = 112, kRegsComputeFused = 168, kRegsEpiFused = 64;
+static_assert(reg_split_fits_dkdv(kRegsLoadFused, kRegsComputeFused, kRegsEpiFused),
+              "register split exceeds the launch allocation");
 
 struct BwdParams {
   const int64_t* q_off;
@@ -334,6 +335,30 @@ __device__ __forceinline__ void store_acc_row_own(uint32_t taddr, float mul, __n
     }
   }
 }
+// All D accumulator columns of this thread's TMEM lane, times `mul`, as bf16 to its own row,
+// 32 columns at a time; arrives on `empty` as soon as the last columns are in registers.
+template <int D>
+__device__ __forceinline__ void drain_row_own(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid,
+                                              uint64_t* empty) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c0, r);
+    tmem_ld_wait();
+    if (c0 + 32 == D) {
+      tc_fence_before();
+      mbar_arrive(empty);
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * mul, __uint_as_float(r[2 * t + 1]) * mul);
+    if (valid) {
+      st_global_v8(dst + c0, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+      st_global_v8(dst + c0 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+    }
+  }
+}
+
 // Write NC (32 or 64) accumulator columns of this thread's TMEM lane, times `mul`, as bf16
 // to global (or zeros when `zero`).  All 32 lanes of the warp call it together: the rows'
 // stores are shared across lanes so that each store instruction writes whole row segments.
@@ -1147,7 +1172,6 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
      if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
      const ItemMeta& it = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
      if (it.b < 0) break;  // end of this CTA's items
-     const int64_t qo = it.qo;
      const int Lq = it.Lq, Lk = it.Lk;
      const int64_t vec0 = int64_t(it.h) * p.qpad_cap + it.qp;
      for (int qt = it.u0; qt < it.u1 && ok; ++qt) {
@@ -1305,7 +1329,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
 // so K and V are read once instead of once per pass, still without atomics.  Key tiles
 // the query tile cannot see (causal) get zero dK / dV rows and no MMAs.
 template <int D, bool kBias, bool kJBias = false>
-__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingFused;
   extern __shared__ uint8_t smem_raw[];
@@ -1334,18 +1358,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     mbar_init(&p_full, 256);
     mbar_init(&ds_full, 256);
     mbar_init(&dv_full, 1);
-    mbar_init(&dv_empty, 256);
+    mbar_init(&dv_empty, 128);
     mbar_init(&dk_full, 1);
-    mbar_init(&dk_empty, 256);
+    mbar_init(&dk_empty, 128);
     mbar_init(&dsm_empty, 1);
     mbar_init(&dq_full, 1);
-    mbar_init(&dq_empty, 256);
+    mbar_init(&dq_empty, 128);
     mbar_init(&mma_done, 1);
     for (int i = 0; i < R; ++i) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    meta_init(meta);
+    meta_init(meta, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1543,7 +1567,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
     if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, p.jb_off, abort_flag))
       raise_status(p.status, JFA_ERR_TIMEOUT);
    }
-  } else {
+  } else if (warp < kFirstEpilogueWarp) {
     setmaxnreg_inc<kRegsComputeFused>();
     // ------------------------------------------------------------ compute warpgroups
     const int w = (warp - kFirstComputeWarp) >> 2;  // queries [64w, 64w+64)
@@ -1574,13 +1598,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
      for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
       const int j = kt * kBN + row;  // local key index
       const bool valid = j < Lk;
-      __nv_bfloat16* dk_row = p.g0 + ((it.ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
-      __nv_bfloat16* dv_row = p.g1 + ((it.ko + j) * p.H + it.h) * int64_t(D) + w * (D / 2);
-      if (!visible(kt, Lq, Lk)) {
-        store_acc_row_own<D / 2>(0, 0.f, dk_row, valid, true);
-        store_acc_row_own<D / 2>(0, 0.f, dv_row, valid, true);
-        continue;
-      }
+      if (!visible(kt, Lq, Lk)) continue;  // zero dK / dV rows: written by the epilogue warpgroup
       uint4 jbw[8];  // general bias for this tile (row order), loaded before the wait
       if (kJBias) {
         const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
@@ -1697,37 +1715,59 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const BwdParams p) {
         dbias_flush(db_straight[0], db_wrapped[0] + db_straight[1], db_wrapped[1],
                     p.bias_grad + size_t(it.h) * p.num_buckets, p.num_buckets,
                     kt * kBN + quarter * 32 - i0 - 63 + p.center, lane);
-      // ---- dV_j and dK_j rows
-      if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-      tc_fence_after();
-      store_acc_row_own<D / 2>(tmem + lane_addr + C::kColFdV + w * (D / 2), 1.f, dv_row, valid, false);
-      tc_fence_before();
-      mbar_arrive(&dv_empty);
-      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
-      if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-      tc_fence_after();
-      store_acc_row_own<D / 2>(tmem + lane_addr + C::kColP + w * (D / 2), p.scale, dk_row, valid, false);
-      tc_fence_before();
-      mbar_arrive(&dk_empty);
-      if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 25);
       ++g;
      }
      if (!ok) break;
-     // ---- dQ rows (TMEM lane = query): zeros when the query tile sees no key
-     {
-      const int i = row;
-      const bool qvalid = i < Lq;
-      __nv_bfloat16* dq_row = p.g2 + ((it.qo + i) * p.H + it.h) * int64_t(D) + w * (D / 2);
-      if (live) {
-        if (!mbar_wait(&dq_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
-        tc_fence_after();
-        store_acc_row_own<D / 2>(tmem + lane_addr + C::kColFdQ + w * (D / 2), p.scale, dq_row, qvalid, false);
-        tc_fence_before();
-        mbar_arrive(&dq_empty);
-        ++item_n;
-      } else {
-        store_acc_row_own<D / 2>(0, 0.f, dq_row, qvalid, true);
+     if (live) ++item_n;  // the item's dQ rows: written by the epilogue warpgroup
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  } else {
+    setmaxnreg_dec<kRegsEpiFused>();
+    // ------------------------------------------------------------ epilogue warpgroup
+    // Each key tile's dV_j and dK_j rows (this thread = one key row, all D columns; zeros
+    // for tiles the query tile cannot see) and, at the item's end, its dQ rows (this thread =
+    // one query row), each accumulator released once its last columns are in registers.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    uint32_t g = 0, item_n = 0;
+    bool ok = true;
+    uint32_t item_k = 0;
+    for (; ok; ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];
+     if (it.b < 0) break;  // end of this CTA's items
+     const int Lq = it.Lq, Lk = it.Lk;
+     const bool live = any_visible(it.u0, it.u1, Lq, Lk);
+     for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
+      const int j = kt * kBN + row;  // local key index
+      const bool valid = j < Lk;
+      __nv_bfloat16* dk_row = p.g0 + ((it.ko + j) * p.H + it.h) * int64_t(D);
+      __nv_bfloat16* dv_row = p.g1 + ((it.ko + j) * p.H + it.h) * int64_t(D);
+      if (!visible(kt, Lq, Lk)) {
+        store_acc_row_own<D>(0, 0.f, dk_row, valid, true);
+        store_acc_row_own<D>(0, 0.f, dv_row, valid, true);
+        continue;
       }
+      if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      drain_row_own<D>(tmem + lane_addr + C::kColFdV, 1.f, dv_row, valid, &dv_empty);
+      if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      drain_row_own<D>(tmem + lane_addr + C::kColP, p.scale, dk_row, valid, &dk_empty);
+      ++g;
+     }
+     if (!ok) break;
+     const bool qvalid = row < Lq;
+     __nv_bfloat16* dq_row = p.g2 + ((it.qo + row) * p.H + it.h) * int64_t(D);
+     if (live) {
+       if (!mbar_wait(&dq_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+       ++item_n;
+       tc_fence_after();
+       drain_row_own<D>(tmem + lane_addr + C::kColFdQ, p.scale, dq_row, qvalid, &dq_empty);
+     } else {
+       store_acc_row_own<D>(0, 0.f, dq_row, qvalid, true);
      }
      if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
     }
@@ -1855,12 +1895,12 @@ cudaError_t launch_bwd_fused(const Problem& pr, const float* lse, void* ws, cons
   bp.g2 = static_cast<__nv_bfloat16*>(dq);
   const bool bias = pr.bias_table != nullptr, jb = pr.jbias != nullptr;
   if (pr.d == 128)
-    return bias ? launch_big(fused_kernel<128, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
-                : jb ? launch_big(fused_kernel<128, false, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
-                     : launch_big(fused_kernel<128, false>, BwdCfg<128>::kSmemFused, num_sms, bp, stream);
-  return bias ? launch_big(fused_kernel<64, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
-              : jb ? launch_big(fused_kernel<64, false, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
-                   : launch_big(fused_kernel<64, false>, BwdCfg<64>::kSmemFused, num_sms, bp, stream);
+    return bias ? launch_dkdv_k(fused_kernel<128, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
+                : jb ? launch_dkdv_k(fused_kernel<128, false, true>, BwdCfg<128>::kSmemFused, num_sms, bp, stream)
+                     : launch_dkdv_k(fused_kernel<128, false>, BwdCfg<128>::kSmemFused, num_sms, bp, stream);
+  return bias ? launch_dkdv_k(fused_kernel<64, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
+              : jb ? launch_dkdv_k(fused_kernel<64, false, true>, BwdCfg<64>::kSmemFused, num_sms, bp, stream)
+                   : launch_dkdv_k(fused_kernel<64, false>, BwdCfg<64>::kSmemFused, num_sms, bp, stream);
 }
 
 cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, int num_sms,
