@@ -1,0 +1,75 @@
+"""The benchmark's work accounting (host logic, CPU): visited pairs against brute force,
+and the flops / bytes split across the kernels that share the work."""
+import importlib.util
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    argv, sys.argv = sys.argv, ["bench.py"]
+    try:
+        spec.loader.exec_module(b)
+    finally:
+        sys.argv = argv
+    return b
+
+
+def _brute_pairs(lq, lk, causal):
+    n = 0
+    for a, c in zip(lq, lk):
+        for i in range(a):
+            for j in range(c):
+                n += 1 if (not causal or j <= i + (c - a)) else 0
+    return n
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_valid_pairs_brute_force(causal):
+    b = _bench()
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        B = int(rng.integers(1, 6))
+        lq = rng.integers(0, 40, B).tolist()
+        lk = rng.integers(0, 40, B).tolist()
+        assert b.valid_pairs(lq, lk, causal) == _brute_pairs(lq, lk, causal), (lq, lk)
+
+
+def test_flops_split_adds_up():
+    b = _bench()
+    from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, make_batch
+    for name in ("tiny", "biased_causal"):
+        batch = make_batch(CONFIGS[name], device="cpu")
+        f = b.workload_flops(batch)
+        dH = batch.cfg.head_dim * batch.cfg.heads
+        assert f["fwd"] == 4.0 * dH * f["pairs"]
+        assert f["bwd"] == 10.0 * dH * f["pairs"]
+        # the split passes and the fused pass cover every visited pair once
+        assert f["dkdv"] / 8 + f["fused"] / 10 == pytest.approx(f["pairs"] * dH)
+        assert f["dq"] * 4 == pytest.approx(f["dkdv"])
+
+
+def test_general_bias_bytes_counted_once_per_pass():
+    b = _bench()
+    import dataclasses
+    from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, make_batch
+    plain = make_batch(dataclasses.replace(CONFIGS["jagged_bias_causal"], batch=6, general_bias=False), device="cpu")
+    jb = make_batch(dataclasses.replace(CONFIGS["jagged_bias_causal"], batch=6), device="cpu")
+    w0, w1 = b.workload_bytes(plain), b.workload_bytes(jb)
+    H = jb.cfg.heads
+    lq, lk = jb.q_lengths.numpy(), jb.kv_lengths.numpy()
+    blocks = 2.0 * H * lq * ((lk + 7) // 8 * 8)
+    long_ = lq > 128
+    assert w1["forward"] - w0["forward"] == pytest.approx(blocks.sum())
+    assert w1["bwd_dkdv"] - w0["bwd_dkdv"] == pytest.approx(blocks[long_].sum())
+    assert w1["bwd_dq"] - w0["bwd_dq"] == pytest.approx(blocks[long_].sum())
+    assert w1["bwd_fused"] - w0["bwd_fused"] == pytest.approx(blocks[~long_].sum())
+    assert jb.jbias.numel() == blocks.sum() / 2
