@@ -5,6 +5,11 @@ a batch shards with no exchange step: each rank runs the kernels on its own sequ
 and, if a caller wants the full outputs everywhere, one all-gather puts them back.
 Sequences are balanced by the work they cost (the (query, key) pairs attention
 visits), longest first onto the least-loaded rank.
+
+Biases follow their sequences: a general jagged bias's blocks are packed per shard like
+the values (select_bias_blocks). A relative-position table is shared by every sequence,
+so its gradient is the one exchange a sharded backward has: each rank's table holds the
+sum over its own sequences, and one all-reduce (sum) over the ranks gives the batch's.
 """
 from __future__ import annotations
 
@@ -63,3 +68,17 @@ def scatter_sequences(full: torch.Tensor, offsets: torch.Tensor, index: Sequence
     poff = part_offsets.tolist()
     for k, b in enumerate(index):
         full[off[b]:off[b + 1]] = part[poff[k]:poff[k + 1]]
+
+
+def select_bias_blocks(values: torch.Tensor, block_offsets: torch.Tensor, index: Sequence[int]):
+    """Pack the general jagged bias blocks (values [H, plane], block offsets [B+1]) of the
+    chosen sequences into the bias of a shard; returns (values, block offsets).  A block's
+    layout depends only on its sequence's lengths, so blocks move unchanged."""
+    off = block_offsets.tolist()
+    parts = [values[:, off[b]:off[b + 1]] for b in index]
+    sizes = [off[b + 1] - off[b] for b in index]
+    new_off = torch.zeros(len(index) + 1, dtype=torch.int64)
+    if sizes:
+        new_off[1:] = torch.cumsum(torch.tensor(sizes, dtype=torch.int64), 0)
+    packed = torch.cat(parts, 1).contiguous() if parts else values[:, :0]
+    return packed, new_off.to(block_offsets.device)

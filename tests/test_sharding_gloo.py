@@ -12,8 +12,8 @@ import torch.multiprocessing as mp
 
 import oracle.jfa_oracle as orc
 from jagged_attention_recsys_jfa_gb300.inputs import JaggedConfig, make_batch
-from jagged_attention_recsys_jfa_gb300.sharding import (scatter_sequences, select_sequences, shard_sequences,
-                                                        visited_pairs)
+from jagged_attention_recsys_jfa_gb300.sharding import (scatter_sequences, select_bias_blocks, select_sequences,
+                                                        shard_sequences, visited_pairs)
 
 
 def test_visited_pairs_matches_mask_count():
@@ -79,3 +79,58 @@ def test_two_rank_gloo_sharding_reassembles_exactly():
     result = mgr.dict()
     mp.spawn(_worker, args=(2, _free_port(), result), nprocs=2, join=True)
     assert result.get("out_equal") and result.get("lse_equal"), dict(result)
+
+
+CFG_JB = JaggedConfig("shard_jb", 6, 2, 8, ("uniform", 1, 30), kv_lengths=("uniform", 1, 40), causal=True,
+                      general_bias=True)
+
+
+def _worker_bias(rank, world, port, result):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # general jagged bias: the shard's blocks travel with its sequences
+        b = make_batch(CFG_JB)
+        shards = shard_sequences(b.q_lengths.tolist(), b.kv_lengths.tolist(), world, CFG_JB.causal)
+        mine = shards[rank]
+        q, qo = select_sequences(b.q, b.q_offsets, mine)
+        k, ko = select_sequences(b.k, b.kv_offsets, mine)
+        v, _ = select_sequences(b.v, b.kv_offsets, mine)
+        jv, jo = select_bias_blocks(b.jbias, b.jbias_offsets, mine)
+        out, _ = orc.jagged_forward(q, k, v, qo, ko, CFG_JB.scale, CFG_JB.causal, jagged_bias=(jv, jo))
+        gathered = [None] * world
+        dist.all_gather_object(gathered, (mine, out, qo))
+        # relative-position table gradient: partial sums per rank, one all-reduce
+        c = make_batch(CFG)
+        cs = shard_sequences(c.q_lengths.tolist(), c.kv_lengths.tolist(), world, CFG.causal)[rank]
+        cq, cqo = select_sequences(c.q, c.q_offsets, cs)
+        ck, cko = select_sequences(c.k, c.kv_offsets, cs)
+        cv, _ = select_sequences(c.v, c.kv_offsets, cs)
+        cdo, _ = select_sequences(c.dout, c.q_offsets, cs)
+        g = torch.from_numpy(orc.jagged_bias_grad(cdo, cq, ck, cv, cqo, cko, CFG.scale, CFG.causal, c.bias,
+                                                  CFG.bias_center))
+        dist.all_reduce(g, op=dist.ReduceOp.SUM)
+        if rank == 0:
+            full_out = torch.zeros(b.q.shape, dtype=torch.float64)
+            for idx, o, off in gathered:
+                scatter_sequences(full_out, b.q_offsets, idx, torch.from_numpy(o), off)
+            ref_out, _ = orc.jagged_forward(b.q, b.k, b.v, b.q_offsets, b.kv_offsets, CFG_JB.scale, CFG_JB.causal,
+                                            jagged_bias=(b.jbias, b.jbias_offsets))
+            result["jb_out_equal"] = bool(np.array_equal(full_out.numpy(), ref_out))
+            ref_g = orc.jagged_bias_grad(c.dout, c.q, c.k, c.v, c.q_offsets, c.kv_offsets, CFG.scale, CFG.causal,
+                                         c.bias, CFG.bias_center)
+            result["dbias_err"] = float(np.abs(g.numpy() - ref_g).max() / max(np.abs(ref_g).max(), 1e-30))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_gloo_biases_shard():
+    """A general bias sharded with its sequences reassembles the unsharded output exactly;
+    the relative-position table's gradient, summed over the ranks by one all-reduce, equals
+    the unsharded gradient up to the order of the float64 additions."""
+    mgr = mp.Manager()
+    result = mgr.dict()
+    mp.spawn(_worker_bias, args=(2, _free_port(), result), nprocs=2, join=True)
+    assert result.get("jb_out_equal"), dict(result)
+    assert result.get("dbias_err", 1.0) <= 1e-12, dict(result)
