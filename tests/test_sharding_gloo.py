@@ -75,7 +75,7 @@ def _worker(rank, world, port, result):
 
 
 def test_two_rank_gloo_sharding_reassembles_exactly():
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (threaded) process
     result = mgr.dict()
     mp.spawn(_worker, args=(2, _free_port(), result), nprocs=2, join=True)
     assert result.get("out_equal") and result.get("lse_equal"), dict(result)
@@ -129,7 +129,7 @@ def test_two_rank_gloo_biases_shard():
     """A general bias sharded with its sequences reassembles the unsharded output exactly;
     the relative-position table's gradient, summed over the ranks by one all-reduce, equals
     the unsharded gradient up to the order of the float64 additions."""
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (threaded) process
     result = mgr.dict()
     mp.spawn(_worker_bias, args=(2, _free_port(), result), nprocs=2, join=True)
     assert result.get("jb_out_equal"), dict(result)
