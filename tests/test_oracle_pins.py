@@ -307,6 +307,63 @@ def test_general_bias_grad_finite_differences(causal):
         assert np.abs(g[:, int(off[0]) + 3:int(off[0]) + 5]).max() == 0.0
 
 
+# --------------------------------------------------------------------------- one-pair entry point
+@pytest.mark.parametrize("bias_kind", ["none", "table", "general"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("as_torch", [False, True])
+def test_sequence_reference_matches_jagged_front_ends(bias_kind, causal, as_torch):
+    """`sequence_reference` (the per-(sequence, head) entry point that checks the full-size
+    GPU runs and times the CPU baseline) slices q, k, v, dout and the bias on its own.  Its
+    results must be exactly the matching slices of `jagged_forward` / `jagged_backward`, for
+    every sequence and head: empty query and key sequences, one-key rows, Lq != Lk (causal
+    rows that see no key), a table small enough that the bucket clamp fires, and a general
+    bias whose row padding holds huge values that a mis-sliced block would pick up.  Inputs
+    are passed both as numpy arrays and as the bf16 torch tensors the GPU tests hand it."""
+    rng = np.random.default_rng(21)
+    lq, lk = [0, 5, 1, 9, 4, 3], [3, 0, 1, 11, 2, 3]
+    q, k, v, do, qo, ko, bt = rand_batch(rng, lq, lk, H=3, d=8, bias_buckets=7 if bias_kind == "table" else 0)
+    H = q.shape[1]
+    jb = None
+    if bias_kind == "general":
+        vals, off = _pack_jagged_bias([rng.standard_normal((H, a, b)) for a, b in zip(lq, lk)], lq, lk, H)
+        jb = (np.nan_to_num(vals, nan=1e300), off)
+    if as_torch:
+        bf = lambda x: torch.from_numpy(x).to(torch.bfloat16)
+        q, k, v, do = bf(q), bf(k), bf(v), bf(do)
+        bt = torch.from_numpy(bt).float() if bt is not None else None
+        qo, ko = torch.from_numpy(qo), torch.from_numpy(ko)
+        if jb is not None:   # bf16 rounds 1e300 to inf: padding reads would give NaN / inf
+            jb = (bf(jb[0]), torch.from_numpy(jb[1]))
+    kw = dict(scale=0.41, causal=causal, bias_table=bt, bias_center=3, jagged_bias=jb)
+    out, lse = orc.jagged_forward(q, k, v, qo, ko, **kw)
+    dq, dk, dv = orc.jagged_backward(do, q, k, v, qo, ko, **kw)
+    qo_, ko_ = orc.to_i64(qo), orc.to_i64(ko)
+    for b in range(len(lq)):
+        sq, sk = slice(qo_[b], qo_[b + 1]), slice(ko_[b], ko_[b + 1])
+        for h in range(H):
+            o1, l1, dq1, dk1, dv1 = orc.sequence_reference(b, h, q, k, v, qo, ko, 0.41, causal, bt, 3, dout=do,
+                                                           jagged_bias=jb)
+            assert o1.shape == (lq[b], q.shape[2]) and dk1.shape == (lk[b], q.shape[2])
+            np.testing.assert_allclose(o1, out[sq, h], rtol=0, atol=1e-13)
+            fin = np.isfinite(lse[h, sq])
+            assert np.array_equal(fin, np.isfinite(l1))
+            np.testing.assert_allclose(l1[fin], lse[h, sq][fin], rtol=0, atol=1e-13)
+            np.testing.assert_allclose(dq1, dq[sq, h], rtol=0, atol=1e-13)
+            np.testing.assert_allclose(dk1, dk[sk, h], rtol=0, atol=1e-13)
+            np.testing.assert_allclose(dv1, dv[sk, h], rtol=0, atol=1e-13)
+            o2, l2 = orc.sequence_reference(b, h, q, k, v, qo, ko, 0.41, causal, bt, 3, jagged_bias=jb)
+            assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # the pin bites: a sequence_reference that reads its general-bias block one row off
+    # (or a table with the wrong center) no longer matches
+    if bias_kind != "none":
+        b, h = 3, 1
+        shifted = dict(bias_table=bt, bias_center=4) if bias_kind == "table" else dict(
+            jagged_bias=(jb[0], (orc.to_i64(jb[1]) + 16)))
+        o_bad, _ = orc.sequence_reference(b, h, q, k, v, qo, ko, 0.41, causal, dout=None,
+                                          **{"bias_table": None, "bias_center": 3, **shifted})
+        assert not np.allclose(o_bad, out[qo_[b]:qo_[b + 1], h], rtol=0, atol=1e-6)
+
+
 # --------------------------------------------------------------------------- invariants
 def test_rows_sum_to_one_and_D_identity():
     rng = np.random.default_rng(5)
