@@ -59,21 +59,42 @@ def bf16_half_ulp(x):
     return np.exp2(np.floor(np.log2(ax)) - 8)
 
 
+def rne_bf16(x):
+    """Round float64 values to the nearest bf16 (ties to even), returned as float64: the
+    best a bf16 output can hold."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+ROUNDING_FLOOR = 2.0   # |O| from which half a bf16 ulp (>= 7.8e-3) nears the 1e-2 bound
+
+
 def compare_out_lse(got_out, got_lse, ref_out, ref_lse, what="", with_rounding=False):
-    """Forward check.  The workload configs use the plain bound |out - oracle| <= 1e-2.
-    With `with_rounding` (edge cases whose rows average one or two value rows, so |O|
-    reaches 2-4) each element may also differ by the unavoidable rounding of the
-    output to bf16, half a bf16 ulp of the exact value (7.8e-3 for |O| in [2, 4))."""
+    """Forward check: max |out - oracle| <= 1e-2 on every element, lse within 2e-3.
+
+    `with_rounding` is for the hand-made edge sets only, whose rows can average one or
+    two value rows, so |O| reaches 2-4 where half a bf16 ulp is already 7.8e-3.  There,
+    and only on elements with |oracle| >= 2, the output's own unavoidable rounding to
+    bf16 (half an ulp of the exact value) is allowed on top of the bound; every other
+    element is held to the flat 1e-2.  Whenever an element needs that allowance the
+    comparison prints how many did and max |out - RNE_bf16(oracle)| over them, the
+    distance from the best bf16 answer."""
     go, gl = _np(got_out), _np(got_lse)
     assert np.all(np.isfinite(go)), f"{what}: non-finite output"
     diff = np.abs(go - ref_out)
     if with_rounding:
-        diff = diff - bf16_half_ulp(ref_out)
+        big = np.abs(ref_out) >= ROUNDING_FLOOR
+        over = big & (diff > OUT_ATOL)
+        if over.any():
+            rne_err = np.abs(go[over] - rne_bf16(ref_out[over])).max()
+            print(f"{what}: {int(over.sum())} element(s) with |oracle| >= {ROUNDING_FLOOR} exceed the flat "
+                  f"{OUT_ATOL} by their bf16 rounding: max |out - oracle| = {diff[over].max():.3g}, "
+                  f"max |out - RNE_bf16(oracle)| = {rne_err:.3g}")
+        diff = np.where(big, diff - bf16_half_ulp(ref_out), diff)
     err = diff.max() if go.size else 0.0
     if err > OUT_ATOL:
         at = np.unravel_index(np.argmax(diff), diff.shape)
-        raise AssertionError(f"{what}: max |out - oracle|{' - half ulp' if with_rounding else ''} = {err:.3g} > "
-                             f"{OUT_ATOL} at {at}, oracle {ref_out[at]:.4f}, got {go[at]:.4f}")
+        raise AssertionError(f"{what}: max |out - oracle|{' (- half ulp where |oracle| >= 2)' if with_rounding else ''}"
+                             f" = {err:.3g} > {OUT_ATOL} at {at}, oracle {ref_out[at]:.4f}, got {go[at]:.4f}")
     ninf_ref = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(gl), ninf_ref), f"{what}: -inf lse pattern differs"
     fin = ~ninf_ref

@@ -37,6 +37,8 @@ def test_jagged_bias_parity(name):
     batch = make_batch(_cfg(name, H, d, len(lq), causal), device="cuda", q_lengths=lq, kv_lengths=lk)
     res = gpu_run(batch)
     ref = oracle_full(batch)
+    # hand-made edge shapes (1-key rows, empty sequences): the bf16 rounding allowance
+    # applies to their |oracle| >= 2 elements only, and is reported when used
     compare_out_lse(res["out"], res["lse"], ref["out"], ref["lse"], name, with_rounding=True)
     compare_grads(res, ref, name)
 
@@ -83,7 +85,7 @@ def test_jagged_bias_full_size_sampled():
             b, h, batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, cfg.scale, cfg.causal,
             dout=batch.dout, jagged_bias=(batch.jbias, batch.jbias_offsets))
         sl = slice(qo[b], qo[b + 1])
-        compare_out_lse(res["out"][sl, h], res["lse"][h, sl], o, lse, f"b={b} h={h}", with_rounding=True)
+        compare_out_lse(res["out"][sl, h], res["lse"][h, sl], o, lse, f"b={b} h={h}")
         for gname, g, r in (("dq", res["dq"][sl, h], dq), ("dk", res["dk"][sl, h], dk), ("dv", res["dv"][sl, h], dv)):
             e = rel_frob(g, r)
             assert e <= GRAD_RTOL, f"b={b} h={h} {gname} rel err {e:.3g}"
