@@ -1,9 +1,10 @@
 """Build the C-ABI shared library in-tree with nvcc for sm_103a.
 
-Each translation unit under csrc/ is compiled in parallel, then linked (with the
-static CUDA runtime, so the library has no link-time dependency on libcuda or a
-particular libcudart) into `_lib/libjfa_gb300.so`.  Rebuilds only when a source
-or header is newer than the library.
+Each translation unit under csrc/ is compiled in parallel, then linked against the
+shared CUDA runtime (libcudart from the toolkit that compiled it, found through an
+rpath; the driver API is reached through the runtime's entry-point query, so there is
+no link-time dependency on libcuda) into `_lib/libjfa_gb300.so`.  Rebuilds only when a
+source or header is newer than the library.
 """
 from __future__ import annotations
 

@@ -14,9 +14,9 @@
 
 namespace jfa {
 namespace {
-
 thread_local int g_last_launches = 0;
 thread_local char g_last_error[256] = "";
+}  // namespace
 
 // Record which CUDA call failed (readable through jfa_last_error) and map it to JFA_ERR_CUDA.
 jfa_status cuda_fail(cudaError_t e, const char* where) {
@@ -24,6 +24,8 @@ jfa_status cuda_fail(cudaError_t e, const char* where) {
                 cudaGetErrorString(e));
   return JFA_ERR_CUDA;
 }
+
+namespace {
 #define JFA_CHECK_LAUNCH(call, where)            \
   do {                                           \
     cudaError_t e_ = (call);                     \
@@ -324,6 +326,10 @@ const char* jfa_status_string(jfa_status s) {
 int jfa_last_launch_count(void) { return g_last_launches; }
 
 const char* jfa_last_error(void) { return g_last_error; }
+
+uint64_t jfa_wait_limit_ns(int64_t planned_tile_pairs, int ctas, int64_t max_item_tile_pairs) {
+  return wait_limit_ns(planned_tile_pairs, ctas, max_item_tile_pairs);
+}
 
 jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_stream_t stream) {
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return JFA_ERR_WORKSPACE;

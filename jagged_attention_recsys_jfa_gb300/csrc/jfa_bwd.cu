@@ -2,7 +2,11 @@
 //
 // The gradients of sum(dO * O) (standard FlashAttention-2 backward, the lineage
 // "Jagged Flash Attention (JFA)" builds on) computed in the split scheme of "Four
-// generations" item 2 -- no atomics anywhere:
+// generations" item 2 -- no atomics on dQ, dK or dV: every gradient tile has exactly one
+// writer.  (The one exception is the optional relative-position table gradient, whose
+// per-warp diagonal sums are added into the caller's table with fp32 reductions in L2;
+// its last bits can therefore differ between calls, while dQ, dK and dV are
+// bit-reproducible.)
 //   preprocess   D_i = sum_c dO_ic O_ic                            (HBM-bound)
 //   dK/dV pass   one CTA work item per (sequence, head, key tile); loops over the
 //                query tiles that see it: S^T = K Q^T, P^T = exp(S^T - lse),
@@ -11,12 +15,15 @@
 //                dQ tile: S = Q K^T, P, dP = dO V^T, dS = P o (dP - D), dQ += dS K
 // Rows past a sequence end arrive as zeros (per-sequence tensor maps); padded query
 // rows carry lse = D = 0, so they add nothing to dK/dV, and padded key rows add
-// nothing to dQ.  Both passes are persistent (grid = #SMs) over longest-first lists
-// and warp specialised: warp 0 loads (TMA), warp 1 issues tcgen05 MMAs, warps 2-9
-// are two warpgroups that split the 128 columns of each S/dP tile (64 each).
-// TMEM: S [0,128), dP [128,256), two d-column accumulators from 256.  P and dS are
-// written back as bf16 over the S / dP columns the warpgroup owns and feed the
-// accumulating MMAs straight from TMEM.
+// nothing to dQ.  The passes are persistent (grid = #SMs) over longest-first lists and
+// warp specialised, 16 warps: warpgroup 0 holds the roles (warp 0 streams tiles with
+// TMA, warp 1 issues the tcgen05 MMAs and owns TMEM, warp 2 loads the item's resident
+// tiles, warp 3 claims work items and publishes them to the others); warpgroups 1 and 2
+// split the 128 columns of each S/dP tile (64 each); warpgroup 3 is the epilogue, which
+// drains the finished accumulators from TMEM and writes the gradient rows while the
+// compute warpgroups start the next tile.  TMEM: S [0,128), dP [128,256), two d-column
+// accumulators from 256.  P and dS are written back as bf16 over the S / dP columns the
+// warpgroup owns and feed the accumulating MMAs straight from TMEM.
 #include <cuda_bf16.h>
 
 #include "jfa_internal.h"
@@ -57,6 +64,7 @@ struct BwdParams {
   const int* n_items;
   int* claim;  // the list's claim counter (zeroed by the planner)
   int* status;
+  const uint64_t* wait_ns;  // the planner's bounded-wait limit for this launch
   const float* lse2;    // [H][qpad_cap]  -lse * log2(e), padded per sequence to 128 rows
   const float* delta;   // [H][qpad_cap]  -D, same layout
   const int64_t* qpad;  // [B+1] sequence offsets in the padded vectors
@@ -465,6 +473,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
+  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
             tmap_acquire(mk.map);
             tmap_acquire(mv.map);
           }
-          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
           trace_event(p.trace, kTraceLoader, tn, 1);
           mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
           load_tile<D>(sK, mk.map, &kv_full, wi.h * D, mk.y);
@@ -544,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       auto fill = [&](const TileMap& m, int col, const float* l2src, const float* dsrc) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
         if (m.tail) tmap_acquire(m.map);
-        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) return false;
         trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes + (l2src ? 2 * kBM * 4 : 0));
         load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
@@ -608,7 +617,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        if (!mbar_wait(bar, par, abort_flag, cta_wait_ns())) return false;
         tc_fence_after();
         return true;
       };
@@ -743,13 +752,13 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         }
         // Q_i's ring slot carries this tile's lse2 / D vectors: wait for it
         const uint32_t nq = ring_n + 1;
-        if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         ring_n += 2;
         const float* vec = sVec + (qtile_n % C::kVecSlots) * 256;
         ++qtile_n;
         const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(vec + 64 * w);  // -lse2 pairs
         const uint64_t* ndvec = reinterpret_cast<const uint64_t*>(vec + 128 + 64 * w);  // -D pairs
-        if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&st_full, tile_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
         float x[64];
@@ -799,7 +808,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         tc_fence_before();
         mbar_arrive(&p_full);
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
-        if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
@@ -875,10 +884,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         }
         continue;
       }
-      if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       tc_fence_after();
       drain_acc_rows<D>(tmem + lane_addr + C::kColA1, 1.f, dv_row, valid, &dv_empty);
-      if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
       drain_acc_rows<D>(tmem + lane_addr + C::kColA0, p.scale, dk_row, valid, &dk_empty);
@@ -945,6 +954,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
+  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -982,7 +992,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
           tmap_acquire(mq.map);
           tmap_acquire(mdo.map);
         }
-        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
         load_tile<D>(sQ, mq.map, &qdo_full, wi.h * D, mq.y);
@@ -1021,7 +1031,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       auto fill = [&](const TileMap& m, int col) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
         if (m.tail) tmap_acquire(m.map);
-        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) return false;
         trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
         load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
@@ -1069,7 +1079,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        if (!mbar_wait(bar, par, abort_flag, cta_wait_ns())) return false;
         tc_fence_after();
         return true;
       };
@@ -1199,7 +1209,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
             prefetch_l2(brow_i + jj0 + kBN + 56);
           }
         }
-        if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&s_full, tile_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
         float x[64];
@@ -1254,7 +1264,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
         for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P
         const uint32_t g = tile_n;
         const uint32_t tP = tmem + lane_addr + colP(g) + 64 * w;
-        if (!mbar_wait(&dp_full[g & 1], (g >> 1) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&dp_full[g & 1], (g >> 1) & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
@@ -1301,7 +1311,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
         for (int c0 = 0; c0 < D; c0 += 32) store_acc_row<32>(0, 0.f, dq_row + c0, valid, true);
         continue;
       }
-      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
       drain_acc_rows<D>(tmem + lane_addr + C::kColDQ, p.scale, dq_row, valid, &acc_empty);
@@ -1377,6 +1387,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
+  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1419,7 +1430,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
           }
           const float* l2src = p.lse2 + int64_t(wi.h) * p.qpad_cap + wi.qp;
           const float* dsrc = p.delta + int64_t(wi.h) * p.qpad_cap + wi.qp;
-          if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+          if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
           trace_event(p.trace, kTraceLoader, tn, 1);
           mbar_arrive_expect_tx(&q_full, 2 * C::kTileBytes + 2 * kBM * 4);
           load_tile<D>(sQ, mq.map, &q_full, wi.h * D, mq.y);
@@ -1452,7 +1463,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
             const TileMap m = tile_map(p.maps, p.B, kv ? kMapV : kMapK, wi.b, wi.ko, kt, p.total_kv);
             if (m.tail) tmap_acquire(m.map);
             const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
-            if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+            if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
             trace_event(p.trace, kTraceProducer, tn, 2);
             mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
             load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], wi.h * D, m.y);
@@ -1475,7 +1486,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
       uint32_t ring_n = 0, item_n = 0, g = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        if (!mbar_wait(bar, par, abort_flag, cta_wait_ns())) return false;
         tc_fence_after();
         return true;
       };
@@ -1591,7 +1602,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
      const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
      const bool live = any_visible(it.u0, it.u1, Lq, Lk);
-     if (live && !__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs))) {
+     if (live && !__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, cta_wait_ns()))) {
        ok = false;
        break;
      }
@@ -1607,7 +1618,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
                             Lq - 64 * w, Lk - kj0, lane);
       }
       // ---- P^T = exp2(S^T * scale * log2e (+ bias) - lse2), 0 on padding and hidden pairs
-      if (!mbar_wait(&st_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&st_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       tc_fence_after();
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
       float x[64];
@@ -1650,9 +1661,9 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
       mbar_arrive(&p_full);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
       // ---- dS^T = P^T o (dP^T - D) -> shared memory (keys x queries, 128-byte swizzle)
-      if (!mbar_wait(&dpt_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dpt_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       tc_fence_after();
-      if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       // bias gradient: diagonal sums of this warp's dS^T (as in dbias_warp_tile, one column
       // half at a time); hidden and padded pairs have P^T = 0, so dS^T = 0 there
       float db_straight[2] = {0.f, 0.f}, db_wrapped[2] = {0.f, 0.f};
@@ -1750,10 +1761,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
         store_acc_row_own<D>(0, 0.f, dv_row, valid, true);
         continue;
       }
-      if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dv_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       tc_fence_after();
       drain_row_own<D>(tmem + lane_addr + C::kColFdV, 1.f, dv_row, valid, &dv_empty);
-      if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&dk_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       tc_fence_after();
       drain_row_own<D>(tmem + lane_addr + C::kColP, p.scale, dk_row, valid, &dk_empty);
       ++g;
@@ -1762,7 +1773,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
      const bool qvalid = row < Lq;
      __nv_bfloat16* dq_row = p.g2 + ((it.qo + row) * p.H + it.h) * int64_t(D);
      if (live) {
-       if (!mbar_wait(&dq_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+       if (!mbar_wait(&dq_full, item_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
        ++item_n;
        tc_fence_after();
        drain_row_own<D>(tmem + lane_addr + C::kColFdQ, p.scale, dq_row, qvalid, &dq_empty);
@@ -1810,6 +1821,8 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   WsHeader* mh = reinterpret_cast<WsHeader*>(w);
   bp.claim = pass == kPassDq ? &mh->claim_dq : pass == kPassFused ? &mh->claim_fused : &mh->claim_dkv;
   bp.status = &reinterpret_cast<WsHeader*>(w)->status;
+  // list kinds of the planner: forward 0, dQ 1, dK/dV 2, fused 3
+  bp.wait_ns = &hdr->wait_ns[pass == kPassDq ? 1 : pass == kPassFused ? 3 : 2];
   (void)lse;
   bp.lse2 = reinterpret_cast<const float*>(w + L.lse2);
   bp.delta = reinterpret_cast<const float*>(w + L.delta);

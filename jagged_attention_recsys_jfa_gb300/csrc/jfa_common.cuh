@@ -13,7 +13,25 @@ constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;  // key rows per tile
 constexpr int kMaxBuckets = 8192;
 constexpr int kCostBuckets = 2048;  // planner's counting-sort buckets (cost clamped)
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded pipeline waits: 2 s
+// Bounded pipeline waits.  A wait that outlasts its limit ends the CTA with
+// JFA_ERR_TIMEOUT, so the limit must exceed any wait a correct launch can have.  The
+// longest legitimate waits are item hand-offs: a CTA's scheduler waits for item k - 2 to
+// be released, i.e. for up to about a CTA's whole share of the launch.  The planner
+// therefore sizes each list's limit from the work it planned: a 2 s floor plus a generous
+// time per tile pair (kWaitNsPerTilePair, ~30x the measured ~1 us per 128x128 tile pair
+// on one SM) for one CTA's share of the pairs and the costliest single item on top.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // floor: 2 s
+constexpr uint64_t kWaitNsPerTilePair = 32000ull;    // 32 us per planned tile pair
+constexpr uint64_t kWaitLimitCapNs = 3600ull * 1000000000ull;  // an hour: no overflow
+__host__ __device__ inline uint64_t wait_limit_ns(long long total_pairs, int ctas, long long max_item_pairs) {
+  if (ctas < 1) ctas = 1;
+  if (total_pairs < 0) total_pairs = 0;
+  if (max_item_pairs < 0) max_item_pairs = 0;
+  const unsigned long long per_cta = (unsigned long long)((total_pairs + ctas - 1) / ctas) + max_item_pairs;
+  const unsigned long long cap_pairs = kWaitLimitCapNs / kWaitNsPerTilePair;
+  const uint64_t extra = per_cta >= cap_pairs ? kWaitLimitCapNs : per_cta * kWaitNsPerTilePair;
+  return kWaitTimeoutNs + extra;
+}
 
 // Persistent tensor-core kernels: 3 warpgroups.  Warpgroup 0 = TMA producer (warp 0),
 // tcgen05 issuer and TMEM owner (warp 1), two idle warps; warpgroups 1 and 2 = the
@@ -99,7 +117,11 @@ struct WsHeader {
   int n_fused;     // number of fused short-query backward items
   // next unclaimed item of each list (forward, dQ, dK/dV, fused), zeroed by the planner
   int claim_fwd, claim_dq, claim_dkv, claim_fused;
-  int pad[53];
+  int pad0;
+  // bounded-wait limit of the kernel that walks each list (forward, dQ, dK/dV, fused), in
+  // ns, from wait_limit_ns over the list's planned tile pairs (written by the planner)
+  uint64_t wait_ns[4];
+  int pad[44];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -194,6 +216,18 @@ __host__ __device__ inline void q_tiles_for_kv_tile(int t, int Lq, int Lk, bool 
 }
 
 #ifdef __CUDACC__
+// This CTA's bounded-wait limit for the launch, read from the planner's per-list value by
+// set_cta_wait_ns (between the kernel's griddepcontrol.wait and the CTA-wide barrier that
+// precedes its first pipeline wait); never below the kWaitTimeoutNs floor.
+__shared__ uint64_t cta_wait_ns_sh;
+__device__ __forceinline__ uint64_t cta_wait_ns() { return cta_wait_ns_sh; }
+__device__ __forceinline__ void set_cta_wait_ns(const uint64_t* planned) {
+  if (threadIdx.x == 0) {
+    const uint64_t w = planned ? *planned : 0;
+    cta_wait_ns_sh = w > kWaitTimeoutNs ? w : kWaitTimeoutNs;
+  }
+}
+
 // The tensor map and box row coordinate that load row tile `t` of a sequence starting at
 // row `row0` of a tensor with `total` rows: the sequence's own map, or the tail map when
 // the 128-row box would reach past the tensor's last row (such a tile is always the

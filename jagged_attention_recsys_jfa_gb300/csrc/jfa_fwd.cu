@@ -56,6 +56,7 @@ struct FwdParams {
   const int* n_items;
   int* claim;  // the list's claim counter (zeroed by the planner)
   int* status;
+  const uint64_t* wait_ns;  // the planner's bounded-wait limit for this launch
   __nv_bfloat16* out;
   float* lse;
   TraceBuf trace;
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
+  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         }
         if (q0.tail) tmap_acquire(q0.map);
         if (q1.tail && q1.map != q0.map) tmap_acquire(q1.map);
-        if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&q_full, (it.has1 ? 2 : 1) * C::kTileBytes);
 #pragma unroll
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t e = ring_n % C::kStages, ph = (ring_n / C::kStages) & 1;
-            if (!mbar_wait(&kv_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+            if (!mbar_wait(&kv_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
             trace_event(p.trace, kTraceProducer, tn, 2);
             mbar_arrive_expect_tx(&kv_full[e], C::kTileBytes);
             uint8_t* dst = sRing + e * C::kTileBytes;
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const int nkv[2] = {it.nkv0, it.nkv1};
-        if (!mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&q_full, item_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         ++item_n;
         tc_fence_after();
         trace_event(p.trace, kTraceMma, tn, 10);
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
                     (acc || kk > 0) ? 1u : 0u);
         };
         auto wait_full = [&](uint32_t n) -> bool {
-          const bool r = mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, kWaitTimeoutNs);
+          const bool r = mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, cta_wait_ns());
           tc_fence_after();
           return r;
         };
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           bool k_ready = false;
           for (int s = 0; s < 2 && ok; ++s) {
             if (j < nkv[s]) {
-              if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+              if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
               ++p_n[s];
               tc_fence_after();
               trace_event(p.trace, kTraceMma, tn, 12 + s);
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             prefetch_l2(brow_j + kvj + kBN + 64);
           }
         }
-        if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
         ++s_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 20);
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, lse = ln(sum) = (m + log2 l) * ln 2
-      if (!mbar_wait(&o_full[s], o_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(&o_full[s], o_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
       ++o_n;
       tc_fence_after();
       if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 22);
@@ -624,6 +626,7 @@ cudaError_t launch_forward(const Problem& pr, void* ws, const WsLayout& L, void*
   fp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_fwd;
   fp.claim = &reinterpret_cast<WsHeader*>(w)->claim_fwd;
   fp.status = &reinterpret_cast<WsHeader*>(w)->status;
+  fp.wait_ns = &reinterpret_cast<const WsHeader*>(w)->wait_ns[0];
   fp.out = static_cast<__nv_bfloat16*>(out);
   fp.lse = lse;
   fp.trace = pr.trace[JFA_KERNEL_FORWARD];

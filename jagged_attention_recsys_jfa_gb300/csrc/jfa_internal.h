@@ -31,6 +31,10 @@ struct PlanMaps {
   int used[kNumMapSlots];
 };
 
+// Record which CUDA call failed (what jfa_last_error then returns, for the calling thread)
+// and return JFA_ERR_CUDA.
+jfa_status cuda_fail(cudaError_t e, const char* where);
+
 // setmaxnreg.inc waits until the registers it asks for are free, so a kernel that
 // rebalances registers must be launched with the full allocation the split assumes.
 // Checked once per kernel before its first launch: a build that lowered the kernel's

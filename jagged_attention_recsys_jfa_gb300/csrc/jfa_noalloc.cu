@@ -30,11 +30,15 @@ void* g_scratch_addr[kMaxDevices] = {};
 // device (with that device current) and cached.
 jfa_status scratch_address(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return JFA_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return jfa::cuda_fail(e, "jfa_forward_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return jfa::cuda_fail(cudaErrorInvalidDevice, "jfa_forward_noalloc: device index");
   std::lock_guard<std::mutex> g(g_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return JFA_ERR_CUDA;
+    const cudaError_t es = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (es != cudaSuccess) return jfa::cuda_fail(es, "jfa_forward_noalloc: cudaGetSymbolAddress");
+    if (p == nullptr) return jfa::cuda_fail(cudaErrorInvalidSymbol, "jfa_forward_noalloc: scratch address");
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -53,9 +57,14 @@ extern "C" jfa_status jfa_forward_noalloc(const void* q, const void* k, const vo
   void* ws = nullptr;
   const jfa_status st = scratch_address(&ws);
   if (st != JFA_OK) return st;
-  // The planner rewrites everything the forward reads from the scratch (status word,
-  // item count, work list, tensor maps, scaled bias) at the start of each call, so
-  // the previous call's contents need no clearing.
+  // The planner rewrites everything the forward kernels read from the scratch (item
+  // counts, claim counters, work list, tensor maps, scaled bias) at the start of each
+  // call, so the previous call's contents need no clearing.  The status word is the
+  // exception: the planner only sets it when an error is found (compare-and-swap from 0)
+  // and nothing here reads or clears it, so in this shared array the first device-side
+  // error stays latched for the life of the process.  No kernel reads the word (aborts
+  // travel through per-CTA shared memory), so a latched error changes no result; callers
+  // of this entry point simply get no device-side error report.
   return jfa_forward(q, k, v, q_offsets, kv_offsets, B, H, d, total_q, total_kv, bias, scale, causal, out, lse,
                      ws, kNoAllocScratchBytes, stream);
 }

@@ -153,15 +153,27 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
     }
     return;
   }
+  __shared__ unsigned long long max_item;
+  if (tid == 0) max_item = 0;
+  __syncthreads();
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
+    unsigned long long mx = 0;
     for_each_range(kind, Lq, Lk, causal, range_cap, [&](int u0, int u1, long long cost) {
       const int pos = atomicAdd(&base[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
       for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u0, u1};
+      if ((unsigned long long)cost > mx) mx = (unsigned long long)cost;
     });
+    if (mx) atomicMax(&max_item, mx);
   }
-  if (tid == 0) *count_out = total;
+  __syncthreads();
+  if (tid == 0) {
+    *count_out = total;
+    // the bounded waits of the kernel that walks this list scale with the planned work
+    reinterpret_cast<WsHeader*>(p.ws)->wait_ns[kind] =
+        wait_limit_ns(total_cost * p.H, p.grid, (long long)max_item);
+  }
   __syncthreads();
 }
 

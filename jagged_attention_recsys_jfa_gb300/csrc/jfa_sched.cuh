@@ -49,7 +49,7 @@ __device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items,
   for (uint32_t k = 0;; ++k) {
     if (k >= 2) {
       const uint32_t kp = k - 2;
-      if (!mbar_wait(&r.empty[kp % kMetaSlots], (kp / kMetaSlots) & 1, abort, kWaitTimeoutNs)) return false;
+      if (!mbar_wait(&r.empty[kp % kMetaSlots], (kp / kMetaSlots) & 1, abort, cta_wait_ns())) return false;
     }
     const int idx = atomicAdd(claim, 1);
     ItemMeta m;
@@ -90,7 +90,7 @@ __device__ __forceinline__ const ItemMeta* meta_peek_next(MetaRing& r, uint32_t 
 // Entry k for a single-thread role, read in place for the item's duration and then
 // freed with meta_release.
 __device__ __forceinline__ bool meta_wait(MetaRing& r, uint32_t k, volatile int* abort) {
-  return mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, kWaitTimeoutNs);
+  return mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, cta_wait_ns());
 }
 __device__ __forceinline__ void meta_release(MetaRing& r, uint32_t k) { mbar_arrive(&r.empty[k % kMetaSlots]); }
 
@@ -99,7 +99,7 @@ __device__ __forceinline__ void meta_release(MetaRing& r, uint32_t k) { mbar_arr
 // outcome: a lane whose wait gave up has raised the abort flag, which ends the other
 // lanes' waits too.
 __device__ __forceinline__ bool meta_wait_warp(MetaRing& r, uint32_t k, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, kWaitTimeoutNs));
+  return __all_sync(0xffffffffu, mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, cta_wait_ns()));
 }
 __device__ __forceinline__ void meta_release_warp(MetaRing& r, uint32_t k) {
   __syncwarp();

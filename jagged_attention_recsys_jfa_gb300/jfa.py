@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
 # Every symbol include/jfa.h declares.
 EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_forward_noalloc", "jfa_backward", "jfa_check_status",
                     "jfa_status_string", "jfa_last_launch_count", "jfa_last_error", "jfa_timing_enable",
-                    "jfa_timing_read", "jfa_trace_configure", "jfa_selftest_wait_timeout")
+                    "jfa_timing_read", "jfa_trace_configure", "jfa_selftest_wait_timeout", "jfa_wait_limit_ns")
 KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq", "bwd_fused")
 
 
@@ -89,6 +89,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.jfa_timing_read.restype = i32
     lib.jfa_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     lib.jfa_selftest_wait_timeout.restype = i32
+    lib.jfa_wait_limit_ns.argtypes = [i64, i32, i64]
+    lib.jfa_wait_limit_ns.restype = ctypes.c_uint64
     lib.jfa_trace_configure.argtypes = [vp, sz, i32]
     lib.jfa_trace_configure.restype = i32
     _LIB = lib
@@ -118,6 +120,25 @@ def _check_values(name, t, rows=None, H=None, d=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [*, {H}, {d}]")
     if rows is not None and t.shape[0] != rows:
         raise ValueError(f"{name} has {t.shape[0]} rows, expected {rows}")
+
+
+def _check_lse(t, H, Tq):
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != (H, Tq)
+            or not t.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous float32 CUDA tensor [{H}, {Tq}]")
+
+
+def _check_workspace(ws, nbytes, device):
+    """A caller-given workspace: contiguous bytes on the inputs' device, at least `nbytes`
+    long (its size is passed to the library in bytes, whatever its dtype)."""
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or ws.device != device or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor on the inputs' device")
+    have = ws.numel() * ws.element_size()
+    if have < nbytes:
+        raise ValueError(f"workspace holds {have} bytes, the call needs {nbytes}")
+    if ws.data_ptr() % 256:
+        raise ValueError("workspace must start on a 256-byte boundary")
+    return have
 
 
 def _check_offsets(name, off):
@@ -199,17 +220,25 @@ def jfa_forward(q, k, v, q_offsets, kv_offsets, bias=None, bias_center=0, scale=
         raise ValueError("q_offsets and kv_offsets must have the same length")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     bstruct, bias_keep = _bias_struct(bias, bias_center, H, jagged_bias=jagged_bias)
+    for name, t in (("k", k), ("v", v), ("q_offsets", q_offsets), ("kv_offsets", kv_offsets)):
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     if out is None:
         out = torch.empty_like(q)
+    else:
+        _check_values("out", out, rows=Tq, H=H, d=d)
     if lse is None:
         lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    else:
+        _check_lse(lse, H, Tq)
     nbytes = int(lib.jfa_workspace_size(B, H, d, Tq, k.shape[0], 0))
     if workspace is None:
         workspace = _workspace(nbytes, q.device)
+    ws_bytes = _check_workspace(workspace, nbytes, q.device)
     st = lib.jfa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), q_offsets.data_ptr(), kv_offsets.data_ptr(),
                          B, H, d, Tq, k.shape[0], ctypes.byref(bstruct) if bstruct is not None else None,
                          scale, 1 if causal else 0, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
-                         workspace.numel(), _stream_handle(stream))
+                         ws_bytes, _stream_handle(stream))
     if st != JFA_OK:
         raise JfaError(st, "jfa_forward")
     del bias_keep
@@ -228,23 +257,34 @@ def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias
     Tq, H, d = q.shape
     for name, t, rows in (("dout", dout, Tq), ("out", out, Tq), ("k", k, None), ("v", v, k.shape[0])):
         _check_values(name, t, rows=rows, H=H, d=d)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, Tq) or not lse.is_contiguous() or not lse.is_cuda:
-        raise ValueError("lse must be a contiguous float32 CUDA tensor [H, Tq]")
+    _check_lse(lse, H, Tq)
     _check_offsets("q_offsets", q_offsets)
     _check_offsets("kv_offsets", kv_offsets)
     B = q_offsets.numel() - 1
+    if kv_offsets.numel() != B + 1:
+        raise ValueError("q_offsets and kv_offsets must have the same length")
+    for name, t in (("dout", dout), ("k", k), ("v", v), ("out", out), ("lse", lse), ("q_offsets", q_offsets),
+                    ("kv_offsets", kv_offsets)):
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     bstruct, bias_keep = _bias_struct(bias, bias_center, H, bias_grad, jagged_bias, jagged_bias_grad)
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t is not None:
+            _check_values(name, t, rows=ref.shape[0], H=H, d=d)
+            if t.device != q.device:
+                raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     nbytes = int(lib.jfa_workspace_size(B, H, d, Tq, k.shape[0], 1))
     if workspace is None:
         workspace = _workspace(nbytes, q.device)
+    ws_bytes = _check_workspace(workspace, nbytes, q.device)
     st = lib.jfa_backward(dout.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                           lse.data_ptr(), q_offsets.data_ptr(), kv_offsets.data_ptr(), B, H, d, Tq, k.shape[0],
                           ctypes.byref(bstruct) if bstruct is not None else None, scale, 1 if causal else 0,
-                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), ws_bytes,
                           _stream_handle(stream))
     if st != JFA_OK:
         raise JfaError(st, "jfa_backward")

@@ -116,3 +116,29 @@ def test_python_binding_checks_bias_arguments():
         jfa.jfa._bias_struct(None, 0, H, jagged_bias_grad=values)
     with pytest.raises(ValueError):   # a table gradient needs a table
         jfa.jfa._bias_struct(None, 0, H, grad=table)
+
+
+def test_wait_limit_scales_with_planned_work():
+    """The bounded-wait limit the planner gives each launch: 2 s for small launches, then
+    32 us per tile pair of one CTA's share plus the costliest item, so a launch of any size
+    stays far inside it (a correct launch's longest wait is about one CTA's share)."""
+    lib = jfa.load_library()
+    f = lib.jfa_wait_limit_ns
+    floor, per_pair = 2_000_000_000, 32_000
+    assert f(0, 152, 0) == floor
+    assert f(-5, 0, -1) == floor                          # clamped arguments
+    assert f(152, 152, 0) == floor + per_pair             # one pair per CTA
+    assert f(153, 152, 0) == floor + 2 * per_pair         # share rounded up
+    assert f(1000, 1, 7) == floor + 1007 * per_pair       # ctas < 1 would count as 1
+    assert f(1000, 0, 7) == floor + 1007 * per_pair
+    # the gem_self forward plans ~45k pairs over 8 heads' items on 152 CTAs: the floor
+    # dominates; a launch 10^4 times larger (about 10 s of work per CTA) gets minutes
+    small = f(45_000, 152, 64)
+    assert floor < small < floor + 20_000_000
+    big = f(450_000_000, 152, 5000)
+    share_s = 450_000_000 / 152 * 1e-6                    # ~1 us per pair: ~3 s per CTA
+    assert big * 1e-9 > 20 * share_s
+    # monotone in each argument and capped without overflow
+    assert f(10**6, 152, 10) < f(2 * 10**6, 152, 10) and f(10**6, 152, 10) < f(10**6, 152, 11)
+    assert f(10**6, 76, 10) > f(10**6, 152, 10)
+    assert f(2**62, 1, 2**62) == floor + 3600 * 10**9

@@ -89,3 +89,47 @@ def test_bias_grad_full_size_one_head():
     ref = _oracle_dbias(batch, heads=[h])
     e = rel_frob(res["dbias"][h], ref[h])
     assert e <= GRAD_RTOL, f"full size head {h}: dbias relative error {e:.3g}"
+
+
+def test_bias_grad_run_to_run_drift_is_bounded():
+    """dq, dk and dv are bit-identical across calls; the table gradient is summed with fp32
+    reductions in L2 whose order is not fixed, so it may drift in its last bits.  The bound
+    checked here is rigorous: each entry is the fp32 sum of m partial sums c_k, each a
+    fixed-order fp32 sum over pairs of that bucket, so two orders differ by at most
+    2 (m - 1) u sum_k |c_k| <= 2 m u A, with u = 2^-24, m <= the bucket's visible pair count
+    and A = sum |dS_ij| over those pairs (from the oracle, plus 5% for the GPU's bf16-input
+    dS differing from the oracle's and for the rounding of the partial sums themselves).
+    The observed drift is printed."""
+    cfg = dataclasses.replace(CONFIGS["biased_causal"], batch=6)
+    batch = make_batch(cfg, device="cuda")
+    runs = [_run(batch) for _ in range(4)]
+    for r in runs[1:]:
+        for name in ("dq", "dk", "dv"):
+            assert torch.equal(r[name], runs[0][name]), f"{name} differs between calls"
+    # A and m per (head, bucket) from the oracle's dS
+    qo, ko = batch.q_offsets.cpu().numpy(), batch.kv_offsets.cpu().numpy()
+    H, nb = batch.bias.shape
+    q, k, v, do = (orc.to_f64(t) for t in (batch.q, batch.k, batch.v, batch.dout))
+    table = orc.to_f64(batch.bias)
+    A = np.zeros((H, nb))
+    m = np.zeros((H, nb))
+    for b in range(qo.size - 1):
+        Lq, Lk = int(qo[b + 1] - qo[b]), int(ko[b + 1] - ko[b])
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lk)[None, :]
+        idx = np.clip(j - i + cfg.bias_center, 0, nb - 1)
+        vis = orc.causal_visible(Lq, Lk)
+        for h in range(H):
+            bias = orc.relpos_bias(table[h], Lq, Lk, cfg.bias_center)
+            ds, _ = orc.sequence_score_grad(do[qo[b]:qo[b + 1], h], q[qo[b]:qo[b + 1], h], k[ko[b]:ko[b + 1], h],
+                                            v[ko[b]:ko[b + 1], h], cfg.scale, bias, vis)
+            A[h] += np.bincount(idx[vis], weights=np.abs(ds[vis]), minlength=nb)
+            m[h] += np.bincount(idx[vis], minlength=nb)
+    bound = 2.0 * m * 2.0 ** -24 * A * 1.05
+    g0 = runs[0]["dbias"].double().cpu().numpy()
+    worst = 0.0
+    for r in runs[1:]:
+        diff = np.abs(r["dbias"].double().cpu().numpy() - g0)
+        assert np.all(diff <= bound), f"drift {diff.max():.3g} beyond its bound at {np.unravel_index(np.argmax(diff - bound), diff.shape)}"
+        worst = max(worst, float((diff / np.maximum(np.abs(g0).max(axis=1, keepdims=True), 1e-30)).max()))
+    print(f"bias-table gradient: max run-to-run drift = {worst:.3g} of the head's largest entry")
