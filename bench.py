@@ -14,9 +14,17 @@ backward that writes the bias's gradient as well, timed against the plain backwa
 step itself holds the bias constant).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl jfa|reference]
+                  [--no-configs] [--shard]
+
+The JSON line is the headline workload (--config, gem_self by default); at N=1 its
+`configs` key then holds every other workload (tiny, cross, biased_causal,
+longtail_causal, jagged_bias_causal), each timed the same way on the same GPU with its
+forward / backward split, per-kernel roofline and the padded dense SDPA comparison.
 
 Multi-GPU (torchrun, one process per GPU): every rank runs its own batch of the same
-workload (independent problems, no collective on the data path): weak scaling.
+workload (independent problems, no collective on the data path): weak scaling.  With
+--shard the ranks split ONE batch by sequence instead (longest-processing-time over
+visited pairs, sharding.py): strong scaling, still no collective on the data path.
 """
 from __future__ import annotations
 
@@ -87,7 +95,10 @@ def workload_flops(batch):
 
 def workload_bytes(batch):
     """Algorithmic DRAM bytes per launch of each kernel: every input read once, every
-    output written once (the per-query lse / D vectors on 128-row-padded rows)."""
+    output written once (the per-query lse / D vectors on 128-row-padded rows).  A general
+    jagged bias counts 2 bytes per visited (query, key) pair and head for each pass that
+    covers its sequence: the elements the method reads (causally hidden pairs and the row
+    padding are never needed)."""
     H, d = batch.cfg.heads, batch.cfg.head_dim
     row = 2.0 * H * d
     lq, lk = np.asarray(batch.q_lengths), np.asarray(batch.kv_lengths)
@@ -98,8 +109,10 @@ def workload_bytes(batch):
     Tql, Tkl, Tqs, Tks = float(lq[long_].sum()), float(lk[long_].sum()), float(lq[short].sum()), float(lk[short].sum())
     vecl = 8.0 * H * float(((lq[long_] + 127) // 128 * 128).sum())
     vecs = vec - vecl
-    # a general jagged bias is read once by each pass that covers its sequence (bf16 blocks)
-    jb = 2.0 * H * lq * ((lk + 7) // 8 * 8) if batch.cfg.general_bias else 0.0 * lq
+    if batch.cfg.general_bias:
+        jb = np.array([2.0 * H * valid_pairs([a], [b], batch.cfg.causal) for a, b in zip(lq, lk)])
+    else:
+        jb = 0.0 * lq
     jbl, jbs = float(np.sum(jb[long_])), float(np.sum(jb[short]))
     return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq + jbl + jbs,
             "bwd_preprocess": 2 * Tq * row + 4.0 * H * Tq + vec,
@@ -300,236 +313,96 @@ def padded_sdpa(batch, steps):
 
 
 # ----------------------------------------------------------------------------- main arms
-def run_jfa(args, rank, world, device):
-    from jagged_attention_recsys_jfa_gb300 import jfa
+OTHER_CONFIGS = ("tiny", "cross", "biased_causal", "longtail_causal", "jagged_bias_causal")
 
-    name = args.config
-    cfg = CONFIGS[name]
-    batch = make_batch(cfg, device=device, seed=cfg.seed + rank)
-    fl = workload_flops(batch)
-    center = cfg.bias_center if batch.bias is not None else 0
-    out = torch.empty_like(batch.q)
-    lse = torch.empty((cfg.heads, batch.q.shape[0]), dtype=torch.float32, device=device)
-    dq, dk, dv = torch.empty_like(batch.q), torch.empty_like(batch.k), torch.empty_like(batch.v)
-    B, H, d = batch.q_lengths.numel(), cfg.heads, cfg.head_dim
-    Tq, Tk = batch.q.shape[0], batch.k.shape[0]
-    ws_f = jfa.new_workspace(B, H, d, Tq, Tk, False, device)
-    ws_b = jfa.new_workspace(B, H, d, Tq, Tk, True, device)
 
-    jb = (batch.jbias, batch.jbias_offsets) if batch.jbias is not None else None
+def shard_batch(batch, index):
+    """The sequences `index` of a batch as a batch of their own (values packed, offsets
+    rebuilt, a general bias's blocks moved with their sequences; a table is shared)."""
+    import dataclasses
 
-    def fwd(q=batch.q, k=batch.k, v=batch.v, qo=batch.q_offsets, ko=batch.kv_offsets):
-        jfa.jfa_forward(q, k, v, qo, ko, batch.bias, center, cfg.scale, cfg.causal, out=out, lse=lse,
-                        workspace=ws_f, jagged_bias=jb)
+    from jagged_attention_recsys_jfa_gb300.sharding import select_bias_blocks, select_sequences
 
-    def bwd(q=batch.q, k=batch.k, v=batch.v, do=batch.dout, qo=batch.q_offsets, ko=batch.kv_offsets):
-        jfa.jfa_backward(do, q, k, v, out, lse, qo, ko, batch.bias, center, cfg.scale, cfg.causal,
-                         dq=dq, dk=dk, dv=dv, workspace=ws_b, jagged_bias=jb)
+    q, qo = select_sequences(batch.q, batch.q_offsets, index)
+    k, ko = select_sequences(batch.k, batch.kv_offsets, index)
+    v, _ = select_sequences(batch.v, batch.kv_offsets, index)
+    do, _ = select_sequences(batch.dout, batch.q_offsets, index)
+    jb = jbo = None
+    if batch.jbias is not None:
+        jb, jbo = select_bias_blocks(batch.jbias, batch.jbias_offsets, index)
+    idx = torch.as_tensor(list(index), dtype=torch.int64)
+    return dataclasses.replace(batch, q_lengths=batch.q_lengths[idx], kv_lengths=batch.kv_lengths[idx],
+                               q_offsets=qo, kv_offsets=ko, q=q.contiguous(), k=k.contiguous(), v=v.contiguous(),
+                               dout=do.contiguous(), jbias=jb, jbias_offsets=jbo)
 
-    for _ in range(args.warmup):
-        fwd()
-        bwd()
-    st = (jfa.jfa_check_status(ws_f), jfa.jfa_check_status(ws_b))
-    if st != (0, 0):
-        raise RuntimeError(f"device status {st} after warm-up")
-    torch.cuda.synchronize()
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+class Step:
+    """One step of the hot path on one resident batch: jfa_forward then jfa_backward through
+    the public binding, outputs and workspaces allocated once."""
 
-    # ---- timed region: inputs resident in HBM
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(device.index or 0)
-    torch.cuda.reset_peak_memory_stats()
-    mem_base = torch.cuda.memory_allocated()
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    # the timed region: K whole steps, nothing recorded between the kernels
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        fwd()
-        bwd()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    # the same K steps again with events around the forward / backward halves and around
-    # every kernel launch (jfa_timing_enable): the breakdown and the per-kernel roofline
+    def __init__(self, batch, device):
+        from jagged_attention_recsys_jfa_gb300 import jfa
+
+        self.jfa, self.batch, cfg = jfa, batch, batch.cfg
+        self.center = cfg.bias_center if batch.bias is not None else 0
+        self.out = torch.empty_like(batch.q)
+        self.lse = torch.empty((cfg.heads, batch.q.shape[0]), dtype=torch.float32, device=device)
+        self.dq, self.dk, self.dv = torch.empty_like(batch.q), torch.empty_like(batch.k), torch.empty_like(batch.v)
+        B, H, d = batch.q_lengths.numel(), cfg.heads, cfg.head_dim
+        Tq, Tk = batch.q.shape[0], batch.k.shape[0]
+        self.ws_f = jfa.new_workspace(B, H, d, Tq, Tk, False, device)
+        self.ws_b = jfa.new_workspace(B, H, d, Tq, Tk, True, device)
+        self.jb = (batch.jbias, batch.jbias_offsets) if batch.jbias is not None else None
+
+    def fwd(self):
+        b, c = self.batch, self.batch.cfg
+        self.jfa.jfa_forward(b.q, b.k, b.v, b.q_offsets, b.kv_offsets, b.bias, self.center, c.scale, c.causal,
+                             out=self.out, lse=self.lse, workspace=self.ws_f, jagged_bias=self.jb)
+
+    def bwd(self, bias_grad=None, jagged_bias_grad=None):
+        b, c = self.batch, self.batch.cfg
+        self.jfa.jfa_backward(b.dout, b.q, b.k, b.v, self.out, self.lse, b.q_offsets, b.kv_offsets, b.bias,
+                              self.center, c.scale, c.causal, dq=self.dq, dk=self.dk, dv=self.dv,
+                              workspace=self.ws_b, jagged_bias=self.jb, bias_grad=bias_grad,
+                              jagged_bias_grad=jagged_bias_grad)
+
+    def __call__(self):
+        self.fwd()
+        self.bwd()
+
+    def check(self, where):
+        st = (self.jfa.jfa_check_status(self.ws_f), self.jfa.jfa_check_status(self.ws_b))
+        if st != (0, 0):
+            raise RuntimeError(f"device status {st} {where}")
+
+
+def kernel_pass(step, steps, stream):
+    """The K steps again with events around the forward / backward halves and around every
+    kernel launch (jfa_timing_enable): (median forward ms, median backward ms, per kernel
+    {kind: (total ms, launches)})."""
+    jfa = step.jfa
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
     jfa.jfa_timing_read()  # drop anything recorded before
     jfa.jfa_timing_enable(True)
-    for i in range(args.steps):
+    for i in range(steps):
         ev[i][0].record(stream)
-        fwd()
+        step.fwd()
         ev[i][1].record(stream)
-        bwd()
+        step.bwd()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     jfa.jfa_timing_enable(False)
     per_kernel = jfa.jfa_timing_read()
-    peak_mem = torch.cuda.max_memory_allocated() - mem_base
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    st = (jfa.jfa_check_status(ws_f), jfa.jfa_check_status(ws_b))
-    if st != (0, 0):
-        raise RuntimeError(f"device status {st} in the timed region (first error since warm-up)")
+    return fwd_ms, bwd_ms, per_kernel
 
-    # max over ranks of the timed region, sum of work over ranks
-    t_local = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    w_local = torch.tensor([fl["fwd"] + fl["bwd"]], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t_local, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(w_local, op=torch.distributed.ReduceOp.SUM)
-    t_max_s = float(t_local.item()) / 1e3
-    total_flops = float(w_local.item()) * args.steps
-    value = total_flops / t_max_s / 1e12
-    launches = sum(c for _, c in per_kernel.values())
 
-    # ---- the same step captured once in a CUDA graph and replayed: the planner reads the
-    # offsets on the device, so one capture serves every batch of the same shape; replays
-    # drop the per-call host work and launch gaps (what launch-bound small batches gain)
-    side = torch.cuda.Stream(device=device)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        fwd()
-        bwd()
-    stream.wait_stream(side)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        fwd()
-        bwd()
-    for _ in range(3):
-        graph.replay()
-    g_start, g_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    g_start.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    g_end.record(stream)
-    torch.cuda.synchronize()
-    graph_ms = g_start.elapsed_time(g_end) / args.steps
-    st = (jfa.jfa_check_status(ws_f), jfa.jfa_check_status(ws_b))
-    if st != (0, 0):
-        raise RuntimeError(f"device status {st} in the graph replays")
-    del graph
-
-    # ---- bias-table gradient (workloads with a relative-position bias): the same backward
-    # also writing the table's gradient, timed against the plain backward on the same inputs
-    bias_grad = None
-    if batch.bias is not None or batch.jbias is not None:
-        dbias = torch.empty_like(batch.bias) if batch.bias is not None else None
-        djb = torch.empty_like(batch.jbias) if batch.jbias is not None else None
-
-        def bwd_g():
-            jfa.jfa_backward(batch.dout, batch.q, batch.k, batch.v, out, lse, batch.q_offsets, batch.kv_offsets,
-                             batch.bias, center, cfg.scale, cfg.causal, dq=dq, dk=dk, dv=dv, workspace=ws_b,
-                             bias_grad=dbias, jagged_bias=jb, jagged_bias_grad=djb)
-
-        def timed(fn):
-            for _ in range(3):
-                fn()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            a.record(stream)
-            for _ in range(args.steps):
-                fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            return a.elapsed_time(b) / args.steps
-
-        t_plain, t_grad = timed(bwd), timed(bwd_g)
-        jfa.jfa_timing_read()
-        jfa.jfa_timing_enable(True)
-        timed(bwd_g)
-        jfa.jfa_timing_enable(False)
-        pk = jfa.jfa_timing_read()
-        if jfa.jfa_check_status(ws_b) != 0:
-            raise RuntimeError("device status after the bias-gradient backward")
-        bias_grad = {"kind": "relative-position table" if batch.bias is not None else "general jagged bias",
-                     "bwd_ms": round(t_grad, 4), "bwd_ms_without": round(t_plain, 4),
-                     "overhead": round(t_grad / t_plain - 1, 4),
-                     "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in pk.items() if v[1]}}
-
-    # ---- end to end through the public call with host buffers.  Every step copies its
-    # inputs in from pinned host memory and its results (out, lse, dq, dk, dv) back out.
-    # Consecutive steps overlap the way a training loop would run them: the next step's
-    # inputs stream in on one copy stream while this step computes, and its results stream
-    # out on another; device inputs and outputs are double-buffered so no copy touches a
-    # buffer a kernel still uses.
-    pin = lambda t: t.cpu().pin_memory()
-    in_names = ("q", "k", "v", "dout", "q_offsets", "kv_offsets") + (
-        ("jbias", "jbias_offsets") if batch.jbias is not None else ())  # a general bias is per-batch input
-    h_in = {n: pin(getattr(batch, n)) for n in in_names}
-    out_names = ("out", "lse", "dq", "dk", "dv")
-    res = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-    h_out = [{n: torch.empty(res[n].shape, dtype=res[n].dtype, pin_memory=True) for n in out_names}
-             for _ in range(2)]
-    d_in = [{n: torch.empty_like(getattr(batch, n)) for n in h_in} for _ in range(2)]
-    d_out = [{n: torch.empty_like(res[n]) for n in out_names} for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
-    s_comp = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_free = [torch.cuda.Event() for _ in range(2)]
-    used = [False, False]
-
-    def e2e_step(i):
-        b = i & 1
-        with torch.cuda.stream(s_in):
-            if used[b]:
-                s_in.wait_event(ev_done[b])  # the step that last used these inputs has computed
-            for n in h_in:
-                d_in[b][n].copy_(h_in[n], non_blocking=True)
-            ev_in[b].record(s_in)
-        s_comp.wait_event(ev_in[b])
-        if used[b]:
-            s_comp.wait_event(ev_free[b])  # its results have been copied out
-        x, o = d_in[b], d_out[b]
-        xjb = (x["jbias"], x["jbias_offsets"]) if "jbias" in x else None
-        jfa.jfa_forward(x["q"], x["k"], x["v"], x["q_offsets"], x["kv_offsets"], batch.bias, center, cfg.scale,
-                        cfg.causal, out=o["out"], lse=o["lse"], workspace=ws_f, jagged_bias=xjb)
-        jfa.jfa_backward(x["dout"], x["q"], x["k"], x["v"], o["out"], o["lse"], x["q_offsets"], x["kv_offsets"],
-                         batch.bias, center, cfg.scale, cfg.causal, dq=o["dq"], dk=o["dk"], dv=o["dv"],
-                         workspace=ws_b, jagged_bias=xjb)
-        ev_done[b].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[b])
-            for n in out_names:
-                h_out[b][n].copy_(o[n], non_blocking=True)
-            ev_free[b].record(s_out)
-        used[b] = True
-
-    for i in range(max(2, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    # the copied-out results are the resident run's (the kernels are deterministic)
-    if not (torch.equal(h_out[0]["out"], out.cpu()) and torch.equal(h_out[0]["dq"], dq.cpu())):
-        raise RuntimeError("end-to-end results differ from the resident run")
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    t_e2e = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = total_flops / float(t_e2e.item()) / 1e12
-
-    if rank != 0:
-        return None
-
-    peaks, peak_src = load_peaks()
-    # dominant kernel = largest share of the timed region's kernel time
+def roofline_of(batch, name, per_kernel, peaks, peak_src):
+    """Per-kernel algorithmic rates and the roofline of the kernel with the largest time
+    share: tensor-bound when its algorithmic flops per byte reach the ridge of the measured
+    peaks, else HBM-bound."""
+    fl = workload_flops(batch)
     kinds = {k: v for k, v in per_kernel.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
     algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"], "bwd_fused": fl["fused"]}
@@ -537,8 +410,6 @@ def run_jfa(args, rank, world, device):
     ms_dom, n_dom = kinds[dom]
     t_dom = ms_dom / n_dom / 1e3
     traffic = load_traffic(dom, name)
-    # the binding roof: tensor when the kernel's algorithmic flops per byte reach the
-    # ridge of the measured peaks, else HBM
     ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
     if dom in algo and algo_bytes.get(dom, 0) > 0 and algo[dom] / algo_bytes[dom] >= ridge:
         achieved = algo[dom] / t_dom / 1e12
@@ -568,7 +439,280 @@ def run_jfa(args, rank, world, device):
     for k, nb in algo_bytes.items():
         if k in kernels:
             kernels[k]["algorithmic_gbs"] = round(nb / (kernels[k]["ms_per_launch"] / 1e3) / 1e9, 1)
+    return roofline, kernels
 
+
+def split_rates(fl, fwd_ms, bwd_ms, peak_tf):
+    return ({"ms": round(fwd_ms, 4), "tflops": round(fl["fwd"] / (fwd_ms / 1e3) / 1e12, 1),
+             "pct_of_peak": round(100 * fl["fwd"] / (fwd_ms / 1e3) / 1e12 / peak_tf, 2)},
+            {"ms": round(bwd_ms, 4), "tflops": round(fl["bwd"] / (bwd_ms / 1e3) / 1e12, 1),
+             "pct_of_peak": round(100 * fl["bwd"] / (bwd_ms / 1e3) / 1e12 / peak_tf, 2)})
+
+
+def measure_config(name, args, device, peaks, peak_src):
+    """One more workload on this GPU, timed like the headline (warm-up, then `steps` whole
+    steps between two events on the launching stream; inputs larger than L2 or launch-bound),
+    with its forward / backward split, per-kernel roofline and the padded dense SDPA
+    comparison."""
+    cfg = CONFIGS[name]
+    batch = make_batch(cfg, device=device)
+    fl = workload_flops(batch)
+    step = Step(batch, device)
+    for _ in range(args.warmup):
+        step()
+    step.check("after warm-up")
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    fwd_ms, bwd_ms, per_kernel = kernel_pass(step, args.steps, stream)
+    step.check("in the timed region")
+    peak_tf = float(peaks["bf16_tflops"])
+    fwd, bwd = split_rates(fl, fwd_ms, bwd_ms, peak_tf)
+    roofline, kernels = roofline_of(batch, name, per_kernel, peaks, peak_src)
+    value = (fl["fwd"] + fl["bwd"]) / (ms / 1e3) / 1e12
+    res = {"config": config_dict(cfg, name), "value": round(value, 2), "unit": "TFLOPS", "ms_per_step": round(ms, 4),
+           "pct_of_tensor_peak": round(100 * value / peak_tf, 2), "fwd": fwd, "bwd": bwd,
+           "valid_pairs": fl["pairs"], "roofline": roofline, "kernels": kernels,
+           "gpu_launches": sum(c for _, c in per_kernel.values())}
+    if not args.no_sdpa:
+        del step
+        torch.cuda.synchronize()
+        sd = padded_sdpa(batch, 2)
+        if "ms_per_step" in sd:
+            sd["valid_tflops"] = round((fl["fwd"] + fl["bwd"]) / (sd["ms_per_step"] / 1e3) / 1e12, 2)
+            sd["jfa_ms_per_step"] = round(ms, 4)
+        res["padded_sdpa"] = sd
+    del batch
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_jfa(args, rank, world, device):
+    from jagged_attention_recsys_jfa_gb300.sharding import shard_sequences
+
+    name = args.config
+    cfg = CONFIGS[name]
+    if args.batch:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, batch=args.batch)
+    if args.shard:
+        # strong scaling: one batch, the same on every rank, split by sequence; each rank
+        # runs only its shard (no collective on the data path)
+        full = make_batch(cfg, device=device, seed=cfg.seed)
+        mine = shard_sequences(full.q_lengths.tolist(), full.kv_lengths.tolist(), world, cfg.causal)[rank]
+        batch = shard_batch(full, mine) if world > 1 else full
+        del full
+    else:
+        batch = make_batch(cfg, device=device, seed=cfg.seed + rank)
+    fl = workload_flops(batch)
+    step = Step(batch, device)
+
+    for _ in range(args.warmup):
+        step()
+    step.check("after warm-up")
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- timed region: inputs resident in HBM
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(device.index or 0)
+    torch.cuda.reset_peak_memory_stats()
+    mem_base = torch.cuda.memory_allocated()
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    # the timed region: K whole steps, nothing recorded between the kernels
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms, bwd_ms, per_kernel = kernel_pass(step, args.steps, stream)
+    peak_mem = torch.cuda.max_memory_allocated() - mem_base
+    step.check("in the timed region (first error since warm-up)")
+
+    # max over ranks of the timed region, sum of work over ranks
+    t_local = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    w_local = torch.tensor([fl["fwd"] + fl["bwd"]], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t_local, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(w_local, op=torch.distributed.ReduceOp.SUM)
+    t_max_s = float(t_local.item()) / 1e3
+    total_flops = float(w_local.item()) * args.steps
+    value = total_flops / t_max_s / 1e12
+    launches = sum(c for _, c in per_kernel.values())
+
+    graph_ms = None
+    if not args.no_extras:
+        graph_ms = graph_replay(step, args.steps, stream, device)
+    bias_grad = None
+    if not args.no_extras and (batch.bias is not None or batch.jbias is not None):
+        bias_grad = bias_grad_leg(step, batch, args.steps, stream)
+    e2e = None
+    if not args.no_extras:
+        e2e_s = e2e_leg(step, batch, args, device, barrier)
+        t_e2e = torch.tensor([e2e_s["seconds"]], dtype=torch.float64, device=device)
+        if world > 1:
+            torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
+        e2e = {"value": round(total_flops / float(t_e2e.item()) / 1e12, 2), "unit": "TFLOPS",
+               "h2d_bytes_per_step": e2e_s["h2d"], "d2h_bytes_per_step": e2e_s["d2h"]}
+
+    if rank != 0:
+        return None
+    return finish(args, name, cfg, batch, step, fl, world, value, t_max_s, total_ms, fwd_ms, bwd_ms, per_kernel,
+                  peak_mem, launches, clk, graph_ms, bias_grad, e2e, device)
+
+
+def graph_replay(step, steps, stream, device):
+    """The same step captured once in a CUDA graph and replayed: the planner reads the
+    offsets on the device, so one capture serves every batch of the same shape; replays
+    drop the per-call host work and launch gaps (what launch-bound small batches gain).
+    Returns ms per replayed step."""
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        graph.replay()
+    g_start, g_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    g_start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    g_end.record(stream)
+    torch.cuda.synchronize()
+    step.check("in the graph replays")
+    del graph
+    return g_start.elapsed_time(g_end) / steps
+
+
+def bias_grad_leg(step, batch, steps, stream):
+    """Workloads with a bias: the same backward also writing the bias's gradient, timed
+    against the plain backward on the same inputs (the step holds the bias constant)."""
+    jfa = step.jfa
+    dbias = torch.empty_like(batch.bias) if batch.bias is not None else None
+    djb = torch.empty_like(batch.jbias) if batch.jbias is not None else None
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    bwd_g = lambda: step.bwd(bias_grad=dbias, jagged_bias_grad=djb)
+    t_plain, t_grad = timed(step.bwd), timed(bwd_g)
+    jfa.jfa_timing_read()
+    jfa.jfa_timing_enable(True)
+    timed(bwd_g)
+    jfa.jfa_timing_enable(False)
+    pk = jfa.jfa_timing_read()
+    step.check("after the bias-gradient backward")
+    return {"kind": "relative-position table" if batch.bias is not None else "general jagged bias",
+            "bwd_ms": round(t_grad, 4), "bwd_ms_without": round(t_plain, 4),
+            "overhead": round(t_grad / t_plain - 1, 4),
+            "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in pk.items() if v[1]}}
+
+
+def e2e_leg(step, batch, args, device, barrier):
+    """End to end through the public call with host buffers.  Every step copies its inputs
+    in from pinned host memory and its results (out, lse, dq, dk, dv) back out.  Consecutive
+    steps overlap the way a training loop would run them: the next step's inputs stream in
+    on one copy stream while this step computes, and its results stream out on another;
+    device inputs and outputs are double-buffered so no copy touches a buffer a kernel
+    still uses.  Returns the wall seconds of `steps` steps and the bytes copied per step."""
+    jfa, cfg, center = step.jfa, batch.cfg, step.center
+    pin = lambda t: t.cpu().pin_memory()
+    in_names = ("q", "k", "v", "dout", "q_offsets", "kv_offsets") + (
+        ("jbias", "jbias_offsets") if batch.jbias is not None else ())  # a general bias is per-batch input
+    h_in = {n: pin(getattr(batch, n)) for n in in_names}
+    out_names = ("out", "lse", "dq", "dk", "dv")
+    res = {"out": step.out, "lse": step.lse, "dq": step.dq, "dk": step.dk, "dv": step.dv}
+    h_out = [{n: torch.empty(res[n].shape, dtype=res[n].dtype, pin_memory=True) for n in out_names}
+             for _ in range(2)]
+    d_in = [{n: torch.empty_like(getattr(batch, n)) for n in h_in} for _ in range(2)]
+    d_out = [{n: torch.empty_like(res[n]) for n in out_names} for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def e2e_step(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(ev_done[b])  # the step that last used these inputs has computed
+            for n in h_in:
+                d_in[b][n].copy_(h_in[n], non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        if used[b]:
+            s_comp.wait_event(ev_free[b])  # its results have been copied out
+        x, o = d_in[b], d_out[b]
+        xjb = (x["jbias"], x["jbias_offsets"]) if "jbias" in x else None
+        jfa.jfa_forward(x["q"], x["k"], x["v"], x["q_offsets"], x["kv_offsets"], batch.bias, center, cfg.scale,
+                        cfg.causal, out=o["out"], lse=o["lse"], workspace=step.ws_f, jagged_bias=xjb)
+        jfa.jfa_backward(x["dout"], x["q"], x["k"], x["v"], o["out"], o["lse"], x["q_offsets"], x["kv_offsets"],
+                         batch.bias, center, cfg.scale, cfg.causal, dq=o["dq"], dk=o["dk"], dv=o["dv"],
+                         workspace=step.ws_b, jagged_bias=xjb)
+        ev_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            for n in out_names:
+                h_out[b][n].copy_(o[n], non_blocking=True)
+            ev_free[b].record(s_out)
+        used[b] = True
+
+    for i in range(max(2, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    # the copied-out results are the resident run's (the kernels are deterministic)
+    if not (torch.equal(h_out[0]["out"], step.out.cpu()) and torch.equal(h_out[0]["dq"], step.dq.cpu())):
+        raise RuntimeError("end-to-end results differ from the resident run")
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0
+    return {"seconds": secs, "h2d": h2d, "d2h": d2h}
+
+
+def finish(args, name, cfg, batch, step, fl, world, value, t_max_s, total_ms, fwd_ms, bwd_ms, per_kernel, peak_mem,
+           launches, clk, graph_ms, bias_grad, e2e, device):
+    """Rank 0: the roofline, the CPU baseline, the padded SDPA comparison and every other
+    workload, then the JSON line."""
+    peaks, peak_src = load_peaks()
+    roofline, kernels = roofline_of(batch, name, per_kernel, peaks, peak_src)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu_batch = make_batch(cfg, device="cpu")
@@ -585,27 +729,39 @@ def run_jfa(args, rank, world, device):
             s["jfa_peak_extra_gb"] = round(peak_mem / 1e9, 3)
         sdpa = s
 
+    # ---- every other workload on the same GPU, after the headline's timed region
+    others = None
+    if world == 1 and not args.no_configs and not args.shard:
+        del step
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        others = {}
+        for other in OTHER_CONFIGS:
+            if other != name:
+                others[other] = measure_config(other, args, device, peaks, peak_src)
+
     step_ms = t_max_s * 1e3 / args.steps
     peak_tf = float(peaks["bf16_tflops"])
-    res = {
+    fwd, bwd = split_rates(fl, fwd_ms, bwd_ms, peak_tf)
+    cfgd = config_dict(cfg, name)
+    if args.shard:
+        cfgd["sharded"] = f"one batch split by sequence over {world} rank(s) (longest-processing-time)"
+    return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "strong" if args.shard else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded jagged batch, values N(0,1) in bf16)",
-        "config": config_dict(cfg, name),
+        "config": cfgd,
         "pct_of_tensor_peak": round(100 * value / world / peak_tf, 2),
-        "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fl["fwd"] / (fwd_ms / 1e3) / 1e12, 1),
-                "pct_of_peak": round(100 * fl["fwd"] / (fwd_ms / 1e3) / 1e12 / peak_tf, 2)},
-        "bwd": {"ms": round(bwd_ms, 4), "tflops": round(fl["bwd"] / (bwd_ms / 1e3) / 1e12, 1),
-                "pct_of_peak": round(100 * fl["bwd"] / (bwd_ms / 1e3) / 1e12 / peak_tf, 2)},
+        "fwd": fwd, "bwd": bwd,
         "valid_pairs": fl["pairs"], "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu,
-        "graph_replay": {"ms_per_step": round(graph_ms, 4), "value": round((fl["fwd"] + fl["bwd"]) / (graph_ms * 1e-3) / 1e12, 2),
-                         "unit": "TFLOPS"},
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches, "clocks": clk, "padded_sdpa": sdpa, "bias_grad": bias_grad,
+        "graph_replay": None if graph_ms is None else {
+            "ms_per_step": round(graph_ms, 4),
+            "value": round((fl["fwd"] + fl["bwd"]) / (graph_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS"},
+        "e2e": e2e, "gpu_launches": launches, "clocks": clk, "padded_sdpa": sdpa, "bias_grad": bias_grad,
         "peak_mem_extra_gb": round(peak_mem / 1e9, 3),
+        "configs": others,
     }
-    return res
 
 
 KERNEL_SOURCE = {"forward": "jfa_fwd.cu", "bwd_preprocess": "jfa_bwd.cu", "bwd_dkdv": "jfa_bwd.cu",
@@ -677,6 +833,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sdpa", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only --config (by default every other workload follows, at N=1)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's sequence count (smaller cases for profiling)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the CUDA-graph, bias-gradient and end-to-end legs")
+    ap.add_argument("--shard", action="store_true",
+                    help="split one batch of --config over the ranks by sequence (strong scaling) instead of "
+                         "one batch per rank (weak scaling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

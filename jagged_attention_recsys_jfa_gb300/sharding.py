@@ -82,3 +82,14 @@ def select_bias_blocks(values: torch.Tensor, block_offsets: torch.Tensor, index:
         new_off[1:] = torch.cumsum(torch.tensor(sizes, dtype=torch.int64), 0)
     packed = torch.cat(parts, 1).contiguous() if parts else values[:, :0]
     return packed, new_off.to(block_offsets.device)
+
+
+def scatter_bias_blocks(full: torch.Tensor, block_offsets: torch.Tensor, index: Sequence[int], part: torch.Tensor,
+                        part_offsets: torch.Tensor) -> None:
+    """Write a shard's packed general-bias blocks (part [H, plane'], part_offsets) back into
+    the full [H, plane] array at the blocks of sequences `index` (inverse of
+    select_bias_blocks; used for the bias's gradient)."""
+    off = block_offsets.tolist()
+    poff = part_offsets.tolist()
+    for k, b in enumerate(index):
+        full[:, off[b]:off[b + 1]] = part[:, poff[k]:poff[k + 1]]

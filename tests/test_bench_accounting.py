@@ -66,10 +66,12 @@ def test_general_bias_bytes_counted_once_per_pass():
     w0, w1 = b.workload_bytes(plain), b.workload_bytes(jb)
     H = jb.cfg.heads
     lq, lk = jb.q_lengths.numpy(), jb.kv_lengths.numpy()
-    blocks = 2.0 * H * lq * ((lk + 7) // 8 * 8)
+    # the visited pairs' elements only (causal: the lower triangle; never the row padding)
+    blocks = np.array([2.0 * H * _brute_pairs([a], [c], True) for a, c in zip(lq, lk)])
+    assert blocks.sum() < 2.0 * H * (lq * ((lk + 7) // 8 * 8)).sum() * 0.6
     long_ = lq > 128
     assert w1["forward"] - w0["forward"] == pytest.approx(blocks.sum())
     assert w1["bwd_dkdv"] - w0["bwd_dkdv"] == pytest.approx(blocks[long_].sum())
     assert w1["bwd_dq"] - w0["bwd_dq"] == pytest.approx(blocks[long_].sum())
     assert w1["bwd_fused"] - w0["bwd_fused"] == pytest.approx(blocks[~long_].sum())
-    assert jb.jbias.numel() == blocks.sum() / 2
+    assert jb.jbias.numel() == (lq * ((lk + 7) // 8 * 8)).sum() * H
