@@ -180,16 +180,18 @@ jfa_status jfa_timing_read(double* ms, int* launches, int n_kinds);
  * stays usable.  `workspace` needs 256 bytes (zeroed status word). */
 jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_stream_t stream);
 
-/* The bounded-wait limit, in ns, that the kernels use for a launch whose planner found
- * `planned_tile_pairs` 128x128 (query tile, key tile) pairs over all heads, to be shared by
- * `ctas` persistent CTAs, the costliest single work item being `max_item_tile_pairs` pairs
- * (not part of the attention itself; exported so the rule can be checked without a GPU).
- * A wait of a kernel's pipeline that lasts longer ends its CTA with JFA_ERR_TIMEOUT.  The
- * limit is 2 s plus 32 us for each pair of one CTA's share (rounded up) and of the
- * costliest item, capped at 2 s + 1 h; negative arguments count as 0, `ctas` < 1 as 1.
- * 32 us is about 30 times the time one SM takes for a pair, so no wait of a correct launch
- * (the longest is a CTA's scheduler waiting for its previous items to finish) comes near
- * it, whatever the launch's size. */
+/* The item hand-off wait limit, in ns, that the kernels use for a launch whose planner
+ * found `planned_tile_pairs` 128x128 (query tile, key tile) pairs over all heads, to be
+ * shared by `ctas` persistent CTAs, the costliest single work item being
+ * `max_item_tile_pairs` pairs (not part of the attention itself; exported so the rule can
+ * be checked without a GPU).  A CTA's scheduler waits for its previous items to finish
+ * before it claims the next, and its roles wait for the next item to be claimed: such a
+ * wait lasting longer ends the CTA with JFA_ERR_TIMEOUT.  The limit is 2 s plus 32 us for
+ * each pair of one CTA's share (rounded up) and of the costliest item, capped at 2 s + 1 h;
+ * negative arguments count as 0, `ctas` < 1 as 1.  32 us is about 30 times the time one SM
+ * takes for a pair, so no hand-off of a correct launch comes near it, whatever the
+ * launch's size.  (Waits inside an item's tile pipeline last at most a few tiles' time and
+ * keep a fixed 2 s limit.) */
 uint64_t jfa_wait_limit_ns(int64_t planned_tile_pairs, int ctas, int64_t max_item_tile_pairs);
 
 /* Developer tracing (not part of the attention itself).  With a non-NULL device buffer,

@@ -64,7 +64,7 @@ struct BwdParams {
   const int* n_items;
   int* claim;  // the list's claim counter (zeroed by the planner)
   int* status;
-  const uint64_t* wait_ns;  // the planner's bounded-wait limit for this launch
+  const uint64_t* wait_ns;  // the planner's item hand-off wait limit for this launch (ns)
   const float* lse2;    // [H][qpad_cap]  -lse * log2(e), padded per sequence to 128 rows
   const float* delta;   // [H][qpad_cap]  -D, same layout
   const int64_t* qpad;  // [B+1] sequence offsets in the padded vectors
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    meta_init(meta, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
+    meta_init(meta, p.wait_ns, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -473,7 +473,6 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
-  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -514,7 +513,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
             tmap_acquire(mk.map);
             tmap_acquire(mv.map);
           }
-          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
           trace_event(p.trace, kTraceLoader, tn, 1);
           mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
           load_tile<D>(sK, mk.map, &kv_full, wi.h * D, mk.y);
@@ -553,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       auto fill = [&](const TileMap& m, int col, const float* l2src, const float* dsrc) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
         if (m.tail) tmap_acquire(m.map);
-        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) return false;
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
         trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes + (l2src ? 2 * kBM * 4 : 0));
         load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
@@ -617,7 +616,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
       uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (!mbar_wait(bar, par, abort_flag, cta_wait_ns())) return false;
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
         tc_fence_after();
         return true;
       };
@@ -752,13 +751,13 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         }
         // Q_i's ring slot carries this tile's lse2 / D vectors: wait for it
         const uint32_t nq = ring_n + 1;
-        if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ring_n += 2;
         const float* vec = sVec + (qtile_n % C::kVecSlots) * 256;
         ++qtile_n;
         const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(vec + 64 * w);  // -lse2 pairs
         const uint64_t* ndvec = reinterpret_cast<const uint64_t*>(vec + 128 + 64 * w);  // -D pairs
-        if (!mbar_wait(&st_full, tile_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
         float x[64];
@@ -808,7 +807,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         tc_fence_before();
         mbar_arrive(&p_full);
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
-        if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
@@ -884,10 +883,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         }
         continue;
       }
-      if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       drain_acc_rows<D>(tmem + lane_addr + C::kColA1, 1.f, dv_row, valid, &dv_empty);
-      if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
       drain_acc_rows<D>(tmem + lane_addr + C::kColA0, p.scale, dk_row, valid, &dk_empty);
@@ -946,7 +945,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    meta_init(meta, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
+    meta_init(meta, p.wait_ns, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -954,7 +953,6 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
-  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -992,7 +990,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
           tmap_acquire(mq.map);
           tmap_acquire(mdo.map);
         }
-        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&qdo_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&qdo_full, 2 * C::kTileBytes);
         load_tile<D>(sQ, mq.map, &qdo_full, wi.h * D, mq.y);
@@ -1031,7 +1029,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       auto fill = [&](const TileMap& m, int col) {
         const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
         if (m.tail) tmap_acquire(m.map);
-        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) return false;
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
         trace_event(p.trace, kTraceProducer, tn, 2);
         mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
         load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
@@ -1079,7 +1077,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       uint32_t ring_n = 0, item_n = 0, tile_n = 0, acc_n = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (!mbar_wait(bar, par, abort_flag, cta_wait_ns())) return false;
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
         tc_fence_after();
         return true;
       };
@@ -1209,7 +1207,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
             prefetch_l2(brow_i + jj0 + kBN + 56);
           }
         }
-        if (!mbar_wait(&s_full, tile_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
         float x[64];
@@ -1264,7 +1262,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
         for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P
         const uint32_t g = tile_n;
         const uint32_t tP = tmem + lane_addr + colP(g) + 64 * w;
-        if (!mbar_wait(&dp_full[g & 1], (g >> 1) & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&dp_full[g & 1], (g >> 1) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++tile_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
@@ -1311,7 +1309,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
         for (int c0 = 0; c0 < D; c0 += 32) store_acc_row<32>(0, 0.f, dq_row + c0, valid, true);
         continue;
       }
-      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&acc_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++acc_n;
       tc_fence_after();
       drain_acc_rows<D>(tmem + lane_addr + C::kColDQ, p.scale, dq_row, valid, &acc_empty);
@@ -1379,7 +1377,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    meta_init(meta, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
+    meta_init(meta, p.wait_ns, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1387,7 +1385,6 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
-  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1430,7 +1427,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
           }
           const float* l2src = p.lse2 + int64_t(wi.h) * p.qpad_cap + wi.qp;
           const float* dsrc = p.delta + int64_t(wi.h) * p.qpad_cap + wi.qp;
-          if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+          if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
           trace_event(p.trace, kTraceLoader, tn, 1);
           mbar_arrive_expect_tx(&q_full, 2 * C::kTileBytes + 2 * kBM * 4);
           load_tile<D>(sQ, mq.map, &q_full, wi.h * D, mq.y);
@@ -1463,7 +1460,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
             const TileMap m = tile_map(p.maps, p.B, kv ? kMapV : kMapK, wi.b, wi.ko, kt, p.total_kv);
             if (m.tail) tmap_acquire(m.map);
             const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
-            if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+            if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
             trace_event(p.trace, kTraceProducer, tn, 2);
             mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes);
             load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], wi.h * D, m.y);
@@ -1486,7 +1483,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
       uint32_t ring_n = 0, item_n = 0, g = 0, tn = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (!mbar_wait(bar, par, abort_flag, cta_wait_ns())) return false;
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
         tc_fence_after();
         return true;
       };
@@ -1602,7 +1599,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
      const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
      const bool live = any_visible(it.u0, it.u1, Lq, Lk);
-     if (live && !__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, cta_wait_ns()))) {
+     if (live && !__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs))) {
        ok = false;
        break;
      }
@@ -1618,7 +1615,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
                             Lq - 64 * w, Lk - kj0, lane);
       }
       // ---- P^T = exp2(S^T * scale * log2e (+ bias) - lse2), 0 on padding and hidden pairs
-      if (!mbar_wait(&st_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&st_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
       float x[64];
@@ -1661,9 +1658,9 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
       mbar_arrive(&p_full);
       if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
       // ---- dS^T = P^T o (dP^T - D) -> shared memory (keys x queries, 128-byte swizzle)
-      if (!mbar_wait(&dpt_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&dpt_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
-      if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       // bias gradient: diagonal sums of this warp's dS^T (as in dbias_warp_tile, one column
       // half at a time); hidden and padded pairs have P^T = 0, so dS^T = 0 there
       float db_straight[2] = {0.f, 0.f}, db_wrapped[2] = {0.f, 0.f};
@@ -1761,10 +1758,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
         store_acc_row_own<D>(0, 0.f, dv_row, valid, true);
         continue;
       }
-      if (!mbar_wait(&dv_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&dv_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       drain_row_own<D>(tmem + lane_addr + C::kColFdV, 1.f, dv_row, valid, &dv_empty);
-      if (!mbar_wait(&dk_full, g & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&dk_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
       drain_row_own<D>(tmem + lane_addr + C::kColP, p.scale, dk_row, valid, &dk_empty);
       ++g;
@@ -1773,7 +1770,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
      const bool qvalid = row < Lq;
      __nv_bfloat16* dq_row = p.g2 + ((it.qo + row) * p.H + it.h) * int64_t(D);
      if (live) {
-       if (!mbar_wait(&dq_full, item_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+       if (!mbar_wait(&dq_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
        ++item_n;
        tc_fence_after();
        drain_row_own<D>(tmem + lane_addr + C::kColFdQ, p.scale, dq_row, qvalid, &dq_empty);

@@ -14,12 +14,15 @@ constexpr int kBN = 128;  // key rows per tile
 constexpr int kMaxBuckets = 8192;
 constexpr int kCostBuckets = 2048;  // planner's counting-sort buckets (cost clamped)
 // Bounded pipeline waits.  A wait that outlasts its limit ends the CTA with
-// JFA_ERR_TIMEOUT, so the limit must exceed any wait a correct launch can have.  The
-// longest legitimate waits are item hand-offs: a CTA's scheduler waits for item k - 2 to
-// be released, i.e. for up to about a CTA's whole share of the launch.  The planner
-// therefore sizes each list's limit from the work it planned: a 2 s floor plus a generous
-// time per tile pair (kWaitNsPerTilePair, ~30x the measured ~1 us per 128x128 tile pair
-// on one SM) for one CTA's share of the pairs and the costliest single item on top.
+// JFA_ERR_TIMEOUT, so the limit must exceed any wait a correct launch can have.  Waits
+// inside an item's tile pipeline last at most a few units' time (a unit visits at most
+// 2 x 128 tile pairs, well under a millisecond) and keep the fixed kWaitTimeoutNs.  The
+// waits that scale with the launch are the item hand-offs of the scheduler ring: a CTA's
+// scheduler waits for item k - 2 to be released, and its roles for item k to be
+// published, i.e. for up to about a CTA's whole share of the launch.  The planner
+// therefore sizes each list's hand-off limit from the work it planned: a 2 s floor plus a
+// generous time per tile pair (kWaitNsPerTilePair, ~30x the measured ~1 us per 128x128
+// tile pair on one SM) for one CTA's share of the pairs and the costliest single item.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // floor: 2 s
 constexpr uint64_t kWaitNsPerTilePair = 32000ull;    // 32 us per planned tile pair
 constexpr uint64_t kWaitLimitCapNs = 3600ull * 1000000000ull;  // an hour: no overflow
@@ -216,18 +219,6 @@ __host__ __device__ inline void q_tiles_for_kv_tile(int t, int Lq, int Lk, bool 
 }
 
 #ifdef __CUDACC__
-// This CTA's bounded-wait limit for the launch, read from the planner's per-list value by
-// set_cta_wait_ns (between the kernel's griddepcontrol.wait and the CTA-wide barrier that
-// precedes its first pipeline wait); never below the kWaitTimeoutNs floor.
-__shared__ uint64_t cta_wait_ns_sh;
-__device__ __forceinline__ uint64_t cta_wait_ns() { return cta_wait_ns_sh; }
-__device__ __forceinline__ void set_cta_wait_ns(const uint64_t* planned) {
-  if (threadIdx.x == 0) {
-    const uint64_t w = planned ? *planned : 0;
-    cta_wait_ns_sh = w > kWaitTimeoutNs ? w : kWaitTimeoutNs;
-  }
-}
-
 // The tensor map and box row coordinate that load row tile `t` of a sequence starting at
 // row `row0` of a tensor with `total` rows: the sequence's own map, or the tail map when
 // the 128-row box would reach past the tensor's last row (such a tile is always the

@@ -56,7 +56,7 @@ struct FwdParams {
   const int* n_items;
   int* claim;  // the list's claim counter (zeroed by the planner)
   int* status;
-  const uint64_t* wait_ns;  // the planner's bounded-wait limit for this launch
+  const uint64_t* wait_ns;  // the planner's item hand-off wait limit for this launch (ns)
   __nv_bfloat16* out;
   float* lse;
   TraceBuf trace;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       mbar_init(&p_full[s], 128);
       mbar_init(&o_full[s], 1);
     }
-    meta_init(meta);
+    meta_init(meta, p.wait_ns);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -148,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     tmem_relinquish();
   }
   grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
-  set_cta_wait_ns(p.wait_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -185,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         }
         if (q0.tail) tmap_acquire(q0.map);
         if (q1.tail && q1.map != q0.map) tmap_acquire(q1.map);
-        if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&q_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         trace_event(p.trace, kTraceLoader, tn, 1);
         mbar_arrive_expect_tx(&q_full, (it.has1 ? 2 : 1) * C::kTileBytes);
 #pragma unroll
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t e = ring_n % C::kStages, ph = (ring_n / C::kStages) & 1;
-            if (!mbar_wait(&kv_empty[e], ph ^ 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+            if (!mbar_wait(&kv_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
             trace_event(p.trace, kTraceProducer, tn, 2);
             mbar_arrive_expect_tx(&kv_full[e], C::kTileBytes);
             uint8_t* dst = sRing + e * C::kTileBytes;
@@ -306,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const int nkv[2] = {it.nkv0, it.nkv1};
-        if (!mbar_wait(&q_full, item_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++item_n;
         tc_fence_after();
         trace_event(p.trace, kTraceMma, tn, 10);
@@ -332,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
                     (acc || kk > 0) ? 1u : 0u);
         };
         auto wait_full = [&](uint32_t n) -> bool {
-          const bool r = mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, cta_wait_ns());
+          const bool r = mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, kWaitTimeoutNs);
           tc_fence_after();
           return r;
         };
@@ -347,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
           bool k_ready = false;
           for (int s = 0; s < 2 && ok; ++s) {
             if (j < nkv[s]) {
-              if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+              if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
               ++p_n[s];
               tc_fence_after();
               trace_event(p.trace, kTraceMma, tn, 12 + s);
@@ -431,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             prefetch_l2(brow_j + kvj + kBN + 64);
           }
         }
-        if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+        if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++s_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 20);
@@ -552,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, lse = ln(sum) = (m + log2 l) * ln 2
-      if (!mbar_wait(&o_full[s], o_n & 1, abort_flag, cta_wait_ns())) { ok = false; break; }
+      if (!mbar_wait(&o_full[s], o_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       ++o_n;
       tc_fence_after();
       if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 22);

@@ -27,14 +27,18 @@ struct ItemMeta {
 struct MetaRing {
   ItemMeta e[kMetaSlots];
   uint64_t full[kMetaSlots], empty[kMetaSlots];
+  // the planner's hand-off wait limit for this launch (global memory; read only by a wait
+  // that did not complete at once, so after griddepcontrol.wait)
+  const uint64_t* wait_ns;
 };
 
 // One thread, before the CTA-wide barrier that publishes mbarrier initialisation.
-__device__ __forceinline__ void meta_init(MetaRing& r, int consumers = kMetaConsumers) {
+__device__ __forceinline__ void meta_init(MetaRing& r, const uint64_t* wait_ns, int consumers = kMetaConsumers) {
   for (int i = 0; i < kMetaSlots; ++i) {
     mbar_init(&r.full[i], 1);
     mbar_init(&r.empty[i], consumers);
   }
+  r.wait_ns = wait_ns;
 }
 
 // Scheduler (one thread).  Claims item k (idx = atomicAdd(claim, 1)) once item k - 2 is
@@ -49,7 +53,7 @@ __device__ __forceinline__ bool meta_publish(MetaRing& r, const WorkItem* items,
   for (uint32_t k = 0;; ++k) {
     if (k >= 2) {
       const uint32_t kp = k - 2;
-      if (!mbar_wait(&r.empty[kp % kMetaSlots], (kp / kMetaSlots) & 1, abort, cta_wait_ns())) return false;
+      if (!mbar_wait(&r.empty[kp % kMetaSlots], (kp / kMetaSlots) & 1, abort, r.wait_ns, kWaitTimeoutNs)) return false;
     }
     const int idx = atomicAdd(claim, 1);
     ItemMeta m;
@@ -90,7 +94,7 @@ __device__ __forceinline__ const ItemMeta* meta_peek_next(MetaRing& r, uint32_t 
 // Entry k for a single-thread role, read in place for the item's duration and then
 // freed with meta_release.
 __device__ __forceinline__ bool meta_wait(MetaRing& r, uint32_t k, volatile int* abort) {
-  return mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, cta_wait_ns());
+  return mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, r.wait_ns, kWaitTimeoutNs);
 }
 __device__ __forceinline__ void meta_release(MetaRing& r, uint32_t k) { mbar_arrive(&r.empty[k % kMetaSlots]); }
 
@@ -99,7 +103,7 @@ __device__ __forceinline__ void meta_release(MetaRing& r, uint32_t k) { mbar_arr
 // outcome: a lane whose wait gave up has raised the abort flag, which ends the other
 // lanes' waits too.
 __device__ __forceinline__ bool meta_wait_warp(MetaRing& r, uint32_t k, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, cta_wait_ns()));
+  return __all_sync(0xffffffffu, mbar_wait(&r.full[k % kMetaSlots], (k / kMetaSlots) & 1, abort, r.wait_ns, kWaitTimeoutNs));
 }
 __device__ __forceinline__ void meta_release_warp(MetaRing& r, uint32_t k) {
   __syncwarp();

@@ -95,6 +95,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The same wait with its limit read from `*timeout_ns` (a per-launch value in global
+// memory) only after the first test has failed, so the fast path loads nothing; never
+// below `floor_ns`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          const uint64_t* timeout_ns, uint64_t floor_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t = *timeout_ns;
+  return mbar_wait(bar, parity, abort, t > floor_ns ? t : floor_ns);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x,
                                             int32_t y) {
