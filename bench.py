@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Jagged Flash Attention benchmark on GB300.
 
-One step = the whole hot path on one synthetic jagged batch: planner + forward,
-then planner + preprocess + dK/dV pass + dQ pass (jfa_forward + jfa_backward).
+One step = the whole hot path on one synthetic jagged batch: planner + forward, then
+planner + preprocess + the backward passes (jfa_forward + jfa_backward): sequences of one
+query tile in the fused pass, of 2 .. 8 in the non-sequence-parallel pass, longer ones in
+the split dK/dV and dQ passes.
 Metric: valid-token TFLOPS (bf16), forward+backward, counting only the (query, key)
 pairs the attention visits: fwd 4*d*H*P, bwd 10*d*H*P flops, P = sum_b Lq_b*Lk_b
 (causal: the visible pairs).  Inputs are resident in HBM for `value`; `e2e` times
@@ -74,26 +76,41 @@ def valid_pairs(lq, lk, causal):
 SHORT_Q = 128  # sequences with at most one query tile: backward in the fused pass
 
 
-def _split(batch):
-    short = np.asarray(batch.q_lengths) <= SHORT_Q
-    return short, ~short
+def nsp_max_rows():
+    """Query rows up to which a sequence's backward takes the non-sequence-parallel pass
+    (the library's process-wide setting; 0 when the library is not loaded)."""
+    try:
+        from jagged_attention_recsys_jfa_gb300 import jfa
+        return 128 * jfa.jfa_nsp_max_tiles() if jfa._LIB is not None else 0
+    except Exception:
+        return 0
 
 
-def workload_flops(batch):
+def _split(batch, nsp_rows=None):
+    """Which backward pass covers each sequence: (fused, non-sequence-parallel, split)."""
+    lq = np.asarray(batch.q_lengths)
+    nsp_rows = nsp_max_rows() if nsp_rows is None else nsp_rows
+    short = lq <= SHORT_Q
+    nsp = (lq > SHORT_Q) & (lq <= nsp_rows)
+    return short, nsp, ~(short | nsp)
+
+
+def workload_flops(batch, nsp_rows=None):
     """Algorithmic flops: forward 4*d*H per visited pair; backward 10*d*H, of which the
-    split passes (sequences with more than one query tile) take 8 (dK/dV) and 2 (dQ) and
-    the fused pass (the others) all 10."""
+    split passes take 8 (dK/dV) and 2 (dQ), and the fused pass (one query tile) and the
+    non-sequence-parallel pass (if enabled for the sequence's length) all 10."""
     lq, lk, causal = np.asarray(batch.q_lengths), np.asarray(batch.kv_lengths), batch.cfg.causal
-    short, long_ = _split(batch)
+    short, nsp, long_ = _split(batch, nsp_rows)
     P = valid_pairs(lq, lk, causal)
     Pl = valid_pairs(lq[long_], lk[long_], causal)
     Ps = valid_pairs(lq[short], lk[short], causal)
+    Pn = valid_pairs(lq[nsp], lk[nsp], causal)
     dH = batch.cfg.head_dim * batch.cfg.heads
     return {"pairs": P, "fwd": 4.0 * dH * P, "bwd": 10.0 * dH * P, "dkdv": 8.0 * dH * Pl, "dq": 2.0 * dH * Pl,
-            "fused": 10.0 * dH * Ps}
+            "fused": 10.0 * dH * Ps, "nsp": 10.0 * dH * Pn}
 
 
-def workload_bytes(batch):
+def workload_bytes(batch, nsp_rows=None):
     """Algorithmic DRAM bytes per launch of each kernel: every input read once, every
     output written once (the per-query lse / D vectors on 128-row-padded rows).  A general
     jagged bias counts 2 bytes per visited (query, key) pair and head for each pass that
@@ -102,23 +119,29 @@ def workload_bytes(batch):
     H, d = batch.cfg.heads, batch.cfg.head_dim
     row = 2.0 * H * d
     lq, lk = np.asarray(batch.q_lengths), np.asarray(batch.kv_lengths)
-    short, long_ = _split(batch)
-    Tq, Tk = float(lq.sum()), float(lk.sum())
-    qpad = float(((lq + 127) // 128 * 128).sum())
-    vec = 8.0 * H * qpad  # lse*log2(e) and D, fp32
-    Tql, Tkl, Tqs, Tks = float(lq[long_].sum()), float(lk[long_].sum()), float(lq[short].sum()), float(lk[short].sum())
-    vecl = 8.0 * H * float(((lq[long_] + 127) // 128 * 128).sum())
-    vecs = vec - vecl
+    Tq = float(lq.sum())
     if batch.cfg.general_bias:
         jb = np.array([2.0 * H * valid_pairs([a], [b], batch.cfg.causal) for a, b in zip(lq, lk)])
     else:
         jb = 0.0 * lq
-    jbl, jbs = float(np.sum(jb[long_])), float(np.sum(jb[short]))
-    return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq + jbl + jbs,
+
+    def part(sel):  # query rows, key rows, padded lse / D vector bytes, bias bytes of a subset
+        return (float(lq[sel].sum()), float(lk[sel].sum()), 8.0 * H * float(((lq[sel] + 127) // 128 * 128).sum()),
+                float(np.sum(jb[sel])))
+    short, nsp, long_ = _split(batch, nsp_rows)
+    Tql, Tkl, vecl, jbl = part(long_)
+    Tqs, Tks, vecs, jbs = part(short)
+    Tqn, Tkn, vecn, jbn = part(nsp)
+    vec = vecl + vecs + vecn
+    Tk = float(lk.sum())
+    # the single-pass backwards read q, dO, k, v once and write dq, dk, dv once
+    one_pass = lambda Tq_, Tk_, vec_, jb_: (2 * Tq_ + 2 * Tk_) * row + vec_ + (Tq_ + 2 * Tk_) * row + jb_
+    return {"forward": (Tq + 2 * Tk) * row + Tq * row + 4.0 * H * Tq + float(np.sum(jb)),
             "bwd_preprocess": 2 * Tq * row + 4.0 * H * Tq + vec,
             "bwd_dkdv": (2 * Tql + 2 * Tkl) * row + vecl + 2 * Tkl * row + jbl,
             "bwd_dq": (2 * Tql + 2 * Tkl) * row + vecl + Tql * row + jbl,
-            "bwd_fused": (2 * Tqs + 2 * Tks) * row + vecs + (Tqs + 2 * Tks) * row + jbs}
+            "bwd_fused": one_pass(Tqs, Tks, vecs, jbs),
+            "bwd_nsp": one_pass(Tqn, Tkn, vecn, jbn)}
 
 
 def load_peaks():
@@ -405,7 +428,8 @@ def roofline_of(batch, name, per_kernel, peaks, peak_src):
     fl = workload_flops(batch)
     kinds = {k: v for k, v in per_kernel.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
-    algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"], "bwd_fused": fl["fused"]}
+    algo = {"forward": fl["fwd"], "bwd_dkdv": fl["dkdv"], "bwd_dq": fl["dq"], "bwd_fused": fl["fused"],
+            "bwd_nsp": fl["nsp"]}
     algo_bytes = workload_bytes(batch)
     ms_dom, n_dom = kinds[dom]
     t_dom = ms_dom / n_dom / 1e3
@@ -765,7 +789,7 @@ def finish(args, name, cfg, batch, step, fl, world, value, t_max_s, total_ms, fw
 
 
 KERNEL_SOURCE = {"forward": "jfa_fwd.cu", "bwd_preprocess": "jfa_bwd.cu", "bwd_dkdv": "jfa_bwd.cu",
-                 "bwd_dq": "jfa_bwd.cu", "bwd_fused": "jfa_bwd.cu", "plan": "jfa_plan.cu"}
+                 "bwd_dq": "jfa_bwd.cu", "bwd_fused": "jfa_bwd.cu", "bwd_nsp": "jfa_bwd.cu", "plan": "jfa_plan.cu"}
 
 
 def kernel_source_hash(kernel):

@@ -162,7 +162,7 @@ const char* jfa_last_error(void);
 
 /* Kernel kinds for per-kernel timing. */
 enum { JFA_KERNEL_PLAN = 0, JFA_KERNEL_FORWARD = 1, JFA_KERNEL_BWD_PREPROCESS = 2, JFA_KERNEL_BWD_DKDV = 3,
-       JFA_KERNEL_BWD_DQ = 4, JFA_KERNEL_BWD_FUSED = 5, JFA_NUM_KERNEL_KINDS = 6 };
+       JFA_KERNEL_BWD_DQ = 4, JFA_KERNEL_BWD_FUSED = 5, JFA_KERNEL_BWD_NSP = 6, JFA_NUM_KERNEL_KINDS = 7 };
 
 /* Benchmark support (not part of the attention itself).  While enabled (process-wide),
  * every kernel launch is bracketed by two CUDA events recorded on the launch stream.
@@ -179,6 +179,20 @@ jfa_status jfa_timing_read(double* ms, int* launches, int n_kinds);
  * status word, readable with jfa_check_status.  Nothing faults or hangs; the context
  * stays usable.  `workspace` needs 256 bytes (zeroed status word). */
 jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_stream_t stream);
+
+/* Which backward pass takes a sequence of two or more query tiles (128 rows each), for
+ * every later jfa_backward call in the process.  Sequences of 2 .. max_tiles query tiles
+ * take the non-sequence-parallel pass -- one CTA owns a (sequence, head), forms every tile
+ * pair's S, P, dP and dS once and computes dK, dV and dQ from them (five GEMMs per tile
+ * pair), summing dQ over key tiles in an fp32 buffer in the workspace with one writer per
+ * row ("Jagged Flash Attention (JFA)", "Four generations" item 2, the reading in which
+ * the backward is not parallel over a sequence's query tiles); longer sequences take the
+ * split passes (dK/dV per key tile, then dQ per query tile: seven GEMMs per tile pair, no
+ * sum buffer).  max_tiles in 0 .. 16; below 2 every such sequence takes the split passes
+ * (the default, which measured faster on GB300).  Both paths give the same results within
+ * rounding and are each deterministic.  A negative max_tiles only reads the setting.
+ * Returns the previous setting, or -1 (nothing changed) for max_tiles > 16. */
+int jfa_set_nsp_max_tiles(int max_tiles);
 
 /* The item hand-off wait limit, in ns, that the kernels use for a launch whose planner
  * found `planned_tile_pairs` 128x128 (query tile, key tile) pairs over all heads, to be

@@ -10,6 +10,8 @@ from .jfa import (  # noqa: F401
     jfa_check_status,
     jfa_forward,
     jfa_last_launch_count,
+    jfa_nsp_max_tiles,
+    jfa_set_nsp_max_tiles,
     jfa_timing_enable,
     jfa_timing_read,
     jfa_trace_configure,

@@ -7,6 +7,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -15,6 +16,8 @@
 namespace jfa {
 namespace {
 thread_local int g_last_launches = 0;
+// query tiles up to which a sequence's backward takes the non-sequence-parallel pass
+std::atomic<int> g_nsp_max_tiles{kNspDefaultMaxTiles};
 thread_local char g_last_error[256] = "";
 }  // namespace
 
@@ -169,6 +172,7 @@ Problem make_problem(int B, int H, int d, int64_t total_q, int64_t total_kv, con
   p.jb_grad = has_jbias ? bias->values_grad : nullptr;
   std::lock_guard<std::mutex> g(g_trace_mu);
   for (int k = 0; k < JFA_NUM_KERNEL_KINDS; ++k) p.trace[k] = (k == g_trace_kind) ? g_trace : TraceBuf{nullptr, 0};
+  p.nsp_max_tiles = g_nsp_max_tiles.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -296,7 +300,11 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
     KernelTimer t(JFA_KERNEL_BWD_FUSED, s);
     JFA_CHECK_LAUNCH(launch_bwd_fused(pr, lse, workspace, L, dq, dk, dv, nsm, s), "fused short-query launch");
   }
-  g_last_launches = 5;
+  {
+    KernelTimer t(JFA_KERNEL_BWD_NSP, s);
+    JFA_CHECK_LAUNCH(launch_bwd_nsp(pr, lse, workspace, L, dq, dk, dv, nsm, s), "non-sequence-parallel launch");
+  }
+  g_last_launches = 6;
   return JFA_OK;
 }
 
@@ -326,6 +334,12 @@ const char* jfa_status_string(jfa_status s) {
 int jfa_last_launch_count(void) { return g_last_launches; }
 
 const char* jfa_last_error(void) { return g_last_error; }
+
+int jfa_set_nsp_max_tiles(int max_tiles) {
+  if (max_tiles < 0) return g_nsp_max_tiles.load();
+  if (max_tiles > kNspMaxTiles) return -1;
+  return g_nsp_max_tiles.exchange(max_tiles);
+}
 
 uint64_t jfa_wait_limit_ns(int64_t planned_tile_pairs, int ctas, int64_t max_item_tile_pairs) {
   return wait_limit_ns(planned_tile_pairs, ctas, max_item_tile_pairs);

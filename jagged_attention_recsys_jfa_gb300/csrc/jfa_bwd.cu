@@ -40,6 +40,10 @@ static_assert(reg_split_fits(kRegsLoad, kRegsCompute), "register split exceeds t
 constexpr uint32_t kRegsLoadDkdv = 96, kRegsComputeDkdv = 168, kRegsEpiDkdv = 72;
 static_assert(reg_split_fits_dkdv(kRegsLoadDkdv, kRegsComputeDkdv, kRegsEpiDkdv),
               "register split exceeds the launch allocation");
+// the non-sequence-parallel pass: the epilogue warps also sum and finish the dQ rows
+constexpr uint32_t kRegsLoadNsp = 104, kRegsComputeNsp = 160, kRegsEpiNsp = 88;
+static_assert(reg_split_fits_dkdv(kRegsLoadNsp, kRegsComputeNsp, kRegsEpiNsp),
+              "register split exceeds the launch allocation");
 // the fused short-query pass: more issue state in warpgroup 0, lighter compute warps
 constexpr uint32_t kRegsLoadFused = 112, kRegsComputeFused = 168, kRegsEpiFused = 64;
 static_assert(reg_split_fits_dkdv(kRegsLoadFused, kRegsComputeFused, kRegsEpiFused),
@@ -71,7 +75,8 @@ struct BwdParams {
   int64_t qpad_cap;
   __nv_bfloat16* g0;   // dK (dK/dV and fused passes) or dQ (dQ pass)
   __nv_bfloat16* g1;   // dV (dK/dV and fused passes)
-  __nv_bfloat16* g2;   // dQ (fused pass)
+  __nv_bfloat16* g2;   // dQ (fused and non-sequence-parallel passes)
+  float* dqacc;        // non-sequence-parallel pass: fp32 dQ sums [total_q][H][D]
   TraceBuf trace;
 };
 
@@ -106,6 +111,8 @@ struct PreParams {
   const int* n_items;
   const WorkItem* items2;     // fused list: the sequence's one query tile
   const int* n_items2;
+  const WorkItem* items3;     // non-sequence-parallel list: all of the sequence's query tiles
+  const int* n_items3;
   const int64_t* qpad;        // [B+1] padded row offsets
   const int64_t* total_qpad;  // qpad[B], written by the planner
   int64_t qpad_cap;
@@ -121,14 +128,14 @@ __global__ void __launch_bounds__(256) preprocess_items_kernel(const PreParams p
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n1 = *p.n_items, n2 = *p.n_items2;
-  for (int idx = blockIdx.x; idx < n1 + n2; idx += gridDim.x) {
-    const bool fused = idx >= n1;
-    const WorkItem it = fused ? p.items2[idx - n1] : p.items[idx];
+  const int n1 = *p.n_items, n2 = *p.n_items2, n3 = *p.n_items3;
+  for (int idx = blockIdx.x; idx < n1 + n2 + n3; idx += gridDim.x) {
+    const bool whole = idx >= n1;  // fused or non-sequence-parallel: every query tile of the sequence
+    const WorkItem it = idx < n1 ? p.items[idx] : idx < n1 + n2 ? p.items2[idx - n1] : p.items3[idx - n1 - n2];
     const int64_t qo = p.q_off[it.b];
     const int Lq = int(p.q_off[it.b + 1] - qo);
     const int64_t pad0 = int64_t(it.h) * p.qpad_cap + p.qpad[it.b];
-    const int t_lo = fused ? 0 : it.u0, t_hi = fused ? (Lq > 0 ? 1 : 0) : it.u1;
+    const int t_lo = whole ? 0 : it.u0, t_hi = whole ? (Lq + kBM - 1) / kBM : it.u1;
     for (int t = t_lo; t < t_hi; ++t) {
       // 8 warps x 16 rows.  A row of one head is D/8 16-byte chunks: a warp covers
       // 32 / (D/8) rows per load, and all of its 16 rows' loads are in flight at once.
@@ -253,7 +260,13 @@ struct BwdCfg {
   static constexpr int kRingFused = D == 128 ? 3 : 8;
   static constexpr uint32_t kColFdV = 256, kColFdQ = 256 + D;
   static constexpr int kSmemFused = 2 * kTileBytes + kRingFused * kTileBytes + 32768 + 1024 + 1024;
-  static_assert(kSmemDkdv <= 232448 && kSmemDq <= 232448 && kSmemFused + 1024 <= 232448, "shared memory per CTA");
+  // Non-sequence-parallel pass: K, V resident, dO / Q ring, dS^T staging, lse2 / D vectors.
+  // dQ_ij over dP^T at d = 128, in the columns d = 64 leaves free otherwise.
+  static constexpr int kRingNsp = D == 128 ? 3 : 8;
+  static constexpr uint32_t kColNspDq = D == 128 ? kColP : 384;
+  static constexpr int kSmemNsp = 2 * kTileBytes + kRingNsp * kTileBytes + 32768 + kVecSlots * 1024 + 1024;
+  static_assert(kSmemDkdv <= 232448 && kSmemDq <= 232448 && kSmemFused + 1024 <= 232448 && kSmemNsp + 1024 <= 232448,
+                "shared memory per CTA");
 };
 
 // Load one row-tile (128 rows x D columns, D/64 boxes of 16 KB) through a tensor map.
@@ -1788,7 +1801,583 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-enum BwdPass { kPassDkdv = 0, kPassDq = 1, kPassFused = 2 };
+// The 32 rows of a warp (one per lane) x 8 chunks of 16 bytes, transposed within groups of 8
+// lanes with xor-shuffles: afterwards lane base + i (base = lane & ~7) holds chunk i of rows
+// base .. base + 7 (c[k] = row base + k), so one instruction of the group covers 128
+// consecutive bytes of a row and one of the warp four whole rows' segments.
+__device__ __forceinline__ void xpose_rows8(uint4 (&c)[8]) {
+  const int i = threadIdx.x & 7;
+#pragma unroll
+  for (int s = 1; s < 8; s <<= 1) {
+    const bool hi = (i & s) != 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if ((k & s) == 0) {
+        const uint4 send = hi ? c[k] : c[k | s];
+        uint4 got;
+        got.x = __shfl_xor_sync(0xffffffffu, send.x, s);
+        got.y = __shfl_xor_sync(0xffffffffu, send.y, s);
+        got.z = __shfl_xor_sync(0xffffffffu, send.z, s);
+        got.w = __shfl_xor_sync(0xffffffffu, send.w, s);
+        if (hi) c[k] = got;
+        else c[k | s] = got;
+      }
+    }
+  }
+}
+
+// ================================================================== non-sequence-parallel pass
+// One CTA owns a (sequence, head) whose queries span 2 .. kNspMaxTiles tiles (the reading of
+// "Jagged Flash Attention (JFA)", "Four generations" item 2, in which the backward is not
+// parallel over a sequence's query tiles).  For each key tile j (K_j, V_j resident) and each
+// query tile i that sees it (Q_i, dO_i and the tile's lse2 / D vectors through a ring),
+// S^T, P^T, dP^T and dS^T are formed once and feed all three products
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i   (accumulated over i in TMEM, as in the dK/dV pass)
+//   dQ_ij = dS K_j                        (dS from a shared-memory staging of dS^T)
+// so a tile pair costs the five algorithmic GEMMs instead of the split passes' seven.  dQ_i
+// is summed over the key tiles in an fp32 buffer of the workspace by the epilogue thread
+// that owns the row -- a store at the first key tile, fp32 additions in key-tile order after
+// it, the bf16 dq row written at the last key tile that sees the query tile -- so every row
+// has one writer and one summation order: no atomics race and the result is deterministic.
+// TMEM: S^T [0,128), dP^T [128,256), dK [256,256+D), dV [256+D,256+2D); dQ_ij goes over dP^T
+// at d = 128 (after dK(i) has read dS^T there; the next dP^T waits for the dQ_ij drain) and
+// into [384,448) at d = 64.
+template <int D, bool kBias, bool kJBias = false>
+__global__ void __launch_bounds__(kThreadsDkdv, 1) nsp_kernel(const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int R = C::kRingNsp;
+  constexpr bool kDqOverDp = C::kColNspDq == C::kColP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kTileBytes;
+  uint8_t* sRing = smem + 2 * C::kTileBytes;
+  uint8_t* sDS = sRing + R * C::kTileBytes;             // dS^T: [keys][queries], two 64-query atoms
+  float* sVec = reinterpret_cast<float*>(sDS + 32768);   // [kVecSlots][2][128]: lse2, D
+
+  __shared__ uint64_t kv_full, kv_empty, st_full, dpt_full, p_full, ds_full, mma_done;
+  __shared__ uint64_t dv_full, dv_empty, dk_full, dk_empty, dq_full, dq_empty, dsm_empty;
+  __shared__ uint64_t ring_full[R], ring_empty[R];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ MetaRing meta;
+  __shared__ uint4 jb_scratch[kJBias ? 8 * 128 : 1];  // general bias: 2 KB transpose scratch per compute warp
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
+    mbar_init(&st_full, 1);
+    mbar_init(&dpt_full, 1);
+    mbar_init(&p_full, 256);
+    mbar_init(&ds_full, 256);
+    mbar_init(&dv_full, 1);
+    mbar_init(&dv_empty, 128);
+    mbar_init(&dk_full, 1);
+    mbar_init(&dk_empty, 128);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_empty, 128);
+    mbar_init(&dsm_empty, 1);
+    mbar_init(&mma_done, 1);
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
+    }
+    meta_init(meta, p.wait_ns, 3 + (kThreadsDkdv / 32 - kFirstComputeWarp));
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();  // the planner's lists and maps, the previous kernels' outputs
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n_items = *p.n_items;
+  volatile int* abort_flag = &abort_sh;
+  const bool causal = p.causal != 0;
+
+  if (warp < kFirstComputeWarp) {
+   setmaxnreg_dec<kRegsLoadNsp>();
+   if (warp == 2) {
+    // ------------------------------------------------------------ K/V loader
+    if (lane == 0) {
+      uint32_t item_n = 0;
+      int acq_b = -1;  // sequence whose maps this thread has acquired
+      bool ok = true;
+      uint32_t item_k = 0;
+      for (; ok; ++item_k) {
+        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+        const ItemMeta& wi = meta.e[item_k % kMetaSlots];  // read in place, freed after the item
+        if (wi.b < 0) break;  // end of this CTA's items
+        const int Lq = wi.Lq, Lk = wi.Lk;
+        acquire_seq_maps(p.maps, wi.b, kMapK, kMapV, acq_b, false);
+        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+          int first, count;
+          q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+          if (count == 0) continue;
+          const TileMap mk = tile_map(p.maps, p.B, kMapK, wi.b, wi.ko, kt, p.total_kv);
+          const TileMap mv = tile_map(p.maps, p.B, kMapV, wi.b, wi.ko, kt, p.total_kv);
+          if (mk.tail) {
+            tmap_acquire(mk.map);
+            tmap_acquire(mv.map);
+          }
+          if (!mbar_wait(&kv_empty, (item_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+          mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
+          load_tile<D>(sK, mk.map, &kv_full, wi.h * D, mk.y);
+          load_tile<D>(sV, mv.map, &kv_full, wi.h * D, mv.y);
+          ++item_n;
+          // the next key tile of this item, else the first of this CTA's next item, into L2
+          int nb = -1, nh = 0, nt = 0;
+          if (kt + 1 < wi.u1) {
+            nb = wi.b, nh = wi.h, nt = kt + 1;
+          } else if (const ItemMeta* wn = meta_peek_next(meta, item_k)) {
+            nb = wn->b, nh = wn->h, nt = wn->u0;
+          }
+          if (nb >= 0) {
+            const int64_t nko = p.kv_off[nb];
+            acquire_seq_maps(p.maps, nb, kMapK, kMapV, acq_b, true);
+            if (nt * kBN < int(p.kv_off[nb + 1] - nko)) {
+              prefetch_tile<D / 64>(p.maps, p.B, kMapK, nb, nko, nt, p.total_kv, nh * D);
+              prefetch_tile<D / 64>(p.maps, p.B, kMapV, nb, nko, nt, p.total_kv, nh * D);
+            }
+          }
+        }
+        if (ok) meta_release(meta, item_k);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      if (item_n > 0) drain_wait(&kv_full, (item_n - 1) & 1);
+    }
+   } else if (warp == 0) {
+    // ------------------------------------------------------------ dO / Q ring producer
+    if (lane == 0) {
+      uint32_t ring_n = 0, qtile_n = 0, tn = 0;
+      int acq_b = -1;
+      bool ok = true;
+      auto fill = [&](const TileMap& m, int col, const float* l2src, const float* dsrc) {
+        const uint32_t e = ring_n % R, ph = (ring_n / R) & 1;
+        if (m.tail) tmap_acquire(m.map);
+        if (!mbar_wait(&ring_empty[e], ph ^ 1, abort_flag, kWaitTimeoutNs)) return false;
+        trace_event(p.trace, kTraceProducer, tn, 2);
+        mbar_arrive_expect_tx(&ring_full[e], C::kTileBytes + (l2src ? 2 * kBM * 4 : 0));
+        load_tile<D>(sRing + e * C::kTileBytes, m.map, &ring_full[e], col, m.y);
+        if (l2src) {
+          float* v = sVec + (qtile_n % C::kVecSlots) * 256;
+          bulk_load(v, l2src, kBM * 4, &ring_full[e]);
+          bulk_load(v + 128, dsrc, kBM * 4, &ring_full[e]);
+        }
+        ++ring_n;
+        return true;
+      };
+      uint32_t item_k = 0;
+      for (; ok; ++item_k) {
+        if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+        const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+        if (wi.b < 0) break;  // end of this CTA's items
+        const int Lq = wi.Lq, Lk = wi.Lk;
+        acquire_seq_maps(p.maps, wi.b, kMapQ, kMapDO, acq_b, false);
+        const int64_t vec0 = int64_t(wi.h) * p.qpad_cap + wi.qp;
+        for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+          int first, count;
+          q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+          for (int i = 0; i < count && ok; ++i) {
+            const int qt = first + i;
+            const TileMap mdo = tile_map(p.maps, p.B, kMapDO, wi.b, wi.qo, qt, p.total_q);
+            const TileMap mq = tile_map(p.maps, p.B, kMapQ, wi.b, wi.qo, qt, p.total_q);
+            // Q first: it is released after dK, dO after dV, so with Q ahead the next Q's
+            // slot frees up a tile pair earlier (S^T of the next query tile is not held up)
+            if (!fill(mq, wi.h * D, p.lse2 + vec0 + qt * kBM, p.delta + vec0 + qt * kBM)) {
+              ok = false;
+              break;
+            }
+            if (!fill(mdo, wi.h * D, nullptr, nullptr)) { ok = false; break; }
+            ++qtile_n;
+          }
+        }
+        if (ok) meta_release(meta, item_k);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      const uint32_t f = ring_n > uint32_t(R) ? ring_n - R : 0;
+      for (uint32_t n = f; n < ring_n; ++n) drain_wait(&ring_full[n % R], (n / R) & 1);
+    }
+   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);  // A K-major (TMEM), B MN-major
+      constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, true, true);    // A (dS) and B (K) MN-major
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(sRing), aDS = smem_u32(sDS);
+      uint32_t ring_n = 0, item_n = 0, g = 0, acc_n = 0, tn = 0;
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (!mbar_wait(bar, par, abort_flag, kWaitTimeoutNs)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto wait_ring = [&](uint32_t n) { return wait(&ring_full[n % R], (n / R) & 1); };
+      auto ra = [&](uint32_t n) { return aR + (n % R) * C::kTileBytes; };
+      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {  // (keys x queries) = A(keys x D) B(queries x D)^T
+        const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
+        }
+      };
+      auto mma_acc = [&](uint32_t dcol, uint32_t xcol, uint32_t b, bool acc) {  // acc(keys x D) += X^T B
+        const uint64_t bd = sdesc_sw128(b, 16384, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * 64 + (kk & 3) * 8, bd + uint32_t(kk * 2048 >> 4), kIdAcc,
+                  (acc || kk > 0) ? 1u : 0u);
+      };
+      uint32_t item_k = 0;
+      for (; ok; ++item_k) {
+       if (!meta_wait(meta, item_k, abort_flag)) { ok = false; break; }
+       const ItemMeta& wi = meta.e[item_k % kMetaSlots];
+       if (wi.b < 0) break;  // end of this CTA's items
+       const int Lq = wi.Lq, Lk = wi.Lk;
+       for (int kt = wi.u0; kt < wi.u1 && ok; ++kt) {
+        int first, count;
+        q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+        if (count == 0) continue;
+        if (!wait(&kv_full, item_n & 1)) { ok = false; break; }
+        ++item_n;
+        trace_event(p.trace, kTraceMma, tn, 10);
+        const uint32_t n0 = ring_n;  // Q_i at n0 + 2i, dO_i at n0 + 2i + 1
+        if (!wait_ring(n0)) { ok = false; break; }
+        mma_nt(C::kColS, aK, ra(n0));
+        umma_commit(&st_full);
+        // d = 128: dP^T's columns held the previous tile pair's dQ: wait for its drain
+        if (kDqOverDp && !wait(&dq_empty, (g & 1) ^ 1)) { ok = false; break; }
+        if (!wait_ring(n0 + 1)) { ok = false; break; }
+        mma_nt(C::kColP, aV, ra(n0 + 1));
+        umma_commit(&dpt_full);
+        for (int i = 0; i < count && ok; ++i) {
+          const uint32_t nq = n0 + 2 * i, nd = nq + 1;
+          if (!wait(&p_full, g & 1)) { ok = false; break; }
+          trace_event(p.trace, kTraceMma, tn, 11);
+          if (i == 0 && !wait(&dv_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
+          mma_acc(C::kColA1, C::kColS, ra(nd), i > 0);  // dV += P^T dO
+          umma_commit(&ring_empty[nd % R]);
+          if (i + 1 == count) umma_commit(&dv_full);
+          if (i + 1 < count) {
+            if (!wait_ring(nq + 2)) { ok = false; break; }
+            mma_nt(C::kColS, aK, ra(nq + 2));
+            umma_commit(&st_full);
+          }
+          if (!wait(&ds_full, g & 1)) { ok = false; break; }
+          trace_event(p.trace, kTraceMma, tn, 14);
+          if (i == 0 && !wait(&dk_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
+          mma_acc(C::kColA0, C::kColP, ra(nq), i > 0);  // dK += dS^T Q
+          umma_commit(&ring_empty[nq % R]);
+          // dQ_ij = dS K_j: the staging read as an MN-major A (queries x keys), K MN-major
+          if (!kDqOverDp && !wait(&dq_empty, (g & 1) ^ 1)) { ok = false; break; }
+          {
+            const uint64_t ad = sdesc_sw128(aDS, 16384, 1024), bd = sdesc_sw128(aK, 16384, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ss(tmem + C::kColNspDq, ad + uint32_t(kk * 2048 >> 4), bd + uint32_t(kk * 2048 >> 4), kIdDq,
+                      kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&dq_full);
+          umma_commit(&dsm_empty);
+          trace_event(p.trace, kTraceMma, tn, 15);
+          if (i + 1 < count) {
+            if (kDqOverDp && !wait(&dq_empty, g & 1)) { ok = false; break; }
+            trace_event(p.trace, kTraceMma, tn, 16);
+            if (!wait_ring(nd + 2)) { ok = false; break; }
+            mma_nt(C::kColP, aV, ra(nd + 2));
+            umma_commit(&dpt_full);
+            trace_event(p.trace, kTraceMma, tn, 17);
+          }
+          ++g;
+        }
+        if (!ok) break;
+        ring_n = n0 + 2 * count;
+        ++acc_n;
+        umma_commit(&dk_full);
+        umma_commit(&kv_empty);  // K is read by S^T and dQ, V by dP^T
+       }
+       if (ok) meta_release(meta, item_k);
+      }
+      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+      umma_commit(&mma_done);
+      drain_wait(&mma_done, 0);
+    }
+   } else if (warp == 3) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0 && !meta_publish(meta, p.items, n_items, p.claim, p.q_off, p.kv_off, p.qpad, p.jb_off, abort_flag))
+      raise_status(p.status, JFA_ERR_TIMEOUT);
+   }
+  } else if (warp < kFirstEpilogueWarp) {
+    setmaxnreg_inc<kRegsComputeNsp>();
+    // ------------------------------------------------------------ compute warpgroups
+    const int w = (warp - kFirstComputeWarp) >> 2;  // column half owned: queries [64w, 64w+64)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row within the tile
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
+    const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
+    uint8_t* drow = sDS + w * 16384 + row * 128;  // this key's 64 queries in the dS^T staging
+    const float sl2 = p.scale_log2;
+    uint32_t ring_n = 0, tile_n = 0, qtile_n = 0, tn = 0;
+    const bool leader = (warp & 3) == 0 && lane == 0;
+    bool ok = true;
+    uint32_t item_k = 0;
+    for (; ok; ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];
+     if (it.b < 0) break;  // end of this CTA's items
+     const int Lq = it.Lq, Lk = it.Lk;
+     for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
+      int first, count;
+      q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+      const int j = kt * kBN + row;  // local key index
+      if (count == 0) continue;  // rows of zeros: written by the epilogue warpgroup
+      const int diag = Lk - Lq;  // key j visible to query i iff i >= j - diag
+      const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
+      for (int i = 0; i < count && ok; ++i) {
+        const int qt = first + i;
+        uint4 jbw[8];  // general bias for this tile (row order), loaded before the waits
+        if (kJBias) {
+          const int64_t pitch = (Lk + 7) / 8 * 8;
+          const int qi0 = qt * kBM + 64 * w, kj0 = kt * kBN + quarter * 32;
+          jbias_load_cols_vec(jbw, p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(qi0) * pitch + kj0, pitch,
+                              Lq - qi0, Lk - kj0, lane);
+        }
+        // Q_i's ring slot (the first of the pair) carries this tile's lse2 / D vectors
+        const uint32_t nq = ring_n;
+        if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ring_n += 2;
+        const float* vec = sVec + (qtile_n % C::kVecSlots) * 256;
+        ++qtile_n;
+        const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(vec + 64 * w);        // -lse2 pairs
+        const uint64_t* ndvec = reinterpret_cast<const uint64_t*>(vec + 128 + 64 * w);  // -D pairs
+        if (!mbar_wait(&st_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
+        float x[64];
+        ld_cols64(tS, x);
+        const int i0 = qt * kBM + 64 * w;  // local query index of column 0 of this half
+        if (kJBias) {
+          uint32_t jbk[32];
+          jbias_col_transpose(jbk, jbw, jb_scratch + (warp - kFirstComputeWarp) * 128, j < Lk, lane);
+          jbias_apply<64>(x, jbk, sl2, kLog2e);
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
+        } else if (kBias) {
+          const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
+          if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2)
+              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
+                               f2_pack(__ldg(brow + idx0 - 2 * c2), __ldg(brow + idx0 - 2 * c2 - 1))),
+                        x[2 * c2], x[2 * c2 + 1]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
+          }
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
+        } else {
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
+        }
+        if (causal) {
+          const int lim = j - diag - i0;  // columns c < lim are hidden
+          if (lim > 0) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < lim) x[c] = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P^T
+        st_bf16_64(tS, x);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full);
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 21);
+        if (!mbar_wait(&dpt_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 22);
+        float dp[64];
+        ld_cols64(tP, dp);
+#pragma unroll
+        for (int c2 = 0; c2 < 32; ++c2)  // dS^T = P^T o (dP^T - D)
+          f2_unpack(f2_mul(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_add(f2_pack(dp[2 * c2], dp[2 * c2 + 1]), ndvec[c2])),
+                    dp[2 * c2], dp[2 * c2 + 1]);
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) pk[t] = pack_bf16x2(dp[2 * t], dp[2 * t + 1]);
+        tmem_st32(tP, pk);  // for dK (TMEM operand)
+        // and into the staging for dQ, once the previous tile pair's dQ MMA has read it
+        if (!mbar_wait(&dsm_empty, (tile_n & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+#pragma unroll
+        for (int chunk = 0; chunk < 8; ++chunk)
+          *reinterpret_cast<uint4*>(drow + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * chunk], pk[4 * chunk + 1], pk[4 * chunk + 2], pk[4 * chunk + 3]);
+        fence_proxy_async_smem();  // the MMAs read the staging through the async proxy
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
+        ++tile_n;
+        if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 23);
+        if (kJBias && p.jb_grad) {  // the general bias's gradient is dS itself
+          const int64_t pitch = (Lk + 7) / 8 * 8;
+          const int kj0 = kt * kBN + quarter * 32;
+          jbias_store_cols(pk, jb_scratch + (warp - kFirstComputeWarp) * 128,
+                           p.jb_grad + size_t(it.h) * p.jb_plane + it.jb + int64_t(i0) * pitch + kj0, pitch, Lq - i0,
+                           Lk - kj0, j < Lk, lane);
+        }
+        if (kBias && p.bias_grad) {
+          // dS^T of a padded key row is not zero (k = 0 but lse2 of the query is not), and
+          // padded query columns only give 0 while their P^T stays finite: count neither
+          const int ncols = j < Lk ? Lq - i0 : 0;
+          if (ncols < 64) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c >= ncols) dp[c] = 0.f;
+          }
+          dbias_warp_tile(dp, p.bias_grad + size_t(it.h) * p.num_buckets, p.num_buckets,
+                          kt * kBN + quarter * 32 - i0 - 63 + p.center, lane);
+        }
+      }
+      if (!ok) break;
+     }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  } else {
+    setmaxnreg_dec<kRegsEpiNsp>();
+    // ------------------------------------------------------------ epilogue warpgroup
+    // Per tile pair: this thread's dQ_ij row (TMEM lane = query row) into the fp32 sum
+    // (store, then additions, then the bf16 dq row at the query tile's last key tile).  Per
+    // key tile: its dV and dK rows (TMEM lane = key row), as in the dK/dV pass.  Per item:
+    // zero dq rows for query tiles that see no key.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    uint32_t acc_n = 0, g = 0, tn = 0;
+    const bool leader = warp == kFirstEpilogueWarp && lane == 0;  // traces as role 4 in this pass
+    bool ok = true;
+    uint32_t item_k = 0;
+    for (; ok; ++item_k) {
+     if (!meta_wait_warp(meta, item_k, abort_flag)) { ok = false; break; }
+     const ItemMeta& it = meta.e[item_k % kMetaSlots];
+     if (it.b < 0) break;  // end of this CTA's items
+     const int64_t ko = it.ko, qo = it.qo;
+     const int Lq = it.Lq, Lk = it.Lk;
+     const int nq = (Lq + kBM - 1) / kBM;
+     for (int qt = 0; qt < nq; ++qt) {  // query tiles no key reaches: zero dq rows
+       if (kv_tiles_for_q_tile(qt, Lq, Lk, causal) > 0) continue;
+       const int qi = qt * kBM + row;
+       store_acc_row_own<D>(0, 0.f, p.g2 + ((qo + qi) * p.H + it.h) * int64_t(D), qi < Lq, true);
+     }
+     for (int kt = it.u0; kt < it.u1 && ok; ++kt) {
+      int first, count;
+      q_tiles_for_kv_tile(kt, Lq, Lk, causal, &first, &count);
+      const int j = kt * kBN + row;  // local key index
+      const bool valid = j < Lk;
+      __nv_bfloat16* dk_row = p.g0 + ((ko + j) * p.H + it.h) * int64_t(D);
+      __nv_bfloat16* dv_row = p.g1 + ((ko + j) * p.H + it.h) * int64_t(D);
+      if (count == 0) {  // no query sees these keys
+        if (kt * kBN < Lk) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            store_acc_row<32>(0, 0.f, dk_row + c0, valid, true);
+            store_acc_row<32>(0, 0.f, dv_row + c0, valid, true);
+          }
+        }
+        continue;
+      }
+      for (int i = 0; i < count && ok; ++i) {
+        const int qt = first + i;
+        const int qi = qt * kBM + row;  // local query index of this thread's dQ row
+        const bool qvalid = qi < Lq;
+        const int jl = kv_tiles_for_q_tile(qt, Lq, Lk, causal) - 1;  // last key tile that sees qt
+        float* acc = p.dqacc + ((qo + qi) * p.H + it.h) * int64_t(D);
+        __nv_bfloat16* dq_row = p.g2 + ((qo + qi) * p.H + it.h) * int64_t(D);
+        if (!mbar_wait(&dq_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++g;
+        tc_fence_after();
+        if (leader) trace_event(p.trace, kTraceLoader, tn, 30);
+        // rows of this warp are 32 tokens apart in memory: transpose 32 columns at a time so
+        // each store / addition instruction writes four rows' 128-byte segments
+        const int base = lane & ~7, sub = lane & 7;
+        const unsigned long long my_acc = qvalid ? reinterpret_cast<unsigned long long>(acc) : 0ull;
+        const unsigned long long my_dq = qvalid ? reinterpret_cast<unsigned long long>(dq_row) : 0ull;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint4 c[8];
+          {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_addr + C::kColNspDq + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) c[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+          }
+          if (c0 + 32 == D) {  // the whole row is in registers: the MMA may reuse the columns
+            tc_fence_before();
+            mbar_arrive(&dq_empty);
+            if (leader) trace_event(p.trace, kTraceLoader, tn, 31);
+          }
+          xpose_rows8(c);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const unsigned long long ra = __shfl_sync(0xffffffffu, my_acc, base + k);
+            const unsigned long long rq = __shfl_sync(0xffffffffu, my_dq, base + k);
+            if (ra == 0ull) continue;  // a padding query row
+            float* a4 = reinterpret_cast<float*>(ra) + c0 + 4 * sub;
+            float v0 = __uint_as_float(c[k].x), v1 = __uint_as_float(c[k].y), v2 = __uint_as_float(c[k].z),
+                  v3 = __uint_as_float(c[k].w);
+            if (kt == jl) {  // the last contribution: finish the row segment in bf16
+              if (kt > 0) {  // add the sum of the earlier key tiles
+                const float4 a = ld_global_cg_v4f(a4);
+                v0 += a.x, v1 += a.y, v2 += a.z, v3 += a.w;
+              }
+              __nv_bfloat16* q4 = reinterpret_cast<__nv_bfloat16*>(rq) + c0 + 4 * sub;
+              *reinterpret_cast<uint2*>(q4) = make_uint2(pack_bf16x2(v0 * p.scale, v1 * p.scale),
+                                                         pack_bf16x2(v2 * p.scale, v3 * p.scale));
+            } else if (kt == 0) {  // the first contribution: store
+              st_global_v4f(a4, v0, v1, v2, v3);
+            } else {  // in between: add (this row has one owner, so the order is the key tiles')
+              red_add_global_v4(a4, v0, v1, v2, v3);
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      if (leader) trace_event(p.trace, kTraceLoader, tn, 32);
+      if (!mbar_wait(&dv_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      tc_fence_after();
+      drain_acc_rows<D>(tmem + lane_addr + C::kColA1, 1.f, dv_row, valid, &dv_empty);
+      if (!mbar_wait(&dk_full, acc_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+      ++acc_n;
+      tc_fence_after();
+      drain_acc_rows<D>(tmem + lane_addr + C::kColA0, p.scale, dk_row, valid, &dk_empty);
+     }
+     if (__all_sync(0xffffffffu, ok)) meta_release_warp(meta, item_k);
+    }
+    if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+enum BwdPass { kPassDkdv = 0, kPassDq = 1, kPassFused = 2, kPassNsp = 3 };
 
 BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLayout& L, int pass) {
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -1803,7 +2392,8 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.scale_log2 = pr.scale * kLog2e;
   bp.causal = pr.causal;
   bp.bias2 = pr.bias_table ? reinterpret_cast<const float*>(w + L.bias2) : nullptr;
-  // the dK/dV and fused passes together see every visible pair once: they add the bias gradient
+  // the dK/dV, fused and non-sequence-parallel passes together see every visible pair once:
+  // they add the bias gradient
   bp.bias_grad = (pr.bias_table && pass != kPassDq) ? pr.bias_grad : nullptr;
   bp.num_buckets = pr.num_buckets;
   bp.center = pr.center;
@@ -1812,14 +2402,18 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.jb_plane = pr.jb_plane;
   bp.jb_grad = pass != kPassDq ? static_cast<__nv_bfloat16*>(pr.jb_grad) : nullptr;
   bp.maps = reinterpret_cast<const CUtensorMap*>(w + L.maps);
-  bp.items = reinterpret_cast<const WorkItem*>(w + (pass == kPassDq ? L.dq : pass == kPassFused ? L.fused : L.dkv));
+  bp.items = reinterpret_cast<const WorkItem*>(
+      w + (pass == kPassDq ? L.dq : pass == kPassFused ? L.fused : pass == kPassNsp ? L.nsp : L.dkv));
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(w);
-  bp.n_items = pass == kPassDq ? &hdr->n_dq : pass == kPassFused ? &hdr->n_fused : &hdr->n_dkv;
+  bp.n_items = pass == kPassDq ? &hdr->n_dq : pass == kPassFused ? &hdr->n_fused
+                                           : pass == kPassNsp ? &hdr->n_nsp : &hdr->n_dkv;
   WsHeader* mh = reinterpret_cast<WsHeader*>(w);
-  bp.claim = pass == kPassDq ? &mh->claim_dq : pass == kPassFused ? &mh->claim_fused : &mh->claim_dkv;
+  bp.claim = pass == kPassDq ? &mh->claim_dq : pass == kPassFused ? &mh->claim_fused
+                                             : pass == kPassNsp ? &mh->claim_nsp : &mh->claim_dkv;
   bp.status = &reinterpret_cast<WsHeader*>(w)->status;
-  // list kinds of the planner: forward 0, dQ 1, dK/dV 2, fused 3
-  bp.wait_ns = &hdr->wait_ns[pass == kPassDq ? 1 : pass == kPassFused ? 3 : 2];
+  // list kinds of the planner: forward 0, dQ 1, dK/dV 2, fused 3, non-sequence-parallel 4
+  bp.wait_ns = &hdr->wait_ns[pass == kPassDq ? 1 : pass == kPassFused ? 3 : pass == kPassNsp ? 4 : 2];
+  bp.dqacc = reinterpret_cast<float*>(w + L.dqacc);
   (void)lse;
   bp.lse2 = reinterpret_cast<const float*>(w + L.lse2);
   bp.delta = reinterpret_cast<const float*>(w + L.delta);
@@ -1828,7 +2422,8 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   bp.g0 = nullptr;
   bp.g1 = nullptr;
   bp.g2 = nullptr;
-  bp.trace = pr.trace[pass == kPassDq ? JFA_KERNEL_BWD_DQ : pass == kPassFused ? JFA_KERNEL_BWD_FUSED : JFA_KERNEL_BWD_DKDV];
+  bp.trace = pr.trace[pass == kPassDq ? JFA_KERNEL_BWD_DQ : pass == kPassFused ? JFA_KERNEL_BWD_FUSED
+                     : pass == kPassNsp ? JFA_KERNEL_BWD_NSP : JFA_KERNEL_BWD_DKDV];
   return bp;
 }
 
@@ -1855,6 +2450,8 @@ cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const voi
   pp.n_items = &reinterpret_cast<const WsHeader*>(w)->n_dq;
   pp.items2 = reinterpret_cast<const WorkItem*>(w + L.fused);
   pp.n_items2 = &reinterpret_cast<const WsHeader*>(w)->n_fused;
+  pp.items3 = reinterpret_cast<const WorkItem*>(w + L.nsp);
+  pp.n_items3 = &reinterpret_cast<const WsHeader*>(w)->n_nsp;
   pp.qpad = reinterpret_cast<const int64_t*>(w + L.qpad);
   pp.total_qpad = &reinterpret_cast<const WsHeader*>(w)->total_qpad;
   pp.qpad_cap = L.qpad_cap;
@@ -1925,6 +2522,22 @@ cudaError_t launch_bwd_dq(const Problem& pr, const float* lse, void* ws, const W
   return bias ? launch_dkdv_k(dq_kernel<64, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
               : jb ? launch_dkdv_k(dq_kernel<64, false, true>, BwdCfg<64>::kSmemDq, num_sms, bp, stream)
                    : launch_dkdv_k(dq_kernel<64, false>, BwdCfg<64>::kSmemDq, num_sms, bp, stream);
+}
+
+cudaError_t launch_bwd_nsp(const Problem& pr, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,
+                           void* dv, int num_sms, cudaStream_t stream) {
+  BwdParams bp = make_params(pr, lse, ws, L, kPassNsp);
+  bp.g0 = static_cast<__nv_bfloat16*>(dk);
+  bp.g1 = static_cast<__nv_bfloat16*>(dv);
+  bp.g2 = static_cast<__nv_bfloat16*>(dq);
+  const bool bias = pr.bias_table != nullptr, jb = pr.jbias != nullptr;
+  if (pr.d == 128)
+    return bias ? launch_dkdv_k(nsp_kernel<128, true>, BwdCfg<128>::kSmemNsp, num_sms, bp, stream)
+                : jb ? launch_dkdv_k(nsp_kernel<128, false, true>, BwdCfg<128>::kSmemNsp, num_sms, bp, stream)
+                     : launch_dkdv_k(nsp_kernel<128, false>, BwdCfg<128>::kSmemNsp, num_sms, bp, stream);
+  return bias ? launch_dkdv_k(nsp_kernel<64, true>, BwdCfg<64>::kSmemNsp, num_sms, bp, stream)
+              : jb ? launch_dkdv_k(nsp_kernel<64, false, true>, BwdCfg<64>::kSmemNsp, num_sms, bp, stream)
+                   : launch_dkdv_k(nsp_kernel<64, false>, BwdCfg<64>::kSmemNsp, num_sms, bp, stream);
 }
 
 }  // namespace jfa

@@ -71,6 +71,15 @@ struct WorkItem {
 };
 constexpr int kItemsPerCta = 4;  // target items per CTA when capping range cost
 
+// Backward paths by query length: one query tile (Lq <= 128) -> the fused short-query
+// pass; 2 .. nsp_max_tiles query tiles -> the non-sequence-parallel pass (one CTA owns the
+// sequence and head: every tile pair once, dQ summed over key tiles in fp32); longer ->
+// the split dK/dV and dQ passes.  nsp_max_tiles is a process-wide setting
+// (jfa_set_nsp_max_tiles), 0 .. kNspMaxTiles; below 2 no sequence takes the pass.
+constexpr int kNspMaxTiles = 16;
+constexpr int kNspDefaultMaxTiles = 0;
+__host__ __device__ inline bool nsp_path(int Lq, int max_tiles) { return Lq > kBM && Lq <= max_tiles * kBM; }
+
 // Tensor-map slots per sequence (per-sequence maps clip TMA boxes at the sequence end
 // so rows past it arrive as zeros).
 enum MapSlot { kMapQ = 0, kMapK = 1, kMapV = 2, kMapDO = 3, kNumMapSlots = 4 };
@@ -118,13 +127,16 @@ struct WsHeader {
   int n_dkv;       // number of dK/dV items
   int64_t total_qpad;  // sum_b round_up(Lq_b, 128): rows of the padded per-query vectors
   int n_fused;     // number of fused short-query backward items
-  // next unclaimed item of each list (forward, dQ, dK/dV, fused), zeroed by the planner
+  // next unclaimed item of each list (forward, dQ, dK/dV, fused, non-sequence-parallel),
+  // zeroed by the planner
   int claim_fwd, claim_dq, claim_dkv, claim_fused;
-  int pad0;
-  // bounded-wait limit of the kernel that walks each list (forward, dQ, dK/dV, fused), in
-  // ns, from wait_limit_ns over the list's planned tile pairs (written by the planner)
-  uint64_t wait_ns[4];
-  int pad[44];
+  int claim_nsp;
+  // item hand-off wait limit of the kernel that walks each list (forward, dQ, dK/dV, fused,
+  // non-sequence-parallel), in ns, from wait_limit_ns over the list's planned tile pairs
+  // (written by the planner)
+  uint64_t wait_ns[5];
+  int n_nsp;       // number of non-sequence-parallel backward items
+  int pad[41];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -136,12 +148,14 @@ struct WsLayout {
   size_t dq = 0;       // WorkItem[cap_dq]
   size_t dkv = 0;      // WorkItem[cap_dkv]
   size_t fused = 0;    // WorkItem[cap_fused]  backward: sequences whose queries fit one tile
+  size_t nsp = 0;      // WorkItem[cap_nsp]    backward: sequences of 2 .. kNspMaxTiles query tiles
+  size_t dqacc = 0;    // float[total_q][H][d] backward: their dQ sums over key tiles
   size_t bias2 = 0;    // float[H][num_buckets]  bias table pre-multiplied by log2(e)
   size_t qpad = 0;     // int64[B+1]  backward: offsets of each sequence in the padded vectors
   size_t lse2 = 0;     // float[H][qpad_cap]  backward: lse * log2(e) (+inf if -inf), 0 on padding
   size_t delta = 0;    // float[H][qpad_cap]  backward: D_i = rowsum(dO * O), 0 on padding
   size_t total = 0;
-  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0, cap_fused = 0, qpad_cap = 0;
+  int64_t cap_fwd = 0, cap_dq = 0, cap_dkv = 0, cap_fused = 0, cap_nsp = 0, qpad_cap = 0;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -172,6 +186,11 @@ __host__ __device__ inline WsLayout make_layout(int B, int H, int d, int64_t tot
     L.cap_fused = int64_t(H) * (B + 1);
     L.fused = align_up(off, 16);
     off = L.fused + size_t(L.cap_fused) * sizeof(WorkItem);
+    L.cap_nsp = int64_t(H) * (B + 1);
+    L.nsp = align_up(off, 16);
+    off = L.nsp + size_t(L.cap_nsp) * sizeof(WorkItem);
+    L.dqacc = align_up(off, 256);
+    off = L.dqacc + size_t(total_q) * size_t(H) * size_t(d) * sizeof(float);
     L.qpad = align_up(off, 256);
     off = L.qpad + size_t(B + 1) * sizeof(int64_t);
     L.qpad_cap = int64_t(align_up(size_t(total_q) + size_t(kBM) * B, kBM));  // rows per head, 512-B aligned

@@ -22,6 +22,7 @@ struct Problem {
   int64_t jb_plane;
   void* jb_grad;            // its gradient (backward), bf16 [H][jb_plane], or nullptr
   TraceBuf trace[JFA_NUM_KERNEL_KINDS];  // per kernel kind (JFA_KERNEL_*): developer tracing, buf == nullptr when off
+  int nsp_max_tiles;        // backward: query tiles up to which a sequence takes the non-sequence-parallel pass
 };
 
 struct PlanMaps {
@@ -87,6 +88,10 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const float* lse, void* ws, const 
                             void* dv, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dq,
                           int num_sms, cudaStream_t stream);
+// Sequences of 2 .. kNspMaxTiles query tiles: one CTA per sequence and head, every tile
+// pair once, dQ summed over key tiles in the workspace.
+cudaError_t launch_bwd_nsp(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,
+                           void* dv, int num_sms, cudaStream_t stream);
 // Sequences whose queries fit one tile: dQ, dK and dV in one pass over K and V.
 cudaError_t launch_bwd_fused(const Problem& p, const float* lse, void* ws, const WsLayout& L, void* dq, void* dk,
                              void* dv, int num_sms, cudaStream_t stream);

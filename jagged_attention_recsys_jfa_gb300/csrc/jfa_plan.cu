@@ -19,6 +19,7 @@ struct PlanParams {
   int64_t total_q, total_kv;
   int causal, backward;
   int grid;  // persistent CTAs of the kernels that consume the lists
+  int nsp_max_tiles;  // query tiles up to which a sequence takes the non-sequence-parallel pass
   uint8_t* ws;
   WsLayout L;
   const float* bias;  // [H][nb] or nullptr
@@ -28,22 +29,31 @@ struct PlanParams {
   int64_t jb_plane;
 };
 
-enum ListKind { kListFwd = 0, kListDq = 1, kListDkv = 2, kListFused = 3 };
+enum ListKind { kListFwd = 0, kListDq = 1, kListDkv = 2, kListFused = 3, kListNsp = 4 };
 
 // Backward: a sequence whose queries fit one tile (Lq <= 128) is done by the fused pass
-// (one CTA per sequence and head, every key tile once); the others by the split
-// dK/dV and dQ passes.
-__device__ __forceinline__ int list_units(int kind, int Lq, int Lk) {
+// (one CTA per sequence and head, every key tile once); one of 2 .. kNspMaxTiles query
+// tiles by the non-sequence-parallel pass (one CTA per sequence and head, every tile pair
+// once); the others by the split dK/dV and dQ passes.  Units: key tiles, except for the
+// forward (query-tile pairs) and the dQ pass (query tiles); a sequence without keys still
+// gets one unit in the fused and non-sequence-parallel lists (its dq rows are zeroed there).
+__device__ __forceinline__ int list_units(int kind, int Lq, int Lk, int nsp_max) {
   const int nq = (Lq + kBM - 1) / kBM;
   const int nk = (Lk + kBN - 1) / kBN;
   if (kind == kListFwd) return (nq + 1) / 2;
   if (kind == kListFused) return Lq <= kBM ? (nk > 0 ? nk : (Lq > 0 ? 1 : 0)) : 0;
-  if (Lq <= kBM) return 0;
+  if (kind == kListNsp) return nsp_path(Lq, nsp_max) ? (nk > 0 ? nk : 1) : 0;
+  if (Lq <= kBM || nsp_path(Lq, nsp_max)) return 0;
   return kind == kListDq ? nq : nk;
 }
 
 __device__ __forceinline__ int unit_cost(int kind, int u, int Lq, int Lk, bool causal) {
   if (kind == kListFused) return 1;  // a key tile (its dK / dV rows are stored even when unseen)
+  if (kind == kListNsp) {            // the query tiles that see key tile u (at least 1)
+    int first, count;
+    q_tiles_for_kv_tile(u, Lq, Lk, causal, &first, &count);
+    return count > 0 ? count : 1;
+  }
   if (kind == kListFwd)
     return kv_tiles_for_q_tile(2 * u, Lq, Lk, causal) + kv_tiles_for_q_tile(2 * u + 1, Lq, Lk, causal);
   if (kind == kListDq) return kv_tiles_for_q_tile(u, Lq, Lk, causal);
@@ -100,8 +110,8 @@ __device__ int scan_desc(const int* hist, int* base) {
 // Walk the units of one sequence, cutting them into consecutive ranges whose summed
 // cost stays <= cap (a unit costlier than cap forms its own range); calls f(u0, u1, cost).
 template <typename F>
-__device__ void for_each_range(int kind, int Lq, int Lk, bool causal, long long cap, F&& f) {
-  const int n = list_units(kind, Lq, Lk);
+__device__ void for_each_range(int kind, int Lq, int Lk, bool causal, int nsp_max, long long cap, F&& f) {
+  const int n = list_units(kind, Lq, Lk, nsp_max);
   int start = 0;
   long long acc = 0;
   for (int u = 0; u < n; ++u) {
@@ -126,21 +136,22 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
-    const int n = list_units(kind, Lq, Lk);
+    const int n = list_units(kind, Lq, Lk, p.nsp_max_tiles);
     for (int u = 0; u < n; ++u) local += unit_cost(kind, u, Lq, Lk, causal);
   }
   block_scan_incl(local, &total_cost);
   const long long share = (total_cost * p.H + (long long)kItemsPerCta * p.grid - 1) /
                           ((long long)kItemsPerCta * p.grid);
-  // the fused pass owns each sequence's dQ tile: its items are never cut into ranges
-  const long long range_cap = kind == kListFused ? (1ll << 62) : (share > 1 ? share : 1);
+  // the fused and non-sequence-parallel passes own each sequence's dQ: their items are
+  // never cut into ranges
+  const long long range_cap = (kind == kListFused || kind == kListNsp) ? (1ll << 62) : (share > 1 ? share : 1);
 
   for (int c = tid; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
   __syncthreads();
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
-    for_each_range(kind, Lq, Lk, causal, range_cap, [&](int, int, long long cost) {
+    for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int, int, long long cost) {
       atomicAdd(&hist[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
     });
   }
@@ -160,7 +171,7 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
     unsigned long long mx = 0;
-    for_each_range(kind, Lq, Lk, causal, range_cap, [&](int u0, int u1, long long cost) {
+    for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int u0, int u1, long long cost) {
       const int pos = atomicAdd(&base[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
       for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u0, u1};
       if ((unsigned long long)cost > mx) mx = (unsigned long long)cost;
@@ -207,7 +218,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
   grid_dependency_wait();    // the offsets and the workspace may come from earlier work
   grid_launch_dependents();  // the next kernel may start its prologue; it waits for this one
 
-  const int list_ctas = p.backward ? 3 : 1;
+  const int list_ctas = p.backward ? 4 : 1;
   if (int(blockIdx.x) >= list_ctas) {
     const size_t gt = size_t(blockIdx.x - list_ctas) * blockDim.x + tid;
     const size_t gstride = size_t(gridDim.x - list_ctas) * blockDim.x;
@@ -284,12 +295,12 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
       bad = 1;
     if (p.jb_off && (p.jb_off[0] != 0 || p.jb_off[p.B] != p.jb_plane)) bad = 1;
   }
-  if (blockIdx.x == 0 && tid == 0) hdr->claim_fwd = hdr->claim_dq = hdr->claim_dkv = hdr->claim_fused = 0;
+  if (blockIdx.x == 0 && tid == 0) hdr->claim_fwd = hdr->claim_dq = hdr->claim_dkv = hdr->claim_fused = hdr->claim_nsp = 0;
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) {
       atomicCAS(&hdr->status, 0, int(JFA_ERR_BAD_OFFSETS));
-      hdr->n_fwd = hdr->n_dq = hdr->n_dkv = hdr->n_fused = 0;
+      hdr->n_fwd = hdr->n_dq = hdr->n_dkv = hdr->n_fused = hdr->n_nsp = 0;
       hdr->total_qpad = 0;  // the preprocess walks no rows
     }
     return;
@@ -304,9 +315,11 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
               base);
   } else if (blockIdx.x == 1) {
     emit_list(p, kListDq, reinterpret_cast<WorkItem*>(p.ws + p.L.dq), p.L.cap_dq, &hdr->n_dq, hist, base);
-  } else {
+  } else if (blockIdx.x == 2) {
     emit_list(p, kListFused, reinterpret_cast<WorkItem*>(p.ws + p.L.fused), p.L.cap_fused, &hdr->n_fused, hist,
               base);
+  } else {
+    emit_list(p, kListNsp, reinterpret_cast<WorkItem*>(p.ws + p.L.nsp), p.L.cap_nsp, &hdr->n_nsp, hist, base);
   }
 }
 
@@ -343,6 +356,7 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   p.causal = pr.causal;
   p.backward = backward ? 1 : 0;
   p.grid = num_sms;
+  p.nsp_max_tiles = pr.nsp_max_tiles;
   p.ws = static_cast<uint8_t*>(ws);
   p.L = L;
   p.bias = pr.bias_table;
@@ -353,7 +367,7 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   // one CTA per list; helpers for the maps (one thread each), tail copies and bias table
   const long long map_ctas = (static_cast<long long>(pr.B) * kNumMapSlots + 1023) / 1024;
   const int helpers = int(map_ctas < 1 ? 1 : (map_ctas > 32 ? 32 : map_ctas)) + 4;
-  return launch_pdl(plan_kernel, dim3((backward ? 3 : 1) + helpers), dim3(1024), 0, stream, maps, p);
+  return launch_pdl(plan_kernel, dim3((backward ? 4 : 1) + helpers), dim3(1024), 0, stream, maps, p);
 }
 
 }  // namespace jfa

@@ -23,8 +23,9 @@ STATUS_NAMES = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
 # Every symbol include/jfa.h declares.
 EXPORTED_SYMBOLS = ("jfa_workspace_size", "jfa_forward", "jfa_forward_noalloc", "jfa_backward", "jfa_check_status",
                     "jfa_status_string", "jfa_last_launch_count", "jfa_last_error", "jfa_timing_enable",
-                    "jfa_timing_read", "jfa_trace_configure", "jfa_selftest_wait_timeout", "jfa_wait_limit_ns")
-KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq", "bwd_fused")
+                    "jfa_timing_read", "jfa_trace_configure", "jfa_selftest_wait_timeout", "jfa_wait_limit_ns",
+                    "jfa_set_nsp_max_tiles")
+KERNEL_KINDS = ("plan", "forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq", "bwd_fused", "bwd_nsp")
 
 
 class JfaError(RuntimeError):
@@ -89,6 +90,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.jfa_timing_read.restype = i32
     lib.jfa_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     lib.jfa_selftest_wait_timeout.restype = i32
+    lib.jfa_set_nsp_max_tiles.argtypes = [i32]
+    lib.jfa_set_nsp_max_tiles.restype = i32
     lib.jfa_wait_limit_ns.argtypes = [i64, i32, i64]
     lib.jfa_wait_limit_ns.restype = ctypes.c_uint64
     lib.jfa_trace_configure.argtypes = [vp, sz, i32]
@@ -295,6 +298,19 @@ def jfa_backward(dout, q, k, v, out, lse, q_offsets, kv_offsets, bias=None, bias
 def jfa_check_status(workspace, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status of the last call."""
     return int(load_library().jfa_check_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+def jfa_set_nsp_max_tiles(max_tiles: int) -> int:
+    """Sequences of 2 .. max_tiles query tiles take the non-sequence-parallel backward pass
+    (0 or 1: none, the default); returns the previous setting.  Process-wide."""
+    prev = int(load_library().jfa_set_nsp_max_tiles(int(max_tiles)))
+    if prev < 0:
+        raise ValueError(f"max_tiles must be in 0 .. 16, got {max_tiles}")
+    return prev
+
+
+def jfa_nsp_max_tiles() -> int:
+    return int(load_library().jfa_set_nsp_max_tiles(-1))
 
 
 def jfa_last_launch_count() -> int:

@@ -142,3 +142,15 @@ def test_wait_limit_scales_with_planned_work():
     assert f(10**6, 152, 10) < f(2 * 10**6, 152, 10) and f(10**6, 152, 10) < f(10**6, 152, 11)
     assert f(10**6, 76, 10) > f(10**6, 152, 10)
     assert f(2**62, 1, 2**62) == floor + 3600 * 10**9
+
+
+def test_nsp_setting_round_trips_and_rejects_out_of_range():
+    lib = jfa.load_library()
+    prev = lib.jfa_set_nsp_max_tiles(-1)
+    assert 0 <= prev <= 16
+    try:
+        assert lib.jfa_set_nsp_max_tiles(8) == prev
+        assert lib.jfa_set_nsp_max_tiles(-1) == 8
+        assert lib.jfa_set_nsp_max_tiles(17) == -1 and lib.jfa_set_nsp_max_tiles(-1) == 8
+    finally:
+        lib.jfa_set_nsp_max_tiles(prev)

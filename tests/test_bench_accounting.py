@@ -48,13 +48,17 @@ def test_flops_split_adds_up():
     from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, make_batch
     for name in ("tiny", "biased_causal"):
         batch = make_batch(CONFIGS[name], device="cpu")
-        f = b.workload_flops(batch)
+        f = b.workload_flops(batch, nsp_rows=1024)
         dH = batch.cfg.head_dim * batch.cfg.heads
         assert f["fwd"] == 4.0 * dH * f["pairs"]
         assert f["bwd"] == 10.0 * dH * f["pairs"]
-        # the split passes and the fused pass cover every visited pair once
-        assert f["dkdv"] / 8 + f["fused"] / 10 == pytest.approx(f["pairs"] * dH)
+        # the split passes, the fused pass and the non-sequence-parallel pass cover every
+        # visited pair once
+        assert f["dkdv"] / 8 + f["fused"] / 10 + f["nsp"] / 10 == pytest.approx(f["pairs"] * dH)
         assert f["dq"] * 4 == pytest.approx(f["dkdv"])
+        lq = np.asarray(batch.q_lengths)
+        assert (f["nsp"] > 0) == bool(((lq > 128) & (lq <= 1024)).any())
+        assert (f["dkdv"] > 0) == bool((lq > 1024).any())
 
 
 def test_general_bias_bytes_counted_once_per_pass():
@@ -63,15 +67,17 @@ def test_general_bias_bytes_counted_once_per_pass():
     from jagged_attention_recsys_jfa_gb300.inputs import CONFIGS, make_batch
     plain = make_batch(dataclasses.replace(CONFIGS["jagged_bias_causal"], batch=6, general_bias=False), device="cpu")
     jb = make_batch(dataclasses.replace(CONFIGS["jagged_bias_causal"], batch=6), device="cpu")
-    w0, w1 = b.workload_bytes(plain), b.workload_bytes(jb)
+    w0, w1 = b.workload_bytes(plain, nsp_rows=1024), b.workload_bytes(jb, nsp_rows=1024)
     H = jb.cfg.heads
     lq, lk = jb.q_lengths.numpy(), jb.kv_lengths.numpy()
     # the visited pairs' elements only (causal: the lower triangle; never the row padding)
     blocks = np.array([2.0 * H * _brute_pairs([a], [c], True) for a, c in zip(lq, lk)])
     assert blocks.sum() < 2.0 * H * (lq * ((lk + 7) // 8 * 8)).sum() * 0.6
-    long_ = lq > 128
+    long_ = lq > 1024
+    nsp = (lq > 128) & ~long_
     assert w1["forward"] - w0["forward"] == pytest.approx(blocks.sum())
     assert w1["bwd_dkdv"] - w0["bwd_dkdv"] == pytest.approx(blocks[long_].sum())
     assert w1["bwd_dq"] - w0["bwd_dq"] == pytest.approx(blocks[long_].sum())
-    assert w1["bwd_fused"] - w0["bwd_fused"] == pytest.approx(blocks[~long_].sum())
+    assert w1["bwd_nsp"] - w0["bwd_nsp"] == pytest.approx(blocks[nsp].sum())
+    assert w1["bwd_fused"] - w0["bwd_fused"] == pytest.approx(blocks[lq <= 128].sum())
     assert jb.jbias.numel() == (lq * ((lk + 7) // 8 * 8)).sum() * H

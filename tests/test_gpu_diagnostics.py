@@ -30,19 +30,23 @@ def test_bounded_wait_times_out_and_reports():
     compare_out_lse(res["out"], res["lse"], ref["out"], ref["lse"], "after timeout")
 
 
-@pytest.mark.parametrize("kind", ["forward", "bwd_dkdv", "bwd_dq", "bwd_fused"])
+@pytest.mark.parametrize("kind", ["forward", "bwd_dkdv", "bwd_dq", "bwd_fused", "bwd_nsp"])
 def test_trace_records_ordered_events(kind):
-    # sequences with several query tiles (split backward passes) and with one (fused).  The
-    # first CTA records; CTAs claim items as they free up and each claims its first two at
-    # once, so every list holds more than two items per SM to be sure the first CTA works
-    lq = [300, 40] * 200
-    batch = make_batch(CONFIGS["tiny"], device="cuda", q_lengths=lq, kv_lengths=[300, 260] * 200)
+    # sequences of more than 8 query tiles (split backward passes), of 3 (non-sequence-
+    # parallel pass) and of one (fused).  The first CTA records; CTAs claim items as they free
+    # up and each claims its first two at once, so every list holds more than two items per
+    # SM to be sure the first CTA works
+    lq = [1100, 300, 40] * 160
+    batch = make_batch(CONFIGS["tiny"], device="cuda", q_lengths=lq, kv_lengths=[1100, 300, 260] * 160)
     buf = torch.zeros(5 * 1024, dtype=torch.int64, device="cuda")
+    from jagged_attention_recsys_jfa_gb300 import jfa_set_nsp_max_tiles
+    prev = jfa_set_nsp_max_tiles(8 if kind == "bwd_nsp" else 0)  # the 3-tile sequences take that pass
     jfa_trace_configure(buf, kind)
     try:
         gpu_run(batch)
     finally:
         jfa_trace_configure(None)
+        jfa_set_nsp_max_tiles(prev)
     roles = decode_trace(buf)
     assert len(roles[1]) > 0, "MMA issuer recorded nothing"
     for r, events in enumerate(roles):
