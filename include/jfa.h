@@ -190,7 +190,10 @@ jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_s
  * split passes (dK/dV per key tile, then dQ per query tile: seven GEMMs per tile pair, no
  * sum buffer).  max_tiles in 0 .. 16; below 2 every such sequence takes the split passes
  * (the default, which measured faster on GB300).  Both paths give the same results within
- * rounding and are each deterministic.  A negative max_tiles only reads the setting.
+ * rounding and are each deterministic.  With max_tiles >= 2 the backward workspace also
+ * holds the fp32 dQ sums (4 * total_q * H * d more bytes): jfa_workspace_size reflects the
+ * setting at the time it is called, and a workspace sized before the pass was enabled is
+ * rejected with JFA_ERR_WORKSPACE.  A negative max_tiles only reads the setting.
  * Returns the previous setting, or -1 (nothing changed) for max_tiles > 16. */
 int jfa_set_nsp_max_tiles(int max_tiles);
 

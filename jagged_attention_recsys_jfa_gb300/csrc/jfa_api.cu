@@ -18,6 +18,7 @@ namespace {
 thread_local int g_last_launches = 0;
 // query tiles up to which a sequence's backward takes the non-sequence-parallel pass
 std::atomic<int> g_nsp_max_tiles{kNspDefaultMaxTiles};
+bool nsp_enabled() { return g_nsp_max_tiles.load(std::memory_order_relaxed) >= 2; }
 thread_local char g_last_error[256] = "";
 }  // namespace
 
@@ -190,7 +191,7 @@ extern "C" {
 
 size_t jfa_workspace_size(int B, int H, int d, int64_t total_q, int64_t total_kv, int is_backward) {
   if (B < 1 || H < 1 || (d != 64 && d != 128) || total_q < 0 || total_kv < 0) return 0;
-  return make_layout(B, H, d, total_q, total_kv, is_backward != 0).total;
+  return make_layout(B, H, d, total_q, total_kv, is_backward != 0, nsp_enabled()).total;
 }
 
 jfa_status jfa_forward(const void* q, const void* k, const void* v, const int64_t* q_offsets,
@@ -252,7 +253,7 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
   if (total_kv > 0 && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
                        !aligned16(dv)))
     return JFA_ERR_INVALID_ARG;
-  const WsLayout L = make_layout(B, H, d, total_q, total_kv, true);
+  const WsLayout L = make_layout(B, H, d, total_q, total_kv, true, nsp_enabled());
   if ((st = check_workspace(workspace, workspace_bytes, L)) != JFA_OK) return st;
   const Problem pr = make_problem(B, H, d, total_q, total_kv, q_offsets, kv_offsets, bias, scale, causal);
   const int nsm = sm_count();

@@ -162,8 +162,10 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 
 // Capacities are upper bounds on the item counts for any offsets with these totals:
 //   sum_b ceil(ceil(L_b/128)/2) <= total/256 + B,  sum_b ceil(L_b/128) <= total/128 + B.
+// `nsp`: the backward may route sequences to the non-sequence-parallel pass, which needs its
+// fp32 dQ sum buffer (4 * total_q * H * d bytes); without it the buffer is left out.
 __host__ __device__ inline WsLayout make_layout(int B, int H, int d, int64_t total_q, int64_t total_kv,
-                                                bool backward) {
+                                                bool backward, bool nsp = false) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
   L.maps = align_up(off, 128);
@@ -190,7 +192,7 @@ __host__ __device__ inline WsLayout make_layout(int B, int H, int d, int64_t tot
     L.nsp = align_up(off, 16);
     off = L.nsp + size_t(L.cap_nsp) * sizeof(WorkItem);
     L.dqacc = align_up(off, 256);
-    off = L.dqacc + size_t(total_q) * size_t(H) * size_t(d) * sizeof(float);
+    off = L.dqacc + (nsp ? size_t(total_q) * size_t(H) * size_t(d) * sizeof(float) : 0);
     L.qpad = align_up(off, 256);
     off = L.qpad + size_t(B + 1) * sizeof(int64_t);
     L.qpad_cap = int64_t(align_up(size_t(total_q) + size_t(kBM) * B, kBM));  // rows per head, 512-B aligned
