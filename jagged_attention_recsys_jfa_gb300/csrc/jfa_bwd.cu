@@ -762,6 +762,19 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
             if (nq0 + 32 + lane < Lq) prefetch_l2(nb + int64_t(32 + lane) * pitch);
           }
         }
+        // relative-position bias * log2(e) of this tile (bucket of column c: idx0 - c), loaded
+        // before the waits so the loads overlap the MMAs
+        float bw[kBias ? 64 : 1];
+        if (kBias) {
+          const int idx0 = j - (qt * kBM + 64 * w) + p.center;
+          if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + idx0 - c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1));
+          }
+        }
         // Q_i's ring slot carries this tile's lse2 / D vectors: wait for it
         const uint32_t nq = ring_n + 1;
         if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
@@ -784,21 +797,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
           for (int c2 = 0; c2 < 32; ++c2)
             f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
         } else if (kBias) {
-          const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
-          if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias, two columns per op
-              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
-                               f2_pack(__ldg(brow + idx0 - 2 * c2), __ldg(brow + idx0 - 2 * c2 - 1))),
-                        x[2 * c2], x[2 * c2 + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
-          }
-#pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2)
-            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
+          for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias - lse2, two columns per op
+            f2_unpack(f2_add(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, f2_pack(bw[2 * c2], bw[2 * c2 + 1])),
+                             nlse2[c2]),
+                      x[2 * c2], x[2 * c2 + 1]);
         } else {
           const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
@@ -1220,6 +1224,19 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
             prefetch_l2(brow_i + jj0 + kBN + 56);
           }
         }
+        // relative-position bias * log2(e) of this tile (bucket of column c: idx0 + c), loaded
+        // before the wait so the loads overlap the MMAs
+        float bw[kBias ? 64 : 1];
+        if (kBias) {
+          const int idx0 = jt * kBN + 64 * w - i + p.center;
+          if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + idx0 + c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + min(max(idx0 + c, 0), p.num_buckets - 1));
+          }
+        }
         if (!mbar_wait(&s_full, tile_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + w, tn, 20);
@@ -1236,21 +1253,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
           for (int c2 = 0; c2 < 32; ++c2)
             f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_nl2), x[2 * c2], x[2 * c2 + 1]);
         } else if (kBias) {
-          const int idx0 = j0 - i + p.center;
-          if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias, two columns per op
-              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
-                               f2_pack(__ldg(brow + idx0 + 2 * c2), __ldg(brow + idx0 + 2 * c2 + 1))),
-                        x[2 * c2], x[2 * c2 + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 + c, 0), p.num_buckets - 1)));
-          }
-#pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2)
-            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_nl2), x[2 * c2], x[2 * c2 + 1]);
+          for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias - lse2, two columns per op
+            f2_unpack(f2_add(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, f2_pack(bw[2 * c2], bw[2 * c2 + 1])),
+                             k_nl2),
+                      x[2 * c2], x[2 * c2 + 1]);
         } else {
           const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
@@ -1627,6 +1635,14 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
         jbias_load_cols_vec(jbw, p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(64 * w) * pitch + kj0, pitch,
                             Lq - 64 * w, Lk - kj0, lane);
       }
+      // relative-position bias * log2(e) (bucket of column c: j - 64 w + center - c), loaded
+      // before the wait so the loads overlap the MMAs
+      float bw[kBias ? 64 : 1];
+      if (kBias) {
+        const int idx0 = j - 64 * w + p.center;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1));
+      }
       // ---- P^T = exp2(S^T * scale * log2e (+ bias) - lse2), 0 on padding and hidden pairs
       if (!mbar_wait(&st_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
       tc_fence_after();
@@ -1642,13 +1658,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
         for (int c2 = 0; c2 < 32; ++c2)
           f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2v[c2]), x[2 * c2], x[2 * c2 + 1]);
       } else if (kBias) {
-        const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
+        const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
-#pragma unroll
-        for (int c2 = 0; c2 < 32; ++c2)
-          f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2v[c2]), x[2 * c2], x[2 * c2 + 1]);
+        for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias - lse2, two columns per op
+          f2_unpack(f2_add(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, f2_pack(bw[2 * c2], bw[2 * c2 + 1])),
+                           nlse2v[c2]),
+                    x[2 * c2], x[2 * c2 + 1]);
       } else {
         const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
@@ -1799,31 +1814,6 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
-}
-
-// The 32 rows of a warp (one per lane) x 8 chunks of 16 bytes, transposed within groups of 8
-// lanes with xor-shuffles: afterwards lane base + i (base = lane & ~7) holds chunk i of rows
-// base .. base + 7 (c[k] = row base + k), so one instruction of the group covers 128
-// consecutive bytes of a row and one of the warp four whole rows' segments.
-__device__ __forceinline__ void xpose_rows8(uint4 (&c)[8]) {
-  const int i = threadIdx.x & 7;
-#pragma unroll
-  for (int s = 1; s < 8; s <<= 1) {
-    const bool hi = (i & s) != 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if ((k & s) == 0) {
-        const uint4 send = hi ? c[k] : c[k | s];
-        uint4 got;
-        got.x = __shfl_xor_sync(0xffffffffu, send.x, s);
-        got.y = __shfl_xor_sync(0xffffffffu, send.y, s);
-        got.z = __shfl_xor_sync(0xffffffffu, send.z, s);
-        got.w = __shfl_xor_sync(0xffffffffu, send.w, s);
-        if (hi) c[k] = got;
-        else c[k | s] = got;
-      }
-    }
-  }
 }
 
 // ================================================================== non-sequence-parallel pass
@@ -2149,6 +2139,19 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) nsp_kernel(const BwdParams p)
           jbias_load_cols_vec(jbw, p.jbias + size_t(it.h) * p.jb_plane + it.jb + int64_t(qi0) * pitch + kj0, pitch,
                               Lq - qi0, Lk - kj0, lane);
         }
+        // relative-position bias * log2(e) of this tile (bucket of column c: idx0 - c), loaded
+        // before the waits so the loads overlap the MMAs
+        float bw[kBias ? 64 : 1];
+        if (kBias) {
+          const int idx0 = j - (qt * kBM + 64 * w) + p.center;
+          if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + idx0 - c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) bw[c] = __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1));
+          }
+        }
         // Q_i's ring slot (the first of the pair) carries this tile's lse2 / D vectors
         const uint32_t nq = ring_n;
         if (!mbar_wait(&ring_full[nq % R], (nq / R) & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
@@ -2171,21 +2174,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) nsp_kernel(const BwdParams p)
           for (int c2 = 0; c2 < 32; ++c2)
             f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
         } else if (kBias) {
-          const int idx0 = j - i0 + p.center;  // bucket of column c is idx0 - c
-          if (idx0 - 63 >= 0 && idx0 < p.num_buckets) {
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2)
-              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
-                               f2_pack(__ldg(brow + idx0 - 2 * c2), __ldg(brow + idx0 - 2 * c2 - 1))),
-                        x[2 * c2], x[2 * c2 + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              x[c] = fmaf(x[c], sl2, __ldg(brow + min(max(idx0 - c, 0), p.num_buckets - 1)));
-          }
-#pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2)
-            f2_unpack(f2_add(f2_pack(x[2 * c2], x[2 * c2 + 1]), nlse2[c2]), x[2 * c2], x[2 * c2 + 1]);
+          for (int c2 = 0; c2 < 32; ++c2)  // packed: x*scale + bias - lse2, two columns per op
+            f2_unpack(f2_add(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), k_sl2, f2_pack(bw[2 * c2], bw[2 * c2 + 1])),
+                             nlse2[c2]),
+                      x[2 * c2], x[2 * c2 + 1]);
         } else {
           const uint64_t k_sl2 = f2_pack(sl2, sl2);
 #pragma unroll
@@ -2311,43 +2305,30 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) nsp_kernel(const BwdParams p)
         ++g;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceLoader, tn, 30);
-        // rows of this warp are 32 tokens apart in memory: transpose 32 columns at a time so
-        // each store / addition instruction writes four rows' 128-byte segments
-        const int base = lane & ~7, sub = lane & 7;
-        const unsigned long long my_acc = qvalid ? reinterpret_cast<unsigned long long>(acc) : 0ull;
-        const unsigned long long my_dq = qvalid ? reinterpret_cast<unsigned long long>(dq_row) : 0ull;
+        // one thread per row: each chunk of 32 columns leaves as eight 16-byte operations
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
-          uint4 c[8];
-          {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_addr + C::kColNspDq + c0, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 8; ++q) c[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-          }
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_addr + C::kColNspDq + c0, r);
+          tmem_ld_wait();
           if (c0 + 32 == D) {  // the whole row is in registers: the MMA may reuse the columns
             tc_fence_before();
             mbar_arrive(&dq_empty);
             if (leader) trace_event(p.trace, kTraceLoader, tn, 31);
           }
-          xpose_rows8(c);
+          if (!qvalid) continue;  // a padding query row
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const unsigned long long ra = __shfl_sync(0xffffffffu, my_acc, base + k);
-            const unsigned long long rq = __shfl_sync(0xffffffffu, my_dq, base + k);
-            if (ra == 0ull) continue;  // a padding query row
-            float* a4 = reinterpret_cast<float*>(ra) + c0 + 4 * sub;
-            float v0 = __uint_as_float(c[k].x), v1 = __uint_as_float(c[k].y), v2 = __uint_as_float(c[k].z),
-                  v3 = __uint_as_float(c[k].w);
+            float* a4 = acc + c0 + 4 * k;
+            float v0 = __uint_as_float(r[4 * k]), v1 = __uint_as_float(r[4 * k + 1]),
+                  v2 = __uint_as_float(r[4 * k + 2]), v3 = __uint_as_float(r[4 * k + 3]);
             if (kt == jl) {  // the last contribution: finish the row segment in bf16
               if (kt > 0) {  // add the sum of the earlier key tiles
                 const float4 a = ld_global_cg_v4f(a4);
                 v0 += a.x, v1 += a.y, v2 += a.z, v3 += a.w;
               }
-              __nv_bfloat16* q4 = reinterpret_cast<__nv_bfloat16*>(rq) + c0 + 4 * sub;
-              *reinterpret_cast<uint2*>(q4) = make_uint2(pack_bf16x2(v0 * p.scale, v1 * p.scale),
-                                                         pack_bf16x2(v2 * p.scale, v3 * p.scale));
+              *reinterpret_cast<uint2*>(dq_row + c0 + 4 * k) =
+                  make_uint2(pack_bf16x2(v0 * p.scale, v1 * p.scale), pack_bf16x2(v2 * p.scale, v3 * p.scale));
             } else if (kt == 0) {  // the first contribution: store
               st_global_v4f(a4, v0, v1, v2, v3);
             } else {  // in between: add (this row has one owner, so the order is the key tiles')

@@ -430,12 +430,46 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             prefetch_l2(brow_j + kvj + kBN + 64);
           }
         }
+        const int kv0 = j * kBN;
+        const bool last = (j == nkv - 1);
+        // relative-position bias * log2(e) of this tile's columns, loaded before the wait so the
+        // loads overlap the MMAs (0 on padded key columns, which then score exactly 0)
+        float bw[kBias ? 128 : 1];
+        if (kBias) {
+          const int n_real = min(kBN, it.Lk - kv0);
+          const int idx0 = kv0 - i + p.center;  // bucket of column c: idx0 + c
+          if (idx0 >= 0 && idx0 + kBN - 1 < p.num_buckets && n_real == kBN) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) bw[c] = __ldg(brow + idx0 + c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              bw[c] = c < n_real ? __ldg(brow + min(max(idx0 + c, 0), p.num_buckets - 1)) : 0.f;
+          }
+        }
         if (!mbar_wait(&s_full[s], s_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
         ++s_n;
         tc_fence_after();
         if (leader) trace_event(p.trace, kTraceCompute0 + s, tn, 20);
         float x[128];
-        {
+        if (kBias) {
+          // x = scale*log2e * (q.k) + bias*log2e, 32 columns at a time (the bias registers
+          // become the scores', so at most 32 more are live)
+          const uint64_t k_sl2 = f2_pack(sl2, sl2);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t r[32];
+            tmem_ld32(tS + 32 * q, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c2 = 0; c2 < 16; ++c2) {
+              const int c = 32 * q + 2 * c2;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * c2]), __uint_as_float(r[2 * c2 + 1])), k_sl2,
+                               f2_pack(bw[c], bw[c + 1])),
+                        x[c], x[c + 1]);
+            }
+          }
+        } else {
           // all four loads in flight before a single wait
           uint32_t r0[32], r1[32], r2[32], r3[32];
           tmem_ld32(tS + 0, r0);
@@ -451,29 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             x[96 + c] = __uint_as_float(r3[c]);
           }
         }
-        const int kv0 = j * kBN;
-        const bool last = (j == nkv - 1);
         if (kJBias) {
           // x = scale*log2e * (q.k) + bias*log2e from this row of the sequence's block
           jbias_apply<128>(x, jbk, sl2, kLog2e);
-        }
-        if (kBias) {
-          // x = scale*log2e * (q.k) + bias*log2e, bias only on real key columns
-          const int n_real = min(kBN, it.Lk - kv0);
-          const int idx0 = kv0 - i + p.center;
-          if (idx0 >= 0 && idx0 + kBN - 1 < p.num_buckets && n_real == kBN) {
-#pragma unroll
-            for (int c2 = 0; c2 < 64; ++c2)  // packed: x*scale + bias, two columns per op
-              f2_unpack(f2_fma(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_pack(sl2, sl2),
-                               f2_pack(__ldg(brow + idx0 + 2 * c2), __ldg(brow + idx0 + 2 * c2 + 1))),
-                        x[2 * c2], x[2 * c2 + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              const int bi = min(max(idx0 + c, 0), p.num_buckets - 1);
-              x[c] = c < n_real ? fmaf(x[c], sl2, __ldg(brow + bi)) : x[c] * sl2;
-            }
-          }
         }
         if (p.causal) {
           const int lim = i + diag - kv0;  // last visible column of this row in this tile
