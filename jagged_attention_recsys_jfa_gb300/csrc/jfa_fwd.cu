@@ -288,50 +288,60 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp walks the schedule (its state stays warp-uniform); one elected lane
+    // issues the tcgen05 instructions
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, false, true);
       const uint32_t colS[2] = {C::kColS0, C::kColS1};
       const uint32_t colO[2] = {C::kColO0, C::kColO1};
       const uint32_t sQ_addr = smem_u32(sQ), sR_addr = smem_u32(sRing);
+      auto mma_commit = [&](uint64_t* bar) {
+        if (elect_one()) umma_commit(bar);
+      };
       uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0}, tn = 0;
       bool ok = true;
       uint32_t k = 0;
       for (; ok; ++k) {
-       if (!meta_wait(meta, k, abort_flag)) { ok = false; break; }
+       if (!meta_wait_warp(meta, k, abort_flag)) { ok = false; break; }
        const ItemMeta& wi = meta.e[k % kMetaSlots];  // read in place, freed after the item
        if (wi.b < 0) break;  // end of this CTA's items
        for (int u = wi.u0; u < wi.u1 && ok; ++u) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const int nkv[2] = {it.nkv0, it.nkv1};
-        if (!mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs))) { ok = false; break; }
         ++item_n;
         tc_fence_after();
-        trace_event(p.trace, kTraceMma, tn, 10);
+        if (lane == 0) trace_event(p.trace, kTraceMma, tn, 10);
         int s_left = it.nkv0 + it.nkv1;
         auto issue_S = [&](int s, uint32_t e) {
           // descriptor start addresses are in 16-byte units in the low bits: step by adding
           const uint64_t qd = sdesc_sw128(sQ_addr + s * C::kTileBytes, 16, 1024);
           const uint64_t kd = sdesc_sw128(sR_addr + e * C::kTileBytes, 16, 1024);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            umma_ss(tmem + colS[s], qd + o, kd + o, kIdS, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              umma_ss(tmem + colS[s], qd + o, kd + o, kIdS, kk > 0);
+            }
           }
-          umma_commit(&s_full[s]);
-          trace_event(p.trace, kTraceMma, tn, 16 + s);
-          if (--s_left == 0) umma_commit(&q_empty);
+          mma_commit(&s_full[s]);
+          if (lane == 0) trace_event(p.trace, kTraceMma, tn, 16 + s);
+          if (--s_left == 0) mma_commit(&q_empty);
         };
         auto issue_PV = [&](int s, uint32_t e, bool acc) {
           const uint64_t vd = sdesc_sw128(sR_addr + e * C::kTileBytes, 16384, 1024);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, vd + uint32_t(kk * 2048 >> 4), kIdPV,
-                    (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, vd + uint32_t(kk * 2048 >> 4), kIdPV,
+                      (acc || kk > 0) ? 1u : 0u);
+          }
         };
         auto wait_full = [&](uint32_t n) -> bool {
-          const bool r = mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, kWaitTimeoutNs);
+          const bool r =
+              __all_sync(0xffffffffu, mbar_wait(&kv_full[n % C::kStages], (n / C::kStages) & 1, abort_flag, kWaitTimeoutNs));
           tc_fence_after();
           return r;
         };
@@ -339,20 +349,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         if (!wait_full(n0)) { ok = false; break; }
         if (it.nkv0 > 0) issue_S(0, n0 % C::kStages);
         if (it.nkv1 > 0) issue_S(1, n0 % C::kStages);
-        umma_commit(&kv_empty[n0 % C::kStages]);
+        mma_commit(&kv_empty[n0 % C::kStages]);
         for (int j = 0; j < it.njt && ok; ++j) {
           const uint32_t nv = n0 + 2 * j + 1, nk = n0 + 2 * j + 2;
           if (!wait_full(nv)) { ok = false; break; }
           bool k_ready = false;
           for (int s = 0; s < 2 && ok; ++s) {
             if (j < nkv[s]) {
-              if (!mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+              if (!__all_sync(0xffffffffu, mbar_wait(&p_full[s], p_n[s] & 1, abort_flag, kWaitTimeoutNs))) {
+                ok = false;
+                break;
+              }
               ++p_n[s];
               tc_fence_after();
-              trace_event(p.trace, kTraceMma, tn, 12 + s);
+              if (lane == 0) trace_event(p.trace, kTraceMma, tn, 12 + s);
               issue_PV(s, nv % C::kStages, j > 0);
-              trace_event(p.trace, kTraceMma, tn, 14 + s);
-              if (j == nkv[s] - 1) umma_commit(&o_full[s]);
+              if (lane == 0) trace_event(p.trace, kTraceMma, tn, 14 + s);
+              if (j == nkv[s] - 1) mma_commit(&o_full[s]);
             }
             if (j + 1 < nkv[s]) {
               if (!k_ready) {
@@ -363,15 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
             }
           }
           if (!ok) break;
-          umma_commit(&kv_empty[nv % C::kStages]);
-          if (j + 1 < it.njt) umma_commit(&kv_empty[nk % C::kStages]);
+          mma_commit(&kv_empty[nv % C::kStages]);
+          if (j + 1 < it.njt) mma_commit(&kv_empty[nk % C::kStages]);
         }
         ring_n = n0 + 2 * it.njt;
        }
-       if (ok) meta_release(meta, k);
+       if (ok) meta_release_warp(meta, k);
       }
-      if (!ok) raise_status(p.status, JFA_ERR_TIMEOUT);
-      umma_commit(&mma_done);
+      if (!ok && lane == 0) raise_status(p.status, JFA_ERR_TIMEOUT);
+      mma_commit(&mma_done);
       drain_wait(&mma_done, 0);
     }
   } else if (warp == 3) {
