@@ -943,6 +943,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ MetaRing meta;
+  __shared__ float rb_scr[kBias && D == 64 ? 8 * 96 : 1];  // relative-position bias windows (d = 64)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -1212,6 +1213,13 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       const uint64_t k_nd = f2_pack(nd, nd);
       const int diag = Lk - Lq;
       const float* brow = kBias ? p.bias2 + size_t(it.h) * p.num_buckets : nullptr;
+      // relative-position bias at d = 64: this warp's window of the table for key tile jt (the
+      // bucket of (lane, column c) is lo0 + jt * 128 + 31 + c - lane), fetched into registers a
+      // tile ahead and staged in the warp's scratch when its tile comes up
+      float* scr = kBias && D == 64 ? rb_scr + (warp - kFirstComputeWarp) * 96 : nullptr;
+      const int lo0 = 64 * w - (i - lane) + p.center - 31;
+      float rbv[3];  // dead unless kBias at d = 64
+      if (kBias && D == 64) relbias_fetch<3>(rbv, brow, lo0, 64 + 31, p.num_buckets, lane);
       for (int jt = 0; jt < nkv && ok; ++jt) {
         uint32_t jbk[kJBias ? 32 : 1];  // general bias for this tile, loaded before the wait
         if (kJBias) {
@@ -1227,7 +1235,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
         // relative-position bias * log2(e) of this tile (bucket of column c: idx0 + c), loaded
         // before the wait so the loads overlap the MMAs
         float bw[kBias ? 64 : 1];
-        if (kBias) {
+        if (kBias && D == 64) {
+          relbias_store<3>(scr, rbv, 64 + 31, lane);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) bw[c] = scr[c + 31 - lane];
+          if (jt + 1 < nkv) relbias_fetch<3>(rbv, brow, lo0 + (jt + 1) * kBN, 64 + 31, p.num_buckets, lane);
+        } else if (kBias) {  // d = 128: no shared memory to spare, gathered from global memory
           const int idx0 = jt * kBN + 64 * w - i + p.center;
           if (idx0 >= 0 && idx0 + 63 < p.num_buckets) {
 #pragma unroll

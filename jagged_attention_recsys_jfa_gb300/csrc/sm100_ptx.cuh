@@ -415,6 +415,38 @@ __device__ __forceinline__ void st_rows_coalesced(uint4 (&c)[NB / 16], void* dst
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// Relative-position bias windows.  The bucket of (query i, key j) is j - i + center, so the
+// 32 rows of a warp and n consecutive columns of a tile need only n + 31 consecutive table
+// entries.  The warp stages them in a per-warp shared scratch with coalesced loads; each lane
+// then reads its n values from there.  For a fixed column the lanes read consecutive words,
+// so every read is one conflict-free wavefront, where the same gather straight from global
+// memory touches two cache lines per instruction.  That pays where the gather bounds the
+// pass (the dQ pass at d = 64, whose three GEMMs per tile pair are short); the forward and
+// the key-row passes measured faster gathering straight from global memory.
+// The window is fetched into registers a tile ahead (relbias_fetch: v = table[clamp(lo + k,
+// 0, nb - 1)] for k = lane + 32 r < len, len <= 32 * kRounds, lo the same in every lane) and
+// written to the scratch when its tile comes up (relbias_store), so the global loads' latency
+// overlaps a whole tile's work.
+template <int kRounds>
+__device__ __forceinline__ void relbias_fetch(float (&v)[kRounds], const float* table, int lo, int len, int nb,
+                                              int lane) {
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int k = lane + 32 * r;
+    v[r] = k < len ? __ldg(table + min(max(lo + k, 0), nb - 1)) : 0.f;
+  }
+}
+template <int kRounds>
+__device__ __forceinline__ void relbias_store(float* scr, const float (&v)[kRounds], int len, int lane) {
+  __syncwarp();  // every lane has read the previous window
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int k = lane + 32 * r;
+    if (k < len) scr[k] = v[r];
+  }
+  __syncwarp();
+}
+
 // General jagged bias, split into loads and arithmetic so the loads can be issued before
 // the wait for the scores they apply to.  Values are kept as packed bf16 pairs (0 where no
 // bias applies).
