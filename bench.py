@@ -263,7 +263,8 @@ def cpu_cores():
 # ----------------------------------------------------------------------------- padded SDPA
 def padded_sdpa(batch, steps):
     """Dense SDPA on the batch padded to its longest sequence (the padding-waste
-    comparison): time per fwd+bwd step and peak memory."""
+    comparison): time per fwd+bwd step after three warm-up steps (a process's first call
+    of a backend ran several times slower) and peak memory."""
     from torch.nn.attention import SDPBackend, sdpa_kernel
 
     cfg = batch.cfg
@@ -314,7 +315,8 @@ def padded_sdpa(batch, steps):
                     o = torch.nn.functional.scaled_dot_product_attention(
                         qq, kk, vv, attn_mask=mask, is_causal=cfg.causal and mask is None, scale=cfg.scale)
                 o.backward(do)
-            step()
+            for _ in range(3):  # a process's first calls load and set up the backend's kernels
+                step()
             torch.cuda.synchronize()
             torch.cuda.reset_peak_memory_stats()
             base = torch.cuda.memory_allocated()
