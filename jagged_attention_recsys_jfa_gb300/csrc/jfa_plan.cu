@@ -20,6 +20,7 @@ struct PlanParams {
   int causal, backward;
   int grid;  // persistent CTAs of the kernels that consume the lists
   int nsp_max_tiles;  // query tiles up to which a sequence takes the non-sequence-parallel pass
+  int d;              // head dimension
   uint8_t* ws;
   WsLayout L;
   const float* bias;  // [H][nb] or nullptr
@@ -143,17 +144,36 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
   const long long share = (total_cost * p.H + (long long)kItemsPerCta * p.grid - 1) /
                           ((long long)kItemsPerCta * p.grid);
   // the fused and non-sequence-parallel passes own each sequence's dQ: their items are
-  // never cut into ranges
-  const long long range_cap = (kind == kListFused || kind == kListNsp) ? (1ll << 62) : (share > 1 ? share : 1);
+  // never cut into ranges.  At d = 128 the dK/dV and dQ passes take one tile per item, and
+  // a (sequence, head)'s items sit next to each other in the list (ordered by the group's
+  // total cost, longest first): neighbouring CTAs claim them together and stream the
+  // operand they share (Q / dO for dK/dV, K / V for dQ) at the same time, so more of it
+  // comes from L2 (GEM-like shape: dK/dV 720 -> 699 us; long-tail causal 1172 -> 1122 us).
+  // At d = 64 a tile is too short for the per-item cost (biased causal shape: dK/dV
+  // 344 -> 398 us), so those lists keep capped ranges, and so does the forward (grouped
+  // query-tile pairs: GEM-like forward 411 -> 447 us).
+  const bool grouped = (kind == kListDkv || kind == kListDq) && p.d == 128;
+  const long long range_cap =
+      (kind == kListFused || kind == kListNsp) ? (1ll << 62) : (grouped ? 1 : (share > 1 ? share : 1));
+  auto bucket = [](long long cost) { return cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1; };
 
   for (int c = tid; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
   __syncthreads();
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
-    for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int, int, long long cost) {
-      atomicAdd(&hist[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
-    });
+    if (grouped) {
+      long long gcost = 0;
+      int nr = 0;
+      for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int, int, long long cost) {
+        gcost += cost;
+        ++nr;
+      });
+      if (nr) atomicAdd(&hist[bucket(gcost)], p.H * nr);
+    } else {
+      for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap,
+                     [&](int, int, long long cost) { atomicAdd(&hist[bucket(cost)], p.H); });
+    }
   }
   __syncthreads();
   const int total = scan_desc(hist, base);
@@ -171,11 +191,30 @@ __device__ void emit_list(const PlanParams& p, int kind, WorkItem* items, int64_
     const int Lq = int(p.q_off[b + 1] - p.q_off[b]);
     const int Lk = int(p.kv_off[b + 1] - p.kv_off[b]);
     unsigned long long mx = 0;
-    for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int u0, int u1, long long cost) {
-      const int pos = atomicAdd(&base[cost < kCostBuckets - 1 ? int(cost) : kCostBuckets - 1], p.H);
-      for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u0, u1};
-      if ((unsigned long long)cost > mx) mx = (unsigned long long)cost;
-    });
+    if (grouped) {
+      long long gcost = 0;
+      int nr = 0;
+      for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int, int, long long cost) {
+        gcost += cost;
+        ++nr;
+      });
+      if (nr) {
+        // head h's tiles at pos + h * nr + r, in tile order
+        const int pos = atomicAdd(&base[bucket(gcost)], p.H * nr);
+        int r = 0;
+        for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int u0, int u1, long long cost) {
+          for (int h = 0; h < p.H; ++h) items[pos + h * nr + r] = WorkItem{b, h, u0, u1};
+          ++r;
+          if ((unsigned long long)cost > mx) mx = (unsigned long long)cost;
+        });
+      }
+    } else {
+      for_each_range(kind, Lq, Lk, causal, p.nsp_max_tiles, range_cap, [&](int u0, int u1, long long cost) {
+        const int pos = atomicAdd(&base[bucket(cost)], p.H);
+        for (int h = 0; h < p.H; ++h) items[pos + h] = WorkItem{b, h, u0, u1};
+        if ((unsigned long long)cost > mx) mx = (unsigned long long)cost;
+      });
+    }
     if (mx) atomicMax(&max_item, mx);
   }
   __syncthreads();
@@ -357,6 +396,7 @@ cudaError_t launch_plan(const Problem& pr, const PlanMaps& maps, void* ws, const
   p.backward = backward ? 1 : 0;
   p.grid = num_sms;
   p.nsp_max_tiles = pr.nsp_max_tiles;
+  p.d = pr.d;
   p.ws = static_cast<uint8_t*>(ws);
   p.L = L;
   p.bias = pr.bias_table;
