@@ -506,6 +506,8 @@ def measure_config(name, args, device, peaks, peak_src):
            "pct_of_tensor_peak": round(100 * value / peak_tf, 2), "fwd": fwd, "bwd": bwd,
            "valid_pairs": fl["pairs"], "roofline": roofline, "kernels": kernels,
            "gpu_launches": sum(c for _, c in per_kernel.values())}
+    if not args.no_extras and int(np.asarray(batch.q_lengths).max()) > SHORT_Q:
+        res["non_sequence_parallel"] = nsp_leg(step, batch, args.steps, stream, device)
     if not args.no_sdpa:
         del step
         torch.cuda.synchronize()
@@ -589,6 +591,9 @@ def run_jfa(args, rank, world, device):
     bias_grad = None
     if not args.no_extras and (batch.bias is not None or batch.jbias is not None):
         bias_grad = bias_grad_leg(step, batch, args.steps, stream)
+    nsp_cmp = None
+    if not args.no_extras and world == 1 and int(np.asarray(batch.q_lengths).max()) > SHORT_Q:
+        nsp_cmp = nsp_leg(step, batch, args.steps, stream, device)
     e2e = None
     if not args.no_extras:
         e2e_s = e2e_leg(step, batch, args, device, barrier)
@@ -601,7 +606,7 @@ def run_jfa(args, rank, world, device):
     if rank != 0:
         return None
     return finish(args, name, cfg, batch, step, fl, world, value, t_max_s, total_ms, fwd_ms, bwd_ms, per_kernel,
-                  peak_mem, launches, clk, graph_ms, bias_grad, e2e, device)
+                  peak_mem, launches, clk, graph_ms, bias_grad, e2e, device, nsp_cmp)
 
 
 def graph_replay(step, steps, stream, device):
@@ -662,6 +667,55 @@ def bias_grad_leg(step, batch, steps, stream):
             "bwd_ms": round(t_grad, 4), "bwd_ms_without": round(t_plain, 4),
             "overhead": round(t_grad / t_plain - 1, 4),
             "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in pk.items() if v[1]}}
+
+
+def nsp_leg(step, batch, steps, stream, device):
+    """Row N2 against the split passes on the same inputs: the backward timed with the
+    library's routing as it stands (by default every sequence of more than one query tile
+    takes the dK/dV + dQ passes) and again with sequences of 2 .. 16 query tiles sent to the
+    non-sequence-parallel pass, each with its per-kernel times and the share of query rows
+    that took each path.  The setting is restored afterwards."""
+    jfa = step.jfa
+    prev = jfa.jfa_nsp_max_tiles()
+    lq = np.asarray(batch.q_lengths)
+    rows = max(int(lq.sum()), 1)
+
+    def one(tiles):
+        jfa.jfa_set_nsp_max_tiles(tiles)
+        ws_keep = step.ws_b
+        b, c = batch, batch.cfg
+        step.ws_b = jfa.new_workspace(b.q_lengths.numel(), c.heads, c.head_dim, b.q.shape[0], b.k.shape[0], True,
+                                      device)
+        try:
+            for _ in range(3):
+                step.bwd()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(steps):
+                step.bwd()
+            e.record(stream)
+            torch.cuda.synchronize()
+            jfa.jfa_timing_read()
+            jfa.jfa_timing_enable(True)
+            step.bwd()
+            torch.cuda.synchronize()
+            jfa.jfa_timing_enable(False)
+            pk = jfa.jfa_timing_read()
+            step.check(f"in the backward with non-sequence-parallel tiles <= {tiles}")
+        finally:
+            step.ws_b = ws_keep
+        short, nsp, split = _split(batch, 128 * tiles if tiles > 1 else 0)
+        return {"nsp_max_tiles": tiles, "bwd_ms": round(a.elapsed_time(e) / steps, 4),
+                "kernels_ms": {k: round(v[0] / v[1], 4) for k, v in pk.items() if v[1]},
+                "query_rows": {"fused": round(float(lq[short].sum()) / rows, 4),
+                               "non_sequence_parallel": round(float(lq[nsp].sum()) / rows, 4),
+                               "split": round(float(lq[split].sum()) / rows, 4)}}
+
+    try:
+        return {"default": one(prev), "all_multi_tile_nsp": one(16)}
+    finally:
+        jfa.jfa_set_nsp_max_tiles(prev)
 
 
 def e2e_leg(step, batch, args, device, barrier):
@@ -734,7 +788,7 @@ def e2e_leg(step, batch, args, device, barrier):
 
 
 def finish(args, name, cfg, batch, step, fl, world, value, t_max_s, total_ms, fwd_ms, bwd_ms, per_kernel, peak_mem,
-           launches, clk, graph_ms, bias_grad, e2e, device):
+           launches, clk, graph_ms, bias_grad, e2e, device, nsp_cmp=None):
     """Rank 0: the roofline, the CPU baseline, the padded SDPA comparison and every other
     workload, then the JSON line."""
     peaks, peak_src = load_peaks()
@@ -785,6 +839,7 @@ def finish(args, name, cfg, batch, step, fl, world, value, t_max_s, total_ms, fw
             "ms_per_step": round(graph_ms, 4),
             "value": round((fl["fwd"] + fl["bwd"]) / (graph_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS"},
         "e2e": e2e, "gpu_launches": launches, "clocks": clk, "padded_sdpa": sdpa, "bias_grad": bias_grad,
+        "non_sequence_parallel": nsp_cmp,
         "peak_mem_extra_gb": round(peak_mem / 1e9, 3),
         "configs": others,
     }
