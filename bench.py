@@ -591,9 +591,6 @@ def run_jfa(args, rank, world, device):
     bias_grad = None
     if not args.no_extras and (batch.bias is not None or batch.jbias is not None):
         bias_grad = bias_grad_leg(step, batch, args.steps, stream)
-    nsp_cmp = None
-    if not args.no_extras and world == 1 and int(np.asarray(batch.q_lengths).max()) > SHORT_Q:
-        nsp_cmp = nsp_leg(step, batch, args.steps, stream, device)
     e2e = None
     if not args.no_extras:
         e2e_s = e2e_leg(step, batch, args, device, barrier)
@@ -602,6 +599,9 @@ def run_jfa(args, rank, world, device):
             torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
         e2e = {"value": round(total_flops / float(t_e2e.item()) / 1e12, 2), "unit": "TFLOPS",
                "h2d_bytes_per_step": e2e_s["h2d"], "d2h_bytes_per_step": e2e_s["d2h"]}
+    nsp_cmp = None
+    if not args.no_extras and world == 1 and int(np.asarray(batch.q_lengths).max()) > SHORT_Q:
+        nsp_cmp = nsp_leg(step, batch, args.steps, stream, device)
 
     if rank != 0:
         return None
@@ -716,6 +716,8 @@ def nsp_leg(step, batch, steps, stream, device):
         return {"default": one(prev), "all_multi_tile_nsp": one(16)}
     finally:
         jfa.jfa_set_nsp_max_tiles(prev)
+        step.bwd()  # the step's gradients as the default routing computes them again
+        torch.cuda.synchronize()
 
 
 def e2e_leg(step, batch, args, device, barrier):
