@@ -852,12 +852,13 @@ KERNEL_SOURCE = {"forward": "jfa_fwd.cu", "bwd_preprocess": "jfa_bwd.cu", "bwd_d
 
 
 def kernel_source_hash(kernel):
-    """Hash of the sources a kernel is compiled from (its translation unit and every shared
-    header); DRAM counters taken from other sources are stale."""
+    """Hash of the sources a kernel's DRAM traffic depends on: its translation unit, the
+    planner (which orders the work and so decides what is re-read from L2) and every shared
+    header; DRAM counters taken from other sources are stale."""
     import glob
     import hashlib
     csrc = os.path.join(ROOT, "jagged_attention_recsys_jfa_gb300", "csrc")
-    files = [os.path.join(csrc, KERNEL_SOURCE[kernel])]
+    files = [os.path.join(csrc, f) for f in sorted({KERNEL_SOURCE[kernel], "jfa_plan.cu"})]
     files += sorted(glob.glob(os.path.join(csrc, "*.cuh")) + glob.glob(os.path.join(csrc, "*.h")))
     h = hashlib.sha256()
     for f in files:
