@@ -189,7 +189,8 @@ jfa_status jfa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, jfa_s
  * the backward is not parallel over a sequence's query tiles); longer sequences take the
  * split passes (dK/dV per key tile, then dQ per query tile: seven GEMMs per tile pair, no
  * sum buffer).  max_tiles in 0 .. 16; below 2 every such sequence takes the split passes
- * (the default, which measured faster on GB300).  Both paths give the same results within
+ * (the default, which measured faster on GB300) and jfa_backward launches five kernels, not
+ * the pass's sixth.  Both paths give the same results within
  * rounding and are each deterministic.  With max_tiles >= 2 the backward workspace also
  * holds the fp32 dQ sums (4 * total_q * H * d more bytes): jfa_workspace_size reflects the
  * setting at the time it is called, and a workspace sized before the pass was enabled is

@@ -253,9 +253,11 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
   if (total_kv > 0 && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
                        !aligned16(dv)))
     return JFA_ERR_INVALID_ARG;
-  const WsLayout L = make_layout(B, H, d, total_q, total_kv, true, nsp_enabled());
-  if ((st = check_workspace(workspace, workspace_bytes, L)) != JFA_OK) return st;
+  // the non-sequence-parallel setting is read once (in pr) for the layout, the lists and the launches
   const Problem pr = make_problem(B, H, d, total_q, total_kv, q_offsets, kv_offsets, bias, scale, causal);
+  const bool nsp = pr.nsp_max_tiles >= 2;
+  const WsLayout L = make_layout(B, H, d, total_q, total_kv, true, nsp);
+  if ((st = check_workspace(workspace, workspace_bytes, L)) != JFA_OK) return st;
   const int nsm = sm_count();
   if (nsm <= 0) return JFA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -301,11 +303,11 @@ jfa_status jfa_backward(const void* dout, const void* q, const void* k, const vo
     KernelTimer t(JFA_KERNEL_BWD_FUSED, s);
     JFA_CHECK_LAUNCH(launch_bwd_fused(pr, lse, workspace, L, dq, dk, dv, nsm, s), "fused short-query launch");
   }
-  {
+  if (nsp) {  // otherwise its list is empty: no sequence is routed to the pass
     KernelTimer t(JFA_KERNEL_BWD_NSP, s);
     JFA_CHECK_LAUNCH(launch_bwd_nsp(pr, lse, workspace, L, dq, dk, dv, nsm, s), "non-sequence-parallel launch");
   }
-  g_last_launches = 6;
+  g_last_launches = nsp ? 6 : 5;
   return JFA_OK;
 }
 
