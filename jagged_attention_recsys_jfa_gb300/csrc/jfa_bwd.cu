@@ -1511,6 +1511,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdS64 = idesc_bf16_f32(128, 64, false, false);  // Lq <= 64: 64 query columns
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, false, true);  // A K-major, B MN-major
       constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, true, true);    // A (dS) and B (K) MN-major
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aR = smem_u32(sRing), aDS = smem_u32(sDS);
@@ -1522,13 +1523,14 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
         return true;
       };
       auto ra = [&](uint32_t n) { return aR + (n % R) * C::kTileBytes; };
-      // D(128 x 128) = A(128 x D) * B(128 x D)^T, both K-major (S^T, dP^T)
-      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
+      // D(128 x nq) = A(128 x D) * B(nq x D)^T, both K-major (S^T, dP^T; nq = 128, or 64 query
+      // columns when the sequence has at most 64 queries)
+      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t idesc) {
         const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
+          umma_ss(tmem + dcol, ad + o, bd + o, idesc, kk > 0);
         }
       };
       uint32_t item_k = 0;
@@ -1537,6 +1539,10 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
        const ItemMeta& wi = meta.e[item_k % kMetaSlots];
        if (wi.b < 0) break;  // end of this CTA's items
        const int Lq = wi.Lq, Lk = wi.Lk;
+       // at most 64 queries: S^T and dP^T with 64 query columns, dV and dK over K = 64
+       const bool half = Lq <= 64;
+       const uint32_t idS = half ? kIdS64 : kIdS;
+       const int kq = half ? 4 : kBM / 16;  // K-steps of dV and dK
        if (any_visible(wi.u0, wi.u1, Lq, Lk)) {
         if (!wait(&q_full, item_n & 1)) { ok = false; break; }
         if (!wait(&dq_empty, (item_n & 1) ^ 1)) { ok = false; break; }
@@ -1548,12 +1554,12 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
           ring_n += 2;
           // S^T = K Q^T
           if (!wait(&ring_full[nk % R], (nk / R) & 1)) { ok = false; break; }
-          mma_nt(C::kColS, ra(nk), aQ);
+          mma_nt(C::kColS, ra(nk), aQ, idS);
           umma_commit(&st_full);
           trace_event(p.trace, kTraceMma, tn, 13);
           // dP^T = V dO^T, into the columns dK of the previous tile is read from
           if (!wait(&dk_empty, (g & 1) ^ 1) || !wait(&ring_full[nv % R], (nv / R) & 1)) { ok = false; break; }
-          mma_nt(C::kColP, ra(nv), aDO);
+          mma_nt(C::kColP, ra(nv), aDO, idS);
           umma_commit(&dpt_full);
           umma_commit(&ring_empty[nv % R]);  // V is read by dP^T only
           trace_event(p.trace, kTraceMma, tn, 14);
@@ -1562,19 +1568,21 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
           {
             const uint64_t bd = sdesc_sw128(aDO, 16384, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kBM / 16; ++kk)
+            for (int kk = 0; kk < kBM / 16 && kk < kq; ++kk)
               umma_ts(tmem + C::kColFdV, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                       bd + uint32_t(kk * 2048 >> 4), kIdAcc, kk > 0 ? 1u : 0u);
           }
           umma_commit(&dv_full);
           trace_event(p.trace, kTraceMma, tn, 11);
           // dK = dS^T Q (dS^T staged in shared memory, K-major over queries), into the
-          // dP^T columns; then dQ += dS K (the same staging read as an MN-major A)
+          // dP^T columns; then dQ += dS K (the same staging read as an MN-major A; with at
+          // most 64 queries its rows 64..127 read the second atom's stale values and are
+          // never stored)
           if (!wait(&ds_full, g & 1)) { ok = false; break; }
           {
             const uint64_t ad = sdesc_sw128(aDS, 16, 1024), bd = sdesc_sw128(aQ, 16384, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kBM / 16; ++kk) {
+            for (int kk = 0; kk < kBM / 16 && kk < kq; ++kk) {
               const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
               umma_ss(tmem + C::kColP, ad + o, bd + uint32_t(kk * 2048 >> 4), kIdAcc, kk > 0 ? 1u : 0u);
             }
@@ -1641,6 +1649,21 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) fused_kernel(const BwdParams 
       const int j = kt * kBN + row;  // local key index
       const bool valid = j < Lk;
       if (!visible(kt, Lq, Lk)) continue;  // zero dK / dV rows: written by the epilogue warpgroup
+      if (Lq <= 64 && w == 1) {
+        // every query is in warpgroup 0's columns (the MMAs run 64 query columns wide):
+        // only the hand-offs, so that each barrier phase still sees both warpgroups once
+        if (!mbar_wait(&st_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        tc_fence_before();
+        mbar_arrive(&p_full);
+        if (!mbar_wait(&dpt_full, g & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        if (!mbar_wait(&dsm_empty, (g & 1) ^ 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        tc_fence_after();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
+        ++g;
+        continue;
+      }
       uint4 jbw[8];  // general bias for this tile (row order), loaded before the wait
       if (kJBias) {
         const int64_t pitch = (Lk + 7) / 8 * 8;  // rows of the sequence's block: bias[i][j] at i * pitch + j
