@@ -598,7 +598,9 @@ def run_jfa(args, rank, world, device):
         if world > 1:
             torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
         e2e = {"value": round(total_flops / float(t_e2e.item()) / 1e12, 2), "unit": "TFLOPS",
-               "h2d_bytes_per_step": e2e_s["h2d"], "d2h_bytes_per_step": e2e_s["d2h"]}
+               "h2d_bytes_per_step": e2e_s["h2d"], "d2h_bytes_per_step": e2e_s["d2h"],
+               # both directions' bytes per second: what the host link carried
+               "host_link_gbs": round((e2e_s["h2d"] + e2e_s["d2h"]) * args.steps / float(t_e2e.item()) / 1e9, 1)}
     nsp_cmp = None
     if not args.no_extras and world == 1 and int(np.asarray(batch.q_lengths).max()) > SHORT_Q:
         nsp_cmp = nsp_leg(step, batch, args.steps, stream, device)
