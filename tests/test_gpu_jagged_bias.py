@@ -24,6 +24,8 @@ CASES = {
     "mixed_causal_d128": (2, 128, [0, 5, 140, 7, 400, 90], [3, 0, 140, 9, 260, 300], True),
     # last tiles reaching past the tensors' ends (tail maps)
     "tails_causal_d64": (3, 64, [129, 3, 0], [131, 0, 2], True),
+    # both sides of the fused pass's half-width limit (64 queries), causal, d = 64
+    "half_width_causal_d64": (3, 64, [64, 65, 20, 1], [64, 200, 300, 70], True),
 }
 
 

@@ -53,6 +53,11 @@ EDGE = {
     "causal_lq_gt_lk": (dict(heads=2, head_dim=128), [300, 64, 129], [40, 1, 128], True, False),
     "causal_lq_lt_lk": (dict(heads=2, head_dim=64), [40, 1, 128], [300, 64, 129], True, False),
     "cross_noncausal_bias": (dict(heads=2, head_dim=128), [33, 1, 200], [500, 2, 129], False, True),
+    # the fused pass runs sequences of at most 64 queries half width: both sides of 64
+    "half_width_boundary_bias_d128": (dict(heads=2, head_dim=128), [63, 64, 65, 1, 96], [300, 64, 65, 200, 129],
+                                      False, True),
+    "half_width_boundary_causal_d64": (dict(heads=3, head_dim=64), [64, 65, 10, 64, 128], [64, 65, 300, 20, 130],
+                                       True, False),
     # last tiles of several sequences reach past the tensor's last row (tail maps): the
     # clipped rows of an earlier sequence's box hold a later sequence's keys, which must
     # still arrive as zeros; totals below one tile; trailing empty sequences
