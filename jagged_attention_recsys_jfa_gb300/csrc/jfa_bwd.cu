@@ -22,8 +22,9 @@
 // split the 128 columns of each S/dP tile (64 each); warpgroup 3 is the epilogue, which
 // drains the finished accumulators from TMEM and writes the gradient rows while the
 // compute warpgroups start the next tile.  TMEM: S [0,128), dP [128,256), two d-column
-// accumulators from 256.  P and dS are written back as bf16 over the S / dP columns the
-// warpgroup owns and feed the accumulating MMAs straight from TMEM.
+// accumulators from 256.  P and dS are written back as bf16 (over the S / dP columns the
+// warpgroup owns at d = 128, in the free columns from 384 at d = 64 in the dK/dV pass) and
+// feed the accumulating MMAs straight from TMEM.
 #include <cuda_bf16.h>
 
 #include "jfa_internal.h"
@@ -253,6 +254,12 @@ struct BwdCfg {
   // dK/dV pass: S^T, dP^T, dK, dV.   dQ pass: S, dP (two buffers), dQ.
   static constexpr uint32_t kColS = 0, kColP = 128, kColA0 = 256, kColA1 = 256 + D;
   static constexpr uint32_t kColP1 = 256, kColDQ = 384;
+  // dK/dV pass: P^T and dS^T (bf16, keys x 128 queries, each compute warpgroup's 64 queries
+  // in 32 columns) over S^T / dP^T at d = 128, two 64-column halves apart; at d = 64 in the
+  // spare columns [384, 448) and [448, 512), so the next S^T / dP^T MMA does not write the
+  // columns the previous dV / dK MMA is still reading
+  static constexpr uint32_t kColPT = D == 64 ? 384 : kColS, kColDST = D == 64 ? 448 : kColP;
+  static constexpr uint32_t kXHalf = D == 64 ? 32 : 64;
   static constexpr int kSmemDkdv = 2 * kTileBytes + kRingDkdv * kTileBytes + kVecSlots * 1024 + 1024;
   static constexpr int kSmemDq = 2 * kTileBytes + kRingDq * kTileBytes + 1024;
   // Fused short-query pass: Q and dO resident, K/V ring, dS^T staging (keys x 128 queries,
@@ -644,13 +651,13 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
           umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
         }
       };
-      // acc(keys x D) += X^T (TMEM bf16, keys x 128 queries, two 64-column halves) * B(queries x D, MN-major)
+      // acc(keys x D) += X^T (TMEM bf16, keys x 128 queries, two halves kXHalf columns apart) * B(queries x D, MN-major)
       auto mma_acc = [&](uint32_t dcol, uint32_t xcol, uint32_t b, bool acc) {
         const uint64_t bd = sdesc_sw128(b, 16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * 64 + (kk & 3) * 8, bd + uint32_t(kk * 2048 >> 4), kIdAcc,
-                  (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + dcol, tmem + xcol + (kk >> 2) * C::kXHalf + (kk & 3) * 8, bd + uint32_t(kk * 2048 >> 4),
+                  kIdAcc, (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t item_k = 0;
       for (; ok; ++item_k) {
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
           if (!wait(&p_full, tile_n & 1)) { ok = false; break; }
           trace_event(p.trace, kTraceMma, tn, 11);
           if (i == 0 && !wait(&dv_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
-          mma_acc(C::kColA1, C::kColS, ra(nd), i > 0);  // dV += P^T dO
+          mma_acc(C::kColA1, C::kColPT, ra(nd), i > 0);  // dV += P^T dO
           umma_commit(&ring_empty[nd % R]);
           if (i + 1 == count) umma_commit(&dv_full);
           trace_event(p.trace, kTraceMma, tn, 12);
@@ -694,7 +701,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
           trace_event(p.trace, kTraceMma, tn, 14);
           ++tile_n;
           if (i == 0 && !wait(&dk_empty, (acc_n & 1) ^ 1)) { ok = false; break; }
-          mma_acc(C::kColA0, C::kColP, ra(nq), i > 0);  // dK += dS^T Q
+          mma_acc(C::kColA0, C::kColDST, ra(nq), i > 0);  // dK += dS^T Q
           umma_commit(&ring_empty[nq % R]);
           trace_event(p.trace, kTraceMma, tn, 15);
           if (i + 1 < count) {
@@ -730,6 +737,8 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const uint32_t tP = tmem + lane_addr + C::kColP + 64 * w;
+    const uint32_t tPT = tmem + lane_addr + C::kColPT + C::kXHalf * w;    // P^T, bf16
+    const uint32_t tDST = tmem + lane_addr + C::kColDST + C::kXHalf * w;  // dS^T, bf16
     const float sl2 = p.scale_log2;
     uint32_t ring_n = 0, tile_n = 0, qtile_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
@@ -819,7 +828,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         }
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c]);  // P^T
-        st_bf16_64(tS, x);
+        st_bf16_64(tPT, x);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full);
@@ -834,7 +843,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dkdv_kernel(const BwdParams p
         for (int c2 = 0; c2 < 32; ++c2)  // dS^T = P^T o (dP^T - D)
           f2_unpack(f2_mul(f2_pack(x[2 * c2], x[2 * c2 + 1]), f2_add(f2_pack(dp[2 * c2], dp[2 * c2 + 1]), ndvec[c2])),
                     dp[2 * c2], dp[2 * c2 + 1]);
-        st_bf16_64(tP, dp);
+        st_bf16_64(tDST, dp);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&ds_full);
