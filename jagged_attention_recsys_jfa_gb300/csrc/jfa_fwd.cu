@@ -20,7 +20,8 @@
 //   warps 4-7   softmax for query tile 0 of the pair (one TMEM lane = one query row)
 //   warps 8-11  softmax for query tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d, 256+2d).
-// P (bf16, two per column) overwrites the first 64 columns of its S region.
+// P (bf16, two per column) overwrites the first 64 columns of its S region.  At d = 64 the
+// query tiles are copied into Q_0 [384,416), Q_1 [416,448) and feed the S MMAs from TMEM.
 // The issue order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) lets one tile's softmax
 // overlap the other tile's MMAs (ping-pong).  The running max is only raised (and O
 // rescaled) when it grows by more than 2^8, which keeps exp2 arguments <= 8 in between.
@@ -70,6 +71,12 @@ struct FwdCfg {
   static constexpr int kSmemBytes = 2 * kTileBytes + kStages * kTileBytes + 1024;
   static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA (dynamic + static barriers)");
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // d = 64: each query tile is also copied into TMEM ([384,416), [416,448)) by its softmax
+  // warpgroup and read from there as the A operand of its S MMAs, so the shared-memory
+  // pair buffer is free again as soon as both copies are done and the next unit's pair
+  // loads a whole unit ahead
+  static constexpr bool kQTmem = D == 64;
+  static constexpr uint32_t kColQ0 = 384, kColQ1 = 416;
 };
 
 struct ItemInfo {
@@ -120,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
 
   __shared__ uint64_t q_full, q_empty, mma_done;
   __shared__ uint64_t kv_full[C::kStages], kv_empty[C::kStages];
-  __shared__ uint64_t s_full[2], p_full[2], o_full[2];
+  __shared__ uint64_t s_full[2], p_full[2], o_full[2], qt_full[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ MetaRing meta;
@@ -129,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
   if (threadIdx.x == 0) {
     abort_sh = 0;
     mbar_init(&q_full, 1);
-    mbar_init(&q_empty, 1);
+    mbar_init(&q_empty, C::kQTmem ? 256 : 1);  // both softmax warpgroups, else the last S MMA
     mbar_init(&mma_done, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -139,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 128);
       mbar_init(&o_full[s], 1);
+      mbar_init(&qt_full[s], 128);
     }
     meta_init(meta, p.wait_ns);
     fence_mbar_init();
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
       auto mma_commit = [&](uint64_t* bar) {
         if (elect_one()) umma_commit(bar);
       };
-      uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0}, tn = 0;
+      uint32_t ring_n = 0, item_n = 0, p_n[2] = {0, 0}, qt_n[2] = {0, 0}, tn = 0;
       bool ok = true;
       uint32_t k = 0;
       for (; ok; ++k) {
@@ -310,9 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         const ItemInfo it = decode(p, wi, u);
         if (it.njt == 0) continue;
         const int nkv[2] = {it.nkv0, it.nkv1};
-        if (!__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs))) { ok = false; break; }
-        ++item_n;
-        tc_fence_after();
+        if (!C::kQTmem) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&q_full, item_n & 1, abort_flag, kWaitTimeoutNs))) { ok = false; break; }
+          ++item_n;
+          tc_fence_after();
+        }
         if (lane == 0) trace_event(p.trace, kTraceMma, tn, 10);
         int s_left = it.nkv0 + it.nkv1;
         auto issue_S = [&](int s, uint32_t e) {
@@ -323,12 +333,24 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-              umma_ss(tmem + colS[s], qd + o, kd + o, kIdS, kk > 0);
+              if (C::kQTmem)
+                umma_ts(tmem + colS[s], tmem + (s ? C::kColQ1 : C::kColQ0) + kk * 8, kd + o, kIdS, kk > 0);
+              else
+                umma_ss(tmem + colS[s], qd + o, kd + o, kIdS, kk > 0);
             }
           }
           mma_commit(&s_full[s]);
           if (lane == 0) trace_event(p.trace, kTraceMma, tn, 16 + s);
-          if (--s_left == 0) mma_commit(&q_empty);
+          if (--s_left == 0 && !C::kQTmem) mma_commit(&q_empty);
+        };
+        // a tile's first S reads Q from TMEM once its softmax warpgroup has copied it there
+        auto wait_qt = [&](int s) -> bool {
+          if (!C::kQTmem) return true;
+          const bool r =
+              __all_sync(0xffffffffu, mbar_wait(&qt_full[s], qt_n[s] & 1, abort_flag, kWaitTimeoutNs));
+          ++qt_n[s];
+          tc_fence_after();
+          return r;
         };
         auto issue_PV = [&](int s, uint32_t e, bool acc) {
           const uint64_t vd = sdesc_sw128(sR_addr + e * C::kTileBytes, 16384, 1024);
@@ -347,8 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
         };
         const uint32_t n0 = ring_n;  // K_j at n0 + 2j, V_j at n0 + 2j + 1
         if (!wait_full(n0)) { ok = false; break; }
-        if (it.nkv0 > 0) issue_S(0, n0 % C::kStages);
-        if (it.nkv1 > 0) issue_S(1, n0 % C::kStages);
+        if (it.nkv0 > 0) {
+          if (!wait_qt(0)) { ok = false; break; }
+          issue_S(0, n0 % C::kStages);
+        }
+        if (it.nkv1 > 0) {
+          if (!wait_qt(1)) { ok = false; break; }
+          issue_S(1, n0 % C::kStages);
+        }
         mma_commit(&kv_empty[n0 % C::kStages]);
         for (int j = 0; j < it.njt && ok; ++j) {
           const uint32_t nv = n0 + 2 * j + 1, nk = n0 + 2 * j + 2;
@@ -401,8 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + (s ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_addr + (s ? C::kColO1 : C::kColO0);
+    const uint32_t tQ = tmem + lane_addr + (s ? C::kColQ1 : C::kColQ0);
     const float sl2 = p.scale_log2;
-    uint32_t s_n = 0, o_n = 0, tn = 0;
+    uint32_t s_n = 0, o_n = 0, q_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;  // records this warpgroup's trace
     bool ok = true;
     uint32_t k = 0;
@@ -413,8 +442,33 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
      for (int u = wi.u0; u < wi.u1 && ok; ++u) {
       const ItemInfo it = decode(p, wi, u);
       const int t = s ? it.t1 : it.t0;
-      if (t * kBM >= it.Lq) continue;
       const int nkv = s ? it.nkv1 : it.nkv0;
+      if (C::kQTmem && it.njt > 0) {
+        // every unit the Q loader fills: wait for the pair (so that neither warpgroup frees a
+        // later unit's buffer early), copy this tile's rows into TMEM if its S MMAs run, free
+        // the buffer.  Row `row` of the 128-byte-swizzled tile: 16-byte chunk c at chunk
+        // position c ^ (row & 7).
+        if (!mbar_wait(&q_full, q_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++q_n;
+        if (nkv > 0) {
+          const uint4* qrow = reinterpret_cast<const uint4*>(sQ + s * C::kTileBytes + row * 128);
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = qrow[c ^ (row & 7)];
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+          tmem_st32(tQ, w);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&qt_full[s]);
+        }
+        mbar_arrive(&q_empty);
+      }
+      if (t * kBM >= it.Lq) continue;
       const int i = t * kBM + row;  // local query index
       const bool valid_row = i < it.Lq;
       __nv_bfloat16* orow = p.out + ((it.qo + i) * p.H + it.h) * int64_t(D);
