@@ -260,6 +260,11 @@ struct BwdCfg {
   // columns the previous dV / dK MMA is still reading
   static constexpr uint32_t kColPT = D == 64 ? 384 : kColS, kColDST = D == 64 ? 448 : kColP;
   static constexpr uint32_t kXHalf = D == 64 ? 32 : 64;
+  // dQ pass at d = 64: the query tile's Q and dO rows copied into the free columns
+  // [448, 480) and [480, 512) by the compute warpgroups feed the S and dP MMAs from TMEM, and
+  // the shared-memory buffers are free for the next query tile once both copies are done
+  static constexpr bool kDqQTmem = D == 64;
+  static constexpr uint32_t kColDqQ = 448, kColDqDO = 480;
   static constexpr int kSmemDkdv = 2 * kTileBytes + kRingDkdv * kTileBytes + kVecSlots * 1024 + 1024;
   static constexpr int kSmemDq = 2 * kTileBytes + kRingDq * kTileBytes + 1024;
   // Fused short-query pass: Q and dO resident, K/V ring, dS^T staging (keys x 128 queries,
@@ -942,7 +947,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
   uint8_t* sDO = smem + C::kTileBytes;
   uint8_t* sRing = smem + 2 * C::kTileBytes;
 
-  __shared__ uint64_t qdo_full, qdo_empty, s_full, s_free, acc_full, acc_empty, mma_done;
+  __shared__ uint64_t qdo_full, qdo_empty, qt_full, s_full, s_free, acc_full, acc_empty, mma_done;
   // dp_full / ds_full of global tile g live at index g & 1: dP(g+1) is issued before dQ(g)
   // waits for dS(g), so one warpgroup may finish tile g+1 while the other still works on
   // tile g (never further: S(g+2) waits for both warpgroups' s_free(g+1)); separate
@@ -958,7 +963,8 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
   if (threadIdx.x == 0) {
     abort_sh = 0;
     mbar_init(&qdo_full, 1);
-    mbar_init(&qdo_empty, 1);
+    mbar_init(&qdo_empty, C::kDqQTmem ? 256 : 1);  // both compute warpgroups, else the last dP MMA
+    mbar_init(&qt_full, 256);
     mbar_init(&s_full, 1);
     mbar_init(&s_free, 256);
     mbar_init(&dp_full[0], 1);
@@ -1110,12 +1116,16 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       };
       auto wait_ring = [&](uint32_t n) { return wait(&ring_full[n % R], (n / R) & 1); };
       auto ra = [&](uint32_t n) { return aR + (n % R) * C::kTileBytes; };
-      auto mma_nt = [&](uint32_t dcol, uint32_t a, uint32_t b) {
-        const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
+      // S (dp = false: Q K^T) or dP (dp = true: dO V^T) of a query tile and the key tile at b
+      auto mma_nt = [&](uint32_t dcol, bool dp, uint32_t b) {
+        const uint64_t ad = sdesc_sw128(dp ? aDO : aQ, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
+          if (C::kDqQTmem)
+            umma_ts(tmem + dcol, tmem + (dp ? C::kColDqDO : C::kColDqQ) + kk * 8, bd + o, kIdS, kk > 0);
+          else
+            umma_ss(tmem + dcol, ad + o, bd + o, kIdS, kk > 0);
         }
       };
       uint32_t item_k = 0;
@@ -1127,20 +1137,21 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
        for (int qt = wi.u0; qt < wi.u1 && ok; ++qt) {
         const int nkv = kv_tiles_for_q_tile(qt, Lq, Lk, causal);
         if (nkv == 0) continue;
-        if (!wait(&qdo_full, item_n & 1)) { ok = false; break; }
+        if (!wait(C::kDqQTmem ? &qt_full : &qdo_full, item_n & 1)) { ok = false; break; }
         ++item_n;
         trace_event(p.trace, kTraceMma, tn, 10);
         const uint32_t n0 = ring_n;  // V_j at n0 + 2j, K_j at n0 + 2j + 1
         if (!wait_ring(n0 + 1)) { ok = false; break; }
-        mma_nt(C::kColS, aQ, ra(n0 + 1));
+        mma_nt(C::kColS, false, ra(n0 + 1));
         umma_commit(&s_full);
         if (!wait_ring(n0)) { ok = false; break; }
-        mma_nt(colP(tile_n), aDO, ra(n0));
+        mma_nt(colP(tile_n), true, ra(n0));
         umma_commit(&dp_full[tile_n & 1]);
         umma_commit(&ring_empty[n0 % R]);
         // Q and dO are read only by S and dP: once the last dP is issued the loader may
-        // bring in the next query tile while dQ of this one still runs
-        if (nkv == 1) umma_commit(&qdo_empty);
+        // bring in the next query tile while dQ of this one still runs (at d = 64 the compute
+        // warpgroups free them after copying them into TMEM)
+        if (nkv == 1 && !C::kDqQTmem) umma_commit(&qdo_empty);
         for (int jt = 0; jt < nkv && ok; ++jt) {
           const uint32_t g = tile_n;  // global tile index
           const uint32_t nv = n0 + 2 * jt, nk = nv + 1;
@@ -1150,14 +1161,14 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
             if (!wait(&s_free, g & 1)) { ok = false; break; }
             trace_event(p.trace, kTraceMma, tn, 11);
             if (!wait_ring(nk + 2)) { ok = false; break; }
-            mma_nt(C::kColS, aQ, ra(nk + 2));
+            mma_nt(C::kColS, false, ra(nk + 2));
             umma_commit(&s_full);
             trace_event(p.trace, kTraceMma, tn, 12);
             if (!wait_ring(nv + 2)) { ok = false; break; }
-            mma_nt(colP(g + 1), aDO, ra(nv + 2));
+            mma_nt(colP(g + 1), true, ra(nv + 2));
             umma_commit(&dp_full[(g + 1) & 1]);
             umma_commit(&ring_empty[(nv + 2) % R]);
-            if (jt + 2 == nkv) umma_commit(&qdo_empty);
+            if (jt + 2 == nkv && !C::kDqQTmem) umma_commit(&qdo_empty);
             trace_event(p.trace, kTraceMma, tn, 13);
           }
           if (!wait(&ds_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
@@ -1199,7 +1210,7 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS + 64 * w;
     const float sl2 = p.scale_log2;
-    uint32_t tile_n = 0, tn = 0;
+    uint32_t tile_n = 0, q_n = 0, tn = 0;
     const bool leader = (warp & 3) == 0 && lane == 0;
     bool ok = true;
     uint32_t item_k = 0;
@@ -1214,6 +1225,27 @@ __global__ void __launch_bounds__(kThreadsDkdv, 1) dq_kernel(const BwdParams p) 
       const int i = qt * kBM + row;
       const bool valid = i < Lq;
       if (nkv == 0) continue;  // rows of zeros: written by the epilogue warpgroup
+      if (C::kDqQTmem) {
+        // this query tile's rows into TMEM: warpgroup 0 copies Q, warpgroup 1 dO (row `row`
+        // of a 128-byte-swizzled tile: 16-byte chunk c at chunk position c ^ (row & 7))
+        if (!mbar_wait(&qdo_full, q_n & 1, abort_flag, kWaitTimeoutNs)) { ok = false; break; }
+        ++q_n;
+        const uint4* src = reinterpret_cast<const uint4*>((w ? sDO : sQ) + row * 128);
+        uint32_t cw[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = src[c ^ (row & 7)];
+          cw[4 * c] = v.x;
+          cw[4 * c + 1] = v.y;
+          cw[4 * c + 2] = v.z;
+          cw[4 * c + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_addr + (w ? C::kColDqDO : C::kColDqQ), cw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&qt_full);
+        mbar_arrive(&qdo_empty);
+      }
       // padded per-query vectors (stored negated): 0 past the sequence end, -inf for rows
       // that see no key
       const float nl2 = __ldg(p.lse2 + vec0 + i);
