@@ -66,6 +66,11 @@ EDGE = {
     "tail_crossing_causal_bias_d64": (dict(heads=3, head_dim=64), [129, 3, 0], [131, 0, 2], True, True),
     # token rows wider than one 128-chunk pass of the row-parallel preprocess (12 heads)
     "many_heads_d128": (dict(heads=12, head_dim=128), [300, 5, 129], [260, 9, 129], False, False),
+    # d = 64 non-causal (query tiles read from TMEM by the forward's and the dQ pass's
+    # MMAs): odd tile counts (a unit without its second tile), sequences without keys
+    # beside ones with several key tiles, unequal lengths
+    "boundaries_d64": (dict(heads=2, head_dim=64), [1, 129, 256, 257, 385, 640], None, False, False),
+    "no_keys_d64_bias": (dict(heads=3, head_dim=64), [300, 129, 5, 260], [0, 64, 0, 700], False, True),
     # one long sequence with many tiles
     "long_single_d128": (dict(heads=1, head_dim=128), [1500], None, False, False),
     "long_single_causal_d64": (dict(heads=2, head_dim=64), [1100], None, True, True),
