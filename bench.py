@@ -166,13 +166,17 @@ def config_dict(cfg, name):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampled every ~10 ms with timestamps; `window(t0, t1)` marks the timed
+    region (host wall-clock seconds), and the report is taken from the samples inside it
+    (all samples when none fell inside, which it then says)."""
+    QUERY = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index):
         self.path = tempfile.mktemp(prefix="jfa_clocks_", suffix=".csv")
         self.proc = None
+        self.t0 = self.t1 = None
         try:
             self.uuid = str(getattr(torch.cuda.get_device_properties(device_index), "uuid", ""))
         except Exception:
@@ -182,9 +186,52 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader",
-                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "10"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    @staticmethod
+    def parse(lines, uuid="", t0=None, t1=None):
+        """Summarise nvidia-smi CSV lines (the QUERY fields, no header)."""
+        import datetime
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 11:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, parts[1:]))
+        if uuid:
+            mine = [r for r in rows if uuid.replace("GPU-", "") in r[1][1]]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        idx0 = rows[0][1][0]
+        rows = [r for r in rows if r[1][0] == idx0]
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        use = [r[1] for r in (inside or rows)]
+
+        def num(x):
+            try:
+                return float(x.split()[0])
+            except Exception:
+                return None
+        sm = [num(r[2]) for r in use if num(r[2]) is not None]
+        mx = [num(r[3]) for r in use if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in use for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        loaded = sm if inside else ([x for x in sm if mx and x >= 0.5 * max(mx)] or sm)
+        out = {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": reasons, "samples": len(inside), "samples_total": len(rows)}
+        if not inside:
+            out["note"] = "no sample fell inside the timed region: figures from all samples of the run"
+        return out
 
     def stop(self):
         if self.proc is None:
@@ -195,33 +242,10 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            rows.append(parts)
+        with open(self.path) as f:
+            lines = f.readlines()
         os.unlink(self.path)
-        if self.uuid:
-            mine = [r for r in rows if self.uuid.replace("GPU-", "") in r[1]]
-            rows = mine or rows
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        idx0 = rows[0][0]
-        rows = [r for r in rows if r[0] == idx0]
-
-        def num(s):
-            try:
-                return float(s.split()[0])
-            except Exception:
-                return None
-        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
-        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
-        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        return self.parse(lines, self.uuid, self.t0, self.t1)
 
 
 # ----------------------------------------------------------------------------- CPU oracle leg
@@ -562,11 +586,15 @@ def run_jfa(args, rank, world, device):
     # the timed region: K whole steps, nothing recorded between the kernels
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    host_t0 = time.time()  # the stream is idle: the GPU starts the region now
     t_start.record(stream)
     for i in range(args.steps):
         step()
     t_end.record(stream)
     torch.cuda.synchronize()
+    host_t1 = time.time()
+    clocks.window(host_t0, host_t1)
+    time.sleep(0.05)  # let the sampler flush the region's last samples
     barrier()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)

@@ -81,3 +81,27 @@ def test_general_bias_bytes_counted_once_per_pass():
     assert w1["bwd_nsp"] - w0["bwd_nsp"] == pytest.approx(blocks[nsp].sum())
     assert w1["bwd_fused"] - w0["bwd_fused"] == pytest.approx(blocks[lq <= 128].sum())
     assert jb.jbias.numel() == (lq * ((lk + 7) // 8 * 8)).sum() * H
+
+
+def test_clock_report_uses_samples_inside_the_timed_region():
+    """The clocks object summarises the nvidia-smi samples whose timestamps fall inside the
+    timed region, keeps throttle reasons seen there, and says when none fell inside."""
+    import datetime
+
+    b = _bench()
+    t = 1_800_000_000.0
+
+    def line(dt, mhz, power_cap="Not Active", uuid="GPU-aa11"):
+        ts = datetime.datetime.fromtimestamp(t + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (f"{ts}, 0, {uuid}, {mhz} MHz, 2070 MHz, 900.00 W, 0x0, Not Active, Not Active, "
+                f"Not Active, {power_cap}")
+
+    lines = [line(-0.30, 900), line(0.011, 2070), line(0.022, 2040, "Active"), line(0.033, 2055),
+             line(0.25, 1200), line(0.02, 1000, uuid="GPU-other")]
+    rep = b.ClockSampler.parse(lines, "GPU-aa11", t, t + 0.036)
+    assert rep["samples"] == 3 and rep["samples_total"] == 5
+    assert rep["sm_mhz"] == 2055.0 and rep["sm_max_mhz"] == 2070.0
+    assert rep["reasons"] == ["sw_power_cap"] and "note" not in rep
+    none = b.ClockSampler.parse(lines, "GPU-aa11", t + 10, t + 11)
+    assert none["samples"] == 0 and "note" in none
+    assert b.ClockSampler.parse([], "GPU-aa11", t, t + 1)["reasons"] == ["no samples"]
