@@ -49,6 +49,8 @@ CASES = {
     # a small table: most pairs clamp onto the two edge buckets, in both passes
     "clamped_d64": (3, 64, [300, 40, 129, 1], [280, 700, 129, 5], False, 64, 20),
     "clamped_causal_d128": (2, 128, [513, 77], [513, 200], True, 33, 16),
+    # the largest table the library takes (8192 buckets), off-centre so both ends are used
+    "max_table_d64": (2, 64, [700, 129, 1, 260], [1500, 64, 300, 9], False, 8192, 1000),
 }
 
 
