@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const FwdParams p) {
    setmaxnreg_dec<kRegsLoad>();
    if (warp == 2) {
     // ------------------------------------------------------------ Q loader
-    // Its own warp, so the next pair's Q load starts the moment the last S MMA of the
-    // current pair frees the buffer, whatever the K/V producer is waiting on.
+    // Its own warp, so the next pair's Q load starts the moment the buffer is free (after
+    // the current pair's last S MMA; at d = 64 once both softmax warpgroups have copied
+    // their tiles into TMEM), whatever the K/V producer is waiting on.
     if (lane == 0) {
       uint32_t item_n = 0, tn = 0;
       bool ok = true;
