@@ -2485,15 +2485,6 @@ BwdParams make_params(const Problem& pr, const float* lse, void* ws, const WsLay
   return bp;
 }
 
-template <typename K>
-cudaError_t launch_big(K kern, int smem, int grid, const BwdParams& bp, cudaStream_t stream) {
-  cudaError_t e = check_launch_registers(kern);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, bp);
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const Problem& pr, const void* dout, const void* out, const float* lse,
